@@ -1,0 +1,66 @@
+"""Plant one plausible mistake at a time in a copy of the oracle's C source,
+build it, and check that at least one pin fails.  This is what makes the pins
+worth trusting: a dropped term, a wrong sign or index, a transposed operand
+or a wrong rounding rule anywhere in the oracle does not go unnoticed.
+CPU only; the real oracle is never modified."""
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+# (name, text in moe_oracle.c, replacement)
+MUTANTS = [
+    ("gate_up_swapped", "a[j] = silu(g) * u;", "a[j] = silu(u) * g;"),
+    ("silu_dropped", "a[j] = silu(g) * u;", "a[j] = g * u;"),
+    ("silu_sign", "return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
+    ("sigmoid_not_silu", "return g / (1.0 + exp(-g));", "return 1.0 / (1.0 + exp(-g));"),
+    ("routing_weight_dropped", "o[c] += w * y[c];", "o[c] += y[c];"),
+    ("slot_index_k_dropped", "int e = ids[(size_t)t * p->K + k];",
+     "int e = ids[(size_t)t * p->K];"),
+    ("weight_index_wrong", "double w = (double)topk_w[(size_t)t * p->K + k];",
+     "double w = (double)topk_w[(size_t)k];"),
+    ("down_proj_wrong_expert", "expert_out(p, w2, w2_scale, e, a, y, wrow);\n            for (int c = 0; c < p->H; ++c) o[c]",
+     "expert_out(p, w2, w2_scale, 0, a, y, wrow);\n            for (int c = 0; c < p->H; ++c) o[c]"),
+    ("up_row_offset_wrong", "e, p->I + j, wrow);", "e, j + 1 < p->I ? j + 1 : j, wrow);"),
+    ("bf16_decode_shift", "((uint32_t)b) << 16", "((uint32_t)b) << 15"),
+    ("e2m1_exponent_bias", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e)"),
+    ("e8m0_bias", "ldexp(1.0, (int)v - 127)", "ldexp(1.0, (int)v - 128)"),
+    ("e4m3_bias", "ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    ("mx_nibble_order", "(c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15)",
+     "(c & 1) ? (uint8_t)(byte & 15) : (uint8_t)(byte >> 4)"),
+    ("mx_scale_block_64", "sc[c / 32]", "sc[c / 64]"),
+    ("e4m3_ties_toward_zero", "(err == best_err && (c & 1) == 0 && (best & 1) == 1)", "0"),
+    ("x_scale_divisor", "amax / 448.0f", "amax / 256.0f"),
+    ("align_unstable_order",
+     "for (long i = 0; i < na; ++i) {\n            if (ids[i] != e) continue;",
+     "for (long i = na - 1; i >= 0; --i) {\n            if (ids[i] != e) continue;"),
+    # under-padding keeps every write inside the buffers (over-padding would not)
+    ("align_padding_rule", "(counts[e] + bm - 1) / bm * bm", "counts[e] / bm * bm"),
+    ("align_sentinel", "sorted_ids[s] = (int32_t)na;", "sorted_ids[s] = -1;"),
+    ("align_valid_rows", "bi[3] = left < bm ? left : bm;", "bi[3] = bm;"),
+    ("align_bad_id_accepted", "if (ids[i] < 0 || ids[i] >= E) return -1;\n    for (int e = 0; e < E; ++e) counts[e] = 0;",
+     "for (int e = 0; e < E; ++e) counts[e] = 0;"),
+    ("combine_slot_index", "y[(size_t)inv_perm[(size_t)t * K + k] * H + c]",
+     "y[(size_t)inv_perm[(size_t)t * K] * H + c]"),
+    ("gather_row_index", "load_token_row(p, x, i / p->K, xrow);",
+     "load_token_row(p, x, i % p->T, xrow);"),
+]
+
+ALL_PINS = pins.FORMAT_PINS + [pins.pin_align_rejects_bad_id, pins.pin_align_invariants] + [
+    (lambda c=c: pins.pin_align_vs_stable_argsort(*c)) for c in pins.ALIGN_CASES[:7]
+] + pins.FFN_PINS
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(mutant, tmp_path):
+    name, old, new = mutant
+    src = oracle.source()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    so = oracle.build_variant(src.replace(old, new, 1), str(tmp_path), name)
+    with oracle.using_library(so):
+        for pin in ALL_PINS:
+            try:
+                pin()
+            except Exception:  # an assertion, or a pin's own indexing tripping on bad output
+                return  # caught
+    pytest.fail(f"no pin caught the planted mistake {name}")
