@@ -1,0 +1,420 @@
+"""Benchmark of the MoE expert-FFN forward (align -> gate/up GEMM + SiLU*up ->
+down GEMM x routing weight -> combine) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME]
+
+One step is one pass of the whole path over one synthetic batch.  The default
+workload is the Mixtral-8x7B-shaped prefill layer (T=4096, H=4096, I=14336,
+E=8, top-2, bf16).  Under torchrun each rank runs its own replica on its own
+GPU with its own batch (weak scaling; no data-path collective).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+(the plain fp64 definition) on the host cores instead, on a bounded sample of
+tokens of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mixture_experts_grouped_02_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "MoE layer tokens/sec and TFLOP/s (prefill); HBM GB/s (decode) vs GB300 peak"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_gate_up_mixtral_prefill.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "mixture_experts_grouped_02_gb300", "csrc", f)
+                  for f in ("gemm.cu", "ptx.cuh", "internal.h")]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mixtral_prefill")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def max_over_ranks(v: float, ws: int, device) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the gate/up GEMM from the committed ncu
+    summary, or None when the kernel changed since it was captured."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    vals = {}
+    with open(PROFILE_TRAFFIC) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["traffic_bytes_per_launch_full"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = list(csv.reader(io.StringIO(out)))
+        samples = []
+        for r in rows:
+            if len(r) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                samples.append(dict(ts=ts, sm=float(r[2]), smax=float(r[3]),
+                                    hw=r[6].strip(), hwt=r[7].strip(), swt=r[8].strip(),
+                                    pcap=r[9].strip()))
+            except (ValueError, IndexError):
+                continue
+        if not samples:
+            return None
+        inside = [s for s in samples if t0 - 1.0 <= s["ts"] <= t1 + 1.0] or samples
+        reasons = set()
+        for s in inside:
+            if s["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if s["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if s["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if s["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(s["sm"] for s in inside),
+                "sm_max_mhz": max(s["smax"] for s in inside), "reasons": sorted(reasons),
+                "samples": len(inside)}
+
+
+def bytes_algorithmic(cfg, inp):
+    """Weights of experts with at least one token + x once + out once + ids
+    and weights."""
+    active = int((torch.bincount(inp.topk_ids.flatten().long(), minlength=cfg.E) > 0).sum())
+    esz = inp.x.element_size()
+    w_per_expert = (inp.w13[0].numel() * inp.w13.element_size() +
+                    inp.w2[0].numel() * inp.w2.element_size())
+    return active * w_per_expert + 2 * cfg.T * cfg.H * esz + 8 * cfg.T * cfg.K, active
+
+
+def cpu_oracle_rate(cfg, inp_cpu, seconds):
+    """Time the oracle (as it stands) on a bounded sample of tokens; returns
+    (tokens/s, sample description, threads)."""
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    oracle.lib()
+    P = oracle.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, gen.to_numpy_storage(inp_cpu.x[:1]),
+                            gen.to_numpy_storage(inp_cpu.w13[:1]))
+    args = (gen.to_numpy_storage(inp_cpu.x), inp_cpu.topk_ids.numpy(),
+            inp_cpu.topk_weights.numpy(), gen.to_numpy_storage(inp_cpu.w13),
+            gen.to_numpy_storage(inp_cpu.w2))
+    probe = np.arange(min(cfg.T, threads), dtype=np.int32)
+    t = time.perf_counter()
+    oracle.forward(P, *args, tokens=probe)
+    dt = time.perf_counter() - t
+    n = int(min(cfg.T, max(len(probe), len(probe) * seconds / max(dt, 1e-3))))
+    n = max(threads, n // threads * threads) if n >= threads else n
+    toks = np.arange(n, dtype=np.int32)
+    t = time.perf_counter()
+    oracle.forward(P, *args, tokens=toks)
+    dt = time.perf_counter() - t
+    return n / dt, f"first {n} of {cfg.T} tokens ({n * cfg.K} assignments), fp64, {dt:.1f} s", \
+        threads
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    cfg = gen.config(args.config)
+    inp = gen.generate(cfg, seed=0, device="cpu")
+    per_step = args.cpu_seconds / max(1, args.steps + args.warmup)
+    rates = []
+    sample = ""
+    threads = 1
+    for i in range(args.warmup + args.steps):
+        r, sample, threads = cpu_oracle_rate(cfg, inp, max(1.0, per_step))
+        if i >= args.warmup:
+            rates.append(r)
+    value = statistics.median(rates)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * cfg.T / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+                       "top_k": cfg.K, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import mixture_experts_grouped_02_gb300 as moe
+    from mixture_experts_grouped_02_gb300 import _abi
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe._abi.lib()
+    cfg = gen.config(args.config)
+    # weights are the same model on every rank; each rank routes its own batch
+    inp = gen.generate(cfg, seed=0, device=dev)
+    if rank > 0:
+        inp.x = gen.draw_x(cfg, seed=1000 + rank, device=dev)
+        inp.topk_ids, inp.topk_weights = gen.route(gen.router_logits(cfg, 1000 + rank, dev),
+                                                   cfg.K)
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype)
+    wsp = moe.Workspace(p, dev)
+    part = lambda i, dt=torch.int32: wsp.part(i, dt)
+    st = wsp.status
+    counts, offs, poffs = part(_abi.MOE_WS_COUNTS), part(_abi.MOE_WS_OFFSETS), \
+        part(_abi.MOE_WS_PADDED_OFFSETS)
+    sorted_ids, inv = part(_abi.MOE_WS_SORTED_IDS), part(_abi.MOE_WS_INV_PERM)
+    binfo, nblk = part(_abi.MOE_WS_BLOCK_INFO), part(_abi.MOE_WS_NUM_BLOCKS)
+    h = part(_abi.MOE_WS_H, torch.uint8)
+    y = part(_abi.MOE_WS_Y, torch.float32)
+    splits = moe.moe_gemm2_default_splits(p)
+    cap = moe.moe_align_capacity(cfg.T, cfg.K, cfg.E, 128)
+    out = torch.empty((cfg.T, cfg.H), dtype=inp.x.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st.zero_()
+
+    def step(ev=None):
+        # exactly the launches moe_forward makes, with events between stages
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_align(inp.topk_ids, cfg.T, cfg.K, cfg.E, 128, counts, offs, poffs, sorted_ids,
+                      inv, binfo, nblk, st, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        moe.moe_gemm1_silu(p, inp.x, None, inp.w13, None, sorted_ids, binfo, nblk, h, st, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        moe.moe_gemm2_weighted(p, h, inp.w2, None, inp.topk_weights, sorted_ids, binfo, nblk, y,
+                               splits, st, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        moe.moe_combine(y, splits, cap, inv, cfg.T, cfg.K, cfg.H, p.act, out, st, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    status = moe.moe_get_device_status(st, stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    barrier(ws)
+    clocks = sampler.stop(t0, t1)
+    status = moe.moe_get_device_status(st, stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region")
+
+    stage = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
+                      for i in range(args.steps)])  # ms
+    total_ms = float(evs[0][0].elapsed_time(evs[-1][4]))
+    ms_step = max_over_ranks(total_ms / args.steps, ws, dev)
+    tokens_all = cfg.T * ws
+    value = tokens_all / (ms_step * 1e-3)
+    flops = cfg.flops
+    tflops = flops * ws / (ms_step * 1e-3) / 1e12
+    bytes_alg, active = bytes_algorithmic(cfg, inp)
+    gemm1_ms = float(stage[:, 1].mean())
+    gemm2_ms = float(stage[:, 2].mean())
+    hbm_gbs, bf16_tflops, peak_kind = peaks()
+    gemm1_flops = 4 * cfg.T * cfg.K * cfg.H * cfg.I
+    achieved = gemm1_flops / (gemm1_ms * 1e-3) / 1e12
+    traffic = profiled_traffic()
+
+    # end to end through the public API: pinned host inputs in, result out
+    x_h = inp.x.cpu().pin_memory()
+    ids_h = inp.topk_ids.cpu().pin_memory()
+    w_h = inp.topk_weights.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    x_d, ids_d, w_d = torch.empty_like(inp.x), torch.empty_like(inp.topk_ids), \
+        torch.empty_like(inp.topk_weights)
+    e2e_steps = min(args.steps, 50)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        ids_d.copy_(ids_h, non_blocking=True)
+        w_d.copy_(w_h, non_blocking=True)
+        moe.moe_forward(p, x_d, ids_d, w_d, inp.w13, None, inp.w2, None, out, wsp.buffer,
+                        wsp.nbytes, stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws, dev)
+    if moe.moe_get_device_status(st, stream) != 0:
+        raise RuntimeError("device status after the end-to-end loop")
+    h2d = x_h.numel() * x_h.element_size() + ids_h.numel() * 4 + w_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        inp_cpu = gen.MoEInputs(cfg, inp.x.cpu(), inp.w13.cpu(), inp.w2.cpu(),
+                                inp.topk_ids.cpu(), inp.topk_weights.cpu())
+        rate, sample, threads = cpu_oracle_rate(cfg, inp_cpu, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if cfg.dtype == "bf16" else cfg.dtype, "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+                       "top_k": cfg.K, "global_batch_tokens": tokens_all,
+                       "parallelism": f"replicas{ws}",
+                       "l2": "inputs larger than L2 (expert weights %.2f GB)" %
+                             (bytes_alg / 1e9)},
+            "tflops": tflops,
+            "hbm_gbs_algorithmic": bytes_alg * ws / (ms_step * 1e-3) / 1e9,
+            "stage_ms": {"align": float(stage[:, 0].mean()), "gemm_gate_up": gemm1_ms,
+                         "gemm_down": gemm2_ms, "combine": float(stage[:, 3].mean())},
+            "roofline": {"bound": "tensor", "kernel": "grouped_gemm gate/up + SiLU*up",
+                         "achieved": achieved, "peak": bf16_tflops, "unit": "TFLOP/s",
+                         "frac": achieved / bf16_tflops, "traffic": traffic,
+                         "peak_source": f"{peak_kind} bf16 dense (burst)",
+                         "flops_per_launch": gemm1_flops},
+            "gemm_down_roofline": {"achieved": 2 * cfg.T * cfg.K * cfg.H * cfg.I /
+                                   (gemm2_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                                   "frac": 2 * cfg.T * cfg.K * cfg.H * cfg.I /
+                                   (gemm2_ms * 1e-3) / 1e12 / bf16_tflops},
+            "active_experts": active,
+            "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)  # rank 0 alone; no process group needed
+    else:
+        init_dist(ws, "nccl")
+        run_ours(args, ws, rank, local)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+/*
+ * moe.h -- C ABI of libmoe_gb300.so: the MoE expert-FFN forward on one
+ * GB300 (sm_103a).
+ *
+ *   align -> gather + grouped GEMM(w13) + SiLU(gate)*up
+ *         -> grouped GEMM(w2) x routing weight -> combine
+ *
+ * The operation is the one the header comment of "factor_moe_fused_gemm.cu"
+ * (ex_engine, Factor 2: MOE_FUSED_GEMM) spells out as its "Current PyTorch
+ * path": per expert, gather the routed token rows, gate_up = x W13[e]^T,
+ * act = SiLU(gate) * up, y = act W2[e]^T, and index-add weight * y back
+ * into the token rows.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library allocates nothing and frees nothing; intermediates live in a
+ *    caller-provided workspace (moe_workspace_size).
+ *  - Tensors are dense, row-major, without padding between rows.
+ *  - `stream` is a cudaStream_t passed as void*; every call is asynchronous
+ *    on that stream and never synchronises the host, except
+ *    moe_get_device_status, which does.
+ *  - Argument and shape errors are detected on the host before any launch
+ *    and returned as a status; nothing is launched then.  Launch failures
+ *    return MOE_ERR_CUDA.  Errors found by the kernels themselves (an expert
+ *    id outside [0, E), a pipeline wait that ran out) are written to a
+ *    device status word (one int32 in device memory, 0 = no error, the first
+ *    error wins); kernels that find it non-zero at start return without
+ *    writing their outputs.  Read it with moe_get_device_status.
+ *  - Expert ids are int32 in [0, E); routing weights are fp32.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum      */
+    MOE_ERR_UNSUPPORTED = 2,   /* shape/dtype combination this build lacks   */
+    MOE_ERR_WORKSPACE = 3,     /* workspace too small or misaligned          */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed          */
+    MOE_ERR_DEVICE_BAD_ID = 5, /* (device) an expert id outside [0, E)       */
+    MOE_ERR_TIMEOUT = 6        /* (device) a pipeline wait ran out; the      */
+                               /* kernel stopped, freed its tensor memory    */
+                               /* and returned                               */
+} moe_status_t;
+
+typedef enum {
+    MOE_F32 = 0,     /* IEEE binary32                                          */
+    MOE_BF16 = 1,    /* bfloat16                                               */
+    MOE_E4M3 = 2,    /* OCP FP8 E4M3 (finite-only variant)                     */
+    MOE_E2M1_MX = 3  /* OCP MX FP4: e2m1 pairs, lower K index in the low       */
+                     /* nibble, plus one e8m0 scale byte per 32 K elements     */
+} moe_dtype_t;
+
+/* One MoE layer.  T tokens of width H, E experts with intermediate size I,
+ * top-K routing.
+ *   act    : dtype of x and out: MOE_F32 or MOE_BF16.
+ *   weight : dtype of w13/w2: equal to act, or MOE_E2M1_MX (then act must
+ *            be MOE_BF16; x is cast to e4m3 with one fp32 scale per row and
+ *            the hidden activation is stored as e4m3(a / h_scale)).
+ *   block_m: rows per alignment block, 0 = automatic (128).
+ *   h_scale: scale of the e4m3 hidden activation (MX weights only; 0 => 1). */
+typedef struct {
+    int T, H, I, E, K;
+    int act;
+    int weight;
+    int block_m;
+    float h_scale;
+} moe_problem_t;
+
+/* Sub-buffers of the moe_forward workspace (byte offsets, see
+ * moe_workspace_offsets). */
+typedef enum {
+    MOE_WS_STATUS = 0,         /* int32 device status word                  */
+    MOE_WS_COUNTS = 1,         /* int32[E]                                  */
+    MOE_WS_OFFSETS = 2,        /* int32[E+1]                                */
+    MOE_WS_PADDED_OFFSETS = 3, /* int32[E+1]                                */
+    MOE_WS_SORTED_IDS = 4,     /* int32[cap]                                */
+    MOE_WS_INV_PERM = 5,       /* int32[T*K]                                */
+    MOE_WS_BLOCK_INFO = 6,     /* int32[cap/block_m][4]                     */
+    MOE_WS_NUM_BLOCKS = 7,     /* int32[1]                                  */
+    MOE_WS_XQ = 8,             /* e4m3[T][H]   (MX weights only)            */
+    MOE_WS_X_SCALE = 9,        /* fp32[T]      (MX weights only)            */
+    MOE_WS_H = 10,             /* act or e4m3 [cap][I]                      */
+    MOE_WS_Y = 11,             /* fp32[splits][cap][H]                      */
+    MOE_WS_NUM = 12
+} moe_ws_part_t;
+
+/* Static string for a status code (never NULL). */
+const char* moe_status_string(int status);
+
+/* Library ABI version (increments on any signature change). */
+int moe_abi_version(void);
+
+/* Rows per alignment block the GEMMs of this build use for `p` (resolves
+ * block_m == 0), or -1 when p is invalid. */
+int moe_resolve_block_m(const moe_problem_t* p);
+
+/* Capacity of the padded sorted list: T*K + min(E, T*K)*(block_m - 1).
+ * Every active expert's list is padded to a multiple of block_m, so this
+ * bounds sum_e ceil(count_e / block_m) * block_m for any routing. */
+size_t moe_align_capacity(int T, int K, int E, int block_m);
+
+/* Number of K splits moe_forward uses for the down projection of `p`
+ * (its fp32 partial outputs are summed by the combine). */
+int moe_gemm2_default_splits(const moe_problem_t* p);
+
+/* Bytes of workspace moe_forward needs for `p` (0 when p is invalid). */
+size_t moe_workspace_size(const moe_problem_t* p);
+
+/* Byte offset of every moe_ws_part_t inside the workspace, written to
+ * offsets[MOE_WS_NUM].  Parts a problem does not use get size 0. */
+int moe_workspace_offsets(const moe_problem_t* p, size_t offsets[MOE_WS_NUM],
+                          size_t sizes[MOE_WS_NUM]);
+
+/* ---- align ------------------------------------------------------------
+ * Source: "factor_moe_fused_gemm.cu", build_expert_map_kernel (expert
+ * histogram, CSR offsets, permutation) and "moe triton kernel use tma"
+ * (LightLLM pull request 1100), the summary's mblocks_to_tuple_info
+ * (expert id, M-index and token start of each M-block).
+ *
+ * With i = t*K + k the flat index of token t's k-th choice (N_a = T*K):
+ *   counts[e]                 number of i with topk_ids[i] == e      int32[E]
+ *   offsets[e]                exclusive prefix sum of counts         int32[E+1]
+ *   padded_offsets[e]         exclusive prefix sum of
+ *                             ceil(counts/block_m)*block_m           int32[E+1]
+ *   sorted_ids[s]             slot s of the padded expert-sorted list: the
+ *                             r-th smallest i routed to e sits at
+ *                             padded_offsets[e] + r (stable order);
+ *                             every other slot < cap holds N_a       int32[cap]
+ *   inv_perm[i]               the slot of i                          int32[N_a]
+ *   block_info[b]             {expert, m, first slot, valid rows} of block
+ *                             b < num_blocks (experts ascending);
+ *                             {-1, 0, 0, 0} for the rest    int32[cap/block_m][4]
+ *   num_blocks[0]             padded_offsets[E] / block_m            int32[1]
+ * cap = moe_align_capacity(T, K, E, block_m); block_m in {16,32,64,128}.
+ * E <= 1024.  An id outside [0, E) makes the kernel write num_blocks = 0,
+ * set MOE_ERR_DEVICE_BAD_ID in *dev_status (when dev_status is not NULL)
+ * and leave the other outputs unspecified.  T == 0 writes nothing and
+ * returns MOE_OK. */
+int moe_align(const int32_t* topk_ids, int T, int K, int E, int block_m, int32_t* counts,
+              int32_t* offsets, int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
+              int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream);
+
+/* ---- fp8 activation step ------------------------------------------------
+ * Source: "MOE Bmm1 Fused Gather" (Triton Gluon example), pack_e4m3x2
+ * (fp32 -> e4m3, round to nearest even, saturating).  Reading: one scale
+ * per row, s_t = amax_t / 448 (1 when the row is zero), both formed in fp32.
+ *   x         (T, H) in x_dtype (MOE_BF16 or MOE_F32)
+ *   xq        (T, H) e4m3 codes, = e4m3_rn_satfinite(x / s_t)
+ *   row_scale (T) fp32 s_t                                                  */
+int moe_quantize_x_fp8(const void* x, int x_dtype, int T, int H, uint8_t* xq, float* row_scale,
+                       void* stream);
+
+/* ---- gather + GEMM1 + SiLU*up -------------------------------------------
+ * Source: "factor_moe_fused_gemm.cu", fused_silu_gate_kernel (gate = first
+ * half of the w13 rows, up = second half, SiLU(g) = g / (1 + e^-g)) and
+ * "MOE Bmm1 Fused Gather", load_activations (token rows gathered by index,
+ * padded rows masked) with epilogue_partition (activation fused into the
+ * GEMM epilogue).
+ * For every slot s of a block b < *num_blocks with i = sorted_ids[s] < N_a
+ * and e = block_info[b].expert:
+ *   h[s, j] = SiLU(W13[e, j, :] . x[i / K, :]) * (W13[e, I + j, :] . x[i / K, :])
+ * x    (T, H) act; for MX weights, e4m3 codes with x_row_scale (T) fp32
+ * w13  (E, 2I, H) weight dtype (MX: (E, 2I, H/2) bytes + w13_scale (E, 2I, H/32))
+ * h    (cap, I) act (MX: e4m3 codes of a / h_scale); rows of padding slots
+ *      are not written.  H and I must be multiples of 64 (32 for MOE_F32).
+ * sorted_ids/block_info/num_blocks as written by moe_align with the same
+ * block_m.  dev_status may be NULL. */
+int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_scale,
+                   const void* w13, const uint8_t* w13_scale, const int32_t* sorted_ids,
+                   const int32_t* block_info, const int32_t* num_blocks, void* h,
+                   int32_t* dev_status, void* stream);
+
+/* ---- GEMM2 x routing weight -----------------------------------------------
+ * Source: "moe triton kernel use tma", the review comment on
+ * TOKEN_INPUT_USE_TMA (token rows of the down projection are contiguous in
+ * sorted order and load as plain tiles; MUL_ROUTED_WEIGHT multiplies the
+ * routing weight there) and the "Current PyTorch path"'s expert_out * weights.
+ * For every valid slot s (as above) and split q < k_splits:
+ *   y[q, s, c] = topk_weights[i] * sum_{j in split q} W2[e, c, j] * h[s, j]
+ * so that sum_q y[q, s, :] is the routing-weighted expert output.  Splits
+ * cut I into k_splits nearly equal runs of 64 columns (k_splits <= I/64).
+ * h (cap, I) as written by moe_gemm1_silu; w2 (E, H, I) weight dtype (MX:
+ * (E, H, I/2) + w2_scale (E, H, I/32)); y (k_splits, cap, H) fp32, padding
+ * rows not written. */
+int moe_gemm2_weighted(const moe_problem_t* p, const void* h, const void* w2,
+                       const uint8_t* w2_scale, const float* topk_weights,
+                       const int32_t* sorted_ids, const int32_t* block_info,
+                       const int32_t* num_blocks, float* y, int k_splits, int32_t* dev_status,
+                       void* stream);
+
+/* ---- combine ---------------------------------------------------------------
+ * Source: the index_add of the "Current PyTorch path" and
+ * weighted_scatter_add_kernel of "factor_moe_fused_gemm.cu", done here as a
+ * deterministic per-token reduction instead of atomics:
+ *   out[t, c] = sum_{k < K} sum_{q < k_splits} y[q, inv_perm[t*K + k], c]
+ * summed in fp32 in k order, rounded once to out_dtype (MOE_F32/MOE_BF16).
+ * y (k_splits, cap, H) fp32; inv_perm (T*K); out (T, H). */
+int moe_combine(const float* y, int k_splits, size_t cap, const int32_t* inv_perm, int T, int K,
+                int H, int out_dtype, void* out, int32_t* dev_status, void* stream);
+
+/* ---- the whole forward -----------------------------------------------------
+ * Runs [fp8 step (MX only)] -> align -> GEMM1 -> GEMM2 -> combine on
+ * `stream`, with every intermediate in `workspace` (device memory of at
+ * least moe_workspace_size(p) bytes, 256-byte aligned, owned by the caller,
+ * reusable across calls but not shared by calls in flight at once).
+ *   x (T, H) act; topk_ids (T, K) int32; topk_weights (T, K) fp32;
+ *   w13 (E, 2I, H), w2 (E, H, I) (MX: packed + scales as above);
+ *   out (T, H) act.
+ * The status word at MOE_WS_STATUS is cleared at the start of each call. */
+int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
+                const float* topk_weights, const void* w13, const uint8_t* w13_scale,
+                const void* w2, const uint8_t* w2_scale, void* out, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream` and return the device status word at dev_status
+ * (MOE_OK when it is 0), or MOE_ERR_CUDA if the stream itself failed. */
+int moe_get_device_status(const int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,95 @@
+"""MoE expert-FFN forward on one GB300 (sm_103a).
+
+The computation lives in ``libmoe_gb300.so`` (C ABI in ``include/moe.h``):
+align -> gathered grouped GEMM with w13 + SiLU(gate)*up -> grouped GEMM with
+w2 x routing weight -> deterministic combine.  This package is its Python
+binding: :mod:`._abi` has one function per C entry point, with the same name;
+the helpers below only allocate device buffers with torch and call them.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _abi
+from ._abi import (MOE_BF16, MOE_E2M1_MX, MOE_E4M3, MOE_F32, MoEError, Problem, moe_abi_version,
+                   moe_align, moe_align_capacity, moe_combine, moe_forward, moe_gemm1_silu,
+                   moe_gemm2_default_splits, moe_gemm2_weighted, moe_get_device_status,
+                   moe_quantize_x_fp8, moe_resolve_block_m, moe_workspace_offsets,
+                   moe_workspace_size)
+
+__all__ = ["MoEError", "Problem", "make_problem", "dtype_code", "align", "Workspace", "forward",
+           "moe_abi_version", "moe_align", "moe_align_capacity", "moe_combine", "moe_forward",
+           "moe_gemm1_silu", "moe_gemm2_default_splits", "moe_gemm2_weighted",
+           "moe_get_device_status", "moe_quantize_x_fp8", "moe_resolve_block_m",
+           "moe_workspace_offsets", "moe_workspace_size"]
+
+
+def dtype_code(dt) -> int:
+    if dt in (torch.float32, "f32"):
+        return MOE_F32
+    if dt in (torch.bfloat16, "bf16"):
+        return MOE_BF16
+    if dt in ("mxfp4", MOE_E2M1_MX):
+        return MOE_E2M1_MX
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def make_problem(T, H, I, E, K, act="bf16", weight=None, block_m=0, h_scale=1.0) -> Problem:
+    a = dtype_code(act)
+    w = a if weight is None else dtype_code(weight)
+    return Problem(T, H, I, E, K, a, w, block_m, h_scale)
+
+
+def align(topk_ids: torch.Tensor, E: int, block_m: int = 128, dev_status=None, stream=None):
+    """Run moe_align on (T, K) int32 ids; returns the outputs as a dict of
+    device tensors."""
+    T, K = topk_ids.shape
+    cap = moe_align_capacity(T, K, E, block_m)
+    dev = topk_ids.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = dict(counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
+               padded_offsets=torch.empty(E + 1, **i32), sorted_ids=torch.empty(cap, **i32),
+               inv_perm=torch.empty(T * K, **i32),
+               block_info=torch.empty((cap // block_m, 4), **i32),
+               num_blocks=torch.empty(1, **i32))
+    moe_align(topk_ids, T, K, E, block_m, out["counts"], out["offsets"], out["padded_offsets"],
+              out["sorted_ids"], out["inv_perm"], out["block_info"], out["num_blocks"],
+              dev_status, stream)
+    return out
+
+
+class Workspace:
+    """A device buffer sized for one problem, with views of its parts."""
+
+    def __init__(self, p: Problem, device="cuda"):
+        self.problem = p
+        self.nbytes = moe_workspace_size(p)
+        if self.nbytes == 0:
+            raise MoEError(_abi.MOE_ERR_INVALID_ARG, "moe_workspace_size")
+        self.buffer = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.offsets, self.sizes = moe_workspace_offsets(p)
+
+    def part(self, idx: int, dtype=torch.uint8) -> torch.Tensor:
+        off, size = self.offsets[idx], self.sizes[idx]
+        return self.buffer[off:off + size].view(dtype)
+
+    @property
+    def status(self) -> torch.Tensor:
+        return self.part(_abi.MOE_WS_STATUS, torch.int32)[:1]
+
+
+def forward(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=None, out=None,
+            workspace: Workspace | None = None, weight=None, h_scale=1.0, stream=None):
+    """out = MoE expert FFN of x routed by (topk_ids, topk_weights)."""
+    T, H = x.shape
+    E = w13.shape[0]
+    I = w2.shape[2] * (2 if weight in ("mxfp4", MOE_E2M1_MX) else 1)
+    K = topk_ids.shape[1]
+    p = make_problem(T, H, I, E, K, x.dtype, weight, 0, h_scale)
+    if workspace is None:
+        workspace = Workspace(p, x.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=x.dtype, device=x.device)
+    moe_forward(p, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, out,
+                workspace.buffer, workspace.nbytes, stream)
+    return out

@@ -1,0 +1,227 @@
+// align.cu -- routing alignment: expert histogram, padded prefix sums,
+// stable scatter into the expert-sorted padded list, inverse permutation
+// and per-block work descriptors.
+//
+// Sources: "factor_moe_fused_gemm.cu", build_expert_map_kernel (expert
+// counts, CSR offsets and the token permutation; its atomics leave the order
+// within an expert undefined, here the order is the ascending flat index);
+// "moe triton kernel use tma", mblocks_to_tuple_info (one (expert, M-index,
+// token start) tuple per M-block); "MOE Bmm1 Fused Gather",
+// load_activations (padding slots of a block are masked).
+//
+// One CTA of 32 warps does the whole job; the work is a few passes over
+// T*K int32 ids.  Warp w owns a contiguous chunk of the flat index range and
+// a private histogram row in shared memory:
+//   1. histogram: per 32-id batch, __match_any_sync groups equal ids and the
+//      group's lowest lane adds the group size to the warp's row;
+//   2. per expert, an exclusive scan over the warps' rows gives each warp its
+//      start inside the expert; a block-wide scan over experts gives the CSR
+//      and padded offsets;
+//   3. scatter: the warps walk their chunks again in the same order; an id's
+//      slot is padded_offset[e] + warp start + running count + rank among the
+//      equal ids of lower lanes.  Chunks are in index order, batches in index
+//      order, lanes in index order, so the result is the stable order.
+//   4. padding slots, the tail up to the capacity, and block descriptors.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kAlignWarps = 32;
+constexpr int kAlignThreads = kAlignWarps * 32;
+
+// Block-wide exclusive scan of two int values per thread (1024 threads).
+__device__ __forceinline__ void block_exclusive_scan2(int& a, int& b, int* s_tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ia = a, ib = b;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int na = __shfl_up_sync(0xffffffffu, ia, d);
+    const int nb = __shfl_up_sync(0xffffffffu, ib, d);
+    if (lane >= d) {
+      ia += na;
+      ib += nb;
+    }
+  }
+  if (lane == 31) {
+    s_tmp[warp] = ia;
+    s_tmp[32 + warp] = ib;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int wa = s_tmp[lane], wb = s_tmp[32 + lane];
+    int xa = wa, xb = wb;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int na = __shfl_up_sync(0xffffffffu, xa, d);
+      const int nb = __shfl_up_sync(0xffffffffu, xb, d);
+      if (lane >= d) {
+        xa += na;
+        xb += nb;
+      }
+    }
+    s_tmp[lane] = xa - wa;  // exclusive warp prefix
+    s_tmp[32 + lane] = xb - wb;
+  }
+  __syncthreads();
+  a = ia - a + s_tmp[warp];
+  b = ib - b + s_tmp[32 + warp];
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs p) {
+  extern __shared__ int sm[];
+  const int E = p.E;
+  int* hist = sm;                        // [kAlignWarps][E]
+  int* s_pad = hist + kAlignWarps * E;   // [E + 1] padded offsets
+  int* s_cnt = s_pad + E + 1;            // [E]
+  __shared__ int s_tmp[64];
+  __shared__ int s_bad;
+  __shared__ int s_carry[2];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int na = p.n_assign;
+  const int bm = p.block_m;
+
+  if (tid == 0) s_bad = 0;
+  for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) hist[i] = 0;
+  __syncthreads();
+
+  // chunk of warp w: [w*chunk, min(na, (w+1)*chunk)), chunk a multiple of 32
+  const int chunk = ((na + kAlignWarps - 1) / kAlignWarps + 31) & ~31;
+  const int lo = warp * chunk;
+  const int hi = min(na, lo + chunk);
+  int* my_hist = hist + warp * E;
+
+  // 1. histogram
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    int e = -1;
+    if (i < hi) {
+      e = p.ids[i];
+      if (e < 0 || e >= E) {
+        s_bad = 1;
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) my_hist[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) {
+      report_error(p.status, MOE_ERR_DEVICE_BAD_ID);
+      p.num_blocks[0] = 0;
+    }
+    return;
+  }
+
+  // 2. per-expert scan over warps, then scans over experts (chunks of 1024)
+  for (int e = tid; e < E; e += kAlignThreads) {
+    int run = 0;
+    for (int w = 0; w < kAlignWarps; ++w) {
+      const int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+    s_cnt[e] = run;
+    p.counts[e] = run;
+  }
+  if (tid == 0) {
+    s_carry[0] = 0;
+    s_carry[1] = 0;
+  }
+  __syncthreads();
+  for (int e0 = 0; e0 < E; e0 += kAlignThreads) {
+    const int e = e0 + tid;
+    const int c = e < E ? s_cnt[e] : 0;
+    int a = c;
+    int b = (c + bm - 1) / bm * bm;
+    const int carry_a = s_carry[0], carry_b = s_carry[1];
+    const int pa = b;  // padded count, kept for the carry update
+    block_exclusive_scan2(a, b, s_tmp);
+    a += carry_a;
+    b += carry_b;
+    if (e < E) {
+      p.offsets[e] = a;
+      p.padded_offsets[e] = b;
+      s_pad[e] = b;
+    }
+    if (e == min(E, e0 + kAlignThreads) - 1) {  // last expert of this chunk
+      s_carry[0] = a + c;
+      s_carry[1] = b + pa;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.offsets[E] = s_carry[0];
+    p.padded_offsets[E] = s_carry[1];
+    s_pad[E] = s_carry[1];
+  }
+  __syncthreads();
+
+  // 3. stable scatter
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const int e = i < hi ? p.ids[i] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const unsigned lower = peers & ((1u << lane) - 1u);
+      const int slot = s_pad[e] + my_hist[e] + __popc(lower);
+      p.sorted_ids[slot] = i;
+      p.inv_perm[i] = slot;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) my_hist[e] += __popc(peers);
+    __syncwarp();
+  }
+
+  // 4a. padding slots of each expert, and the tail [padded_offsets[E], cap)
+  for (int e = tid; e < E; e += kAlignThreads)
+    for (int s = s_pad[e] + s_cnt[e]; s < s_pad[e + 1]; ++s) p.sorted_ids[s] = na;
+  for (long long s = s_pad[E] + tid; s < p.cap; s += kAlignThreads) p.sorted_ids[s] = na;
+
+  // 4b. block descriptors {expert, m, first slot, valid rows}
+  const int nb = s_pad[E] / bm;
+  const long long max_blocks = p.cap / bm;
+  int4* bi = reinterpret_cast<int4*>(p.block_info);
+  for (long long b = tid; b < max_blocks; b += kAlignThreads) {
+    int4 v = make_int4(-1, 0, 0, 0);
+    if (b < nb) {
+      const int row = static_cast<int>(b) * bm;
+      // the expert whose padded range holds `row`: last e with s_pad[e] <= row
+      // among experts with a non-empty range
+      int l = 0, h = E;  // find smallest e with s_pad[e + 1] > row
+      while (l < h) {
+        const int mid = (l + h) >> 1;
+        if (s_pad[mid + 1] > row)
+          h = mid;
+        else
+          l = mid + 1;
+      }
+      const int m = (row - s_pad[l]) / bm;
+      v = make_int4(l, m, row, min(bm, s_cnt[l] - m * bm));
+    }
+    bi[b] = v;
+  }
+  if (tid == 0) p.num_blocks[0] = nb;
+}
+
+}  // namespace
+
+size_t align_smem_bytes(int E) {
+  return sizeof(int) * (static_cast<size_t>(kAlignWarps) * E + (E + 1) + E);
+}
+
+cudaError_t launch_align(const AlignArgs& a, cudaStream_t s) {
+  const size_t smem = align_smem_bytes(a.E);
+  cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  align_kernel<<<1, kAlignThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

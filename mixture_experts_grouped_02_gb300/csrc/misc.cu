@@ -1,0 +1,114 @@
+// misc.cu -- the bandwidth-bound stages: the deterministic per-token combine
+// and the per-row fp8 (e4m3) activation step.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+// out[t, :] = sum_k sum_q y[q, inv_perm[t*K + k], :], fp32 in k order, then
+// one rounding to the output type.  Source: the index_add of the "Current
+// PyTorch path" in "factor_moe_fused_gemm.cu" and its
+// weighted_scatter_add_kernel, made deterministic: each token owns its row,
+// so no atomics and a fixed summation order.  One CTA per token row (grid
+// stride), 16-byte loads of y.
+template <typename OutT>
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int splits,
+                                                      long long cap,
+                                                      const int32_t* __restrict__ inv_perm, int T,
+                                                      int K, int H, OutT* __restrict__ out,
+                                                      const int32_t* status) {
+  if (status != nullptr && *status != 0) return;
+  const int h4 = H >> 2;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const int32_t* slots = inv_perm + static_cast<long long>(t) * K;
+    for (int c = threadIdx.x; c < h4; c += blockDim.x) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < K; ++k) {
+        const long long row = slots[k];
+        for (int q = 0; q < splits; ++q) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(
+                                     y + (static_cast<long long>(q) * cap + row) * H) +
+                                 c);
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+      }
+      if constexpr (sizeof(OutT) == 2) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        reinterpret_cast<uint2*>(out + static_cast<long long>(t) * H)[c] = pk;
+      } else {
+        reinterpret_cast<float4*>(out + static_cast<long long>(t) * H)[c] = acc;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float load_act(const void* x, int bf16, long long idx) {
+  if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(x)[idx]);
+  return reinterpret_cast<const float*>(x)[idx];
+}
+
+// Per-row e4m3 quantisation: s_t = amax_t / 448 (1 for an all-zero row),
+// xq = cvt.rn.satfinite.e4m3(x / s_t), both in fp32 with IEEE rounding.
+// Source: "MOE Bmm1 Fused Gather", pack_e4m3x2 (the same conversion
+// instruction); one scale per row is this workload's reading.
+__global__ void __launch_bounds__(256) quantize_x_kernel(const void* __restrict__ x, int bf16,
+                                                         int T, int H, uint8_t* __restrict__ xq,
+                                                         float* __restrict__ row_scale) {
+  __shared__ float s_red[8];
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const long long base = static_cast<long long>(t) * H;
+    float amax = 0.0f;
+    for (int c = threadIdx.x; c < H; c += blockDim.x) amax = fmaxf(amax, fabsf(load_act(x, bf16, base + c)));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = s_red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, s_red[w]);
+    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    if (threadIdx.x == 0) row_scale[t] = s;
+    for (int c = 2 * threadIdx.x; c < H; c += 2 * blockDim.x) {
+      const float v0 = __fdiv_rn(load_act(x, bf16, base + c), s);
+      const float v1 = __fdiv_rn(load_act(x, bf16, base + c + 1), s);
+      uint16_t pk;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pk) : "f"(v1), "f"(v0));
+      *reinterpret_cast<uint16_t*>(xq + base + c) = pk;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* y, int splits, long long cap, const int32_t* inv_perm,
+                           int T, int K, int H, int out_dtype, void* out, int32_t* status,
+                           cudaStream_t s) {
+  const int grid = T < 65535 ? T : 65535;
+  if (out_dtype == MOE_BF16)
+    combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(y, splits, cap, inv_perm, T, K, H,
+                                                        reinterpret_cast<__nv_bfloat16*>(out),
+                                                        status);
+  else
+    combine_kernel<float><<<grid, 256, 0, s>>>(y, splits, cap, inv_perm, T, K, H,
+                                                reinterpret_cast<float*>(out), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_x(const void* x, int x_dtype, int T, int H, uint8_t* xq,
+                              float* row_scale, cudaStream_t s) {
+  const int grid = T < 65535 ? T : 65535;
+  quantize_x_kernel<<<grid, 256, 0, s>>>(x, x_dtype == MOE_BF16 ? 1 : 0, T, H, xq, row_scale);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,453 @@
+// moe_abi.cu -- the C ABI declared in include/moe.h: argument checks,
+// workspace layout, TMA descriptor encoding and stage launches.  Allocates
+// nothing; every launch goes on the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe {
+size_t align_smem_bytes(int E);
+}
+
+using namespace moe;
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr size_t kWsAlign = 1024;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxDevices = 64;
+constexpr int kBand = 8;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool valid_dtype_pair(int act, int weight) {
+  if (act != MOE_F32 && act != MOE_BF16) return false;
+  if (weight == act) return true;
+  return weight == MOE_E2M1_MX && act == MOE_BF16;
+}
+
+int check_problem(const moe_problem_t* p) {
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  if (p->T < 0 || p->H <= 0 || p->I <= 0 || p->E <= 0 || p->K <= 0) return MOE_ERR_INVALID_ARG;
+  if (!valid_dtype_pair(p->act, p->weight)) return MOE_ERR_INVALID_ARG;
+  if (p->block_m != 0 && p->block_m != 16 && p->block_m != 32 && p->block_m != 64 &&
+      p->block_m != 128)
+    return MOE_ERR_INVALID_ARG;
+  if (p->E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  const long long na = static_cast<long long>(p->T) * p->K;
+  if (na >= (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int block_m_of(const moe_problem_t* p) { return p->block_m == 0 ? kBlockM : p->block_m; }
+
+// The GEMMs read 128-byte k-tiles (64 bf16 / 32 fp32) and write 32-column
+// output chunks; the GEMM tile is 128 sorted rows.
+int check_gemm_shapes(const moe_problem_t* p) {
+  if (p->weight == MOE_E2M1_MX) return MOE_ERR_UNSUPPORTED;
+  const int bk = p->act == MOE_BF16 ? 64 : 32;
+  if (p->H % bk != 0 || p->I % bk != 0) return MOE_ERR_UNSUPPORTED;
+  if (block_m_of(p) != kBlockM) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+size_t act_bytes(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
+
+struct DeviceInfo {
+  int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 152;
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev[dev].sms == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    g_dev[dev].sms = n;
+  }
+  return g_dev[dev].sms;
+}
+
+long long capacity(long long T, long long K, long long E, long long bm) {
+  const long long na = T * K;
+  return na + std::min(E, na) * (bm - 1);
+}
+
+int default_splits(const moe_problem_t* p) {
+  const int bm = block_m_of(p);
+  const long long na = static_cast<long long>(p->T) * p->K;
+  if (na == 0) return 1;
+  const long long cap = capacity(p->T, p->K, p->E, bm);
+  const long long est_blocks =
+      std::min(cap / bm, (na + bm - 1) / bm + std::min<long long>(p->E, na));
+  const long long n_tiles = (p->H + 255) / 256;
+  const int bk = p->act == MOE_BF16 ? 64 : 32;
+  const long long k_tiles = std::max(1, p->I / bk);
+  const long long work = std::max(1ll, est_blocks * n_tiles);
+  const long long target = 2ll * sm_count();
+  if (work >= target) return 1;
+  long long s = (target + work - 1) / work;
+  s = std::min(s, std::max(1ll, k_tiles / 4));
+  s = std::min(s, 32ll);
+  return static_cast<int>(std::max(1ll, s));
+}
+
+struct Layout {
+  size_t off[MOE_WS_NUM];
+  size_t size[MOE_WS_NUM];
+  size_t total;
+};
+
+void layout_of(const moe_problem_t* p, Layout* L) {
+  const int bm = block_m_of(p);
+  const long long na = static_cast<long long>(p->T) * p->K;
+  const long long cap = capacity(p->T, p->K, p->E, bm);
+  const bool mx = p->weight == MOE_E2M1_MX;
+  const int splits = default_splits(p);
+  size_t sz[MOE_WS_NUM] = {};
+  sz[MOE_WS_STATUS] = 256;
+  sz[MOE_WS_COUNTS] = 4ull * p->E;
+  sz[MOE_WS_OFFSETS] = 4ull * (p->E + 1);
+  sz[MOE_WS_PADDED_OFFSETS] = 4ull * (p->E + 1);
+  sz[MOE_WS_SORTED_IDS] = 4ull * cap;
+  sz[MOE_WS_INV_PERM] = 4ull * na;
+  sz[MOE_WS_BLOCK_INFO] = 16ull * (cap / bm);
+  sz[MOE_WS_NUM_BLOCKS] = 4;
+  sz[MOE_WS_XQ] = mx ? 1ull * p->T * p->H : 0;
+  sz[MOE_WS_X_SCALE] = mx ? 4ull * p->T : 0;
+  sz[MOE_WS_H] = static_cast<size_t>(cap) * p->I * (mx ? 1 : act_bytes(p->act));
+  sz[MOE_WS_Y] = 4ull * splits * static_cast<size_t>(cap) * p->H;
+  size_t off = 0;
+  for (int i = 0; i < MOE_WS_NUM; ++i) {
+    L->off[i] = off;
+    L->size[i] = sz[i];
+    off = round_up(off + sz[i], kWsAlign);
+  }
+  L->total = off;
+}
+
+// ---------------------------------------------------------------- TMA maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode;
+}
+
+// 2-D row-major tensor (outer rows of `inner` elements), 128-byte swizzled
+// boxes of box_inner x box_outer elements.
+int make_map(CUtensorMap* tm, int dtype, const void* base, long long inner, long long outer,
+             int box_inner, int box_outer) {
+  auto enc = encoder();
+  if (enc == nullptr) return MOE_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  const CUtensorMapDataType dt =
+      dtype == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * act_bytes(dtype)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner),
+                             static_cast<cuuint32_t>(box_outer)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int run_align(const int32_t* ids, int T, int K, int E, int bm, int32_t* counts, int32_t* offsets,
+              int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
+              int32_t* block_info, int32_t* num_blocks, int32_t* status, cudaStream_t s) {
+  AlignArgs a;
+  a.ids = ids;
+  a.n_assign = T * K;
+  a.E = E;
+  a.block_m = bm;
+  a.cap = capacity(T, K, E, bm);
+  a.counts = counts;
+  a.offsets = offsets;
+  a.padded_offsets = padded_offsets;
+  a.sorted_ids = sorted_ids;
+  a.inv_perm = inv_perm;
+  a.block_info = block_info;
+  a.num_blocks = num_blocks;
+  a.status = status;
+  return cuda_status(launch_align(a, s));
+}
+
+GemmArgs base_args(const moe_problem_t* p) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.T = p->T;
+  a.H = p->H;
+  a.I = p->I;
+  a.E = p->E;
+  a.K = p->K;
+  a.cap = capacity(p->T, p->K, p->E, kBlockM);
+  a.timeout_ns = kWaitTimeoutNs;
+  return a;
+}
+
+int run_gemm1(const moe_problem_t* p, const void* x, const void* w13, const int32_t* sorted_ids,
+              const int32_t* block_info, const int32_t* num_blocks, void* h, int32_t* status,
+              cudaStream_t s) {
+  GemmArgs a = base_args(p);
+  const int bk = p->act == MOE_BF16 ? 64 : 32;
+  a.n_tiles = (p->I + 127) / 128;
+  a.k_tiles = p->H / bk;
+  a.splits = 1;
+  a.band = std::min(kBand, a.n_tiles);
+  a.sorted_ids = sorted_ids;
+  a.block_info = block_info;
+  a.num_blocks = num_blocks;
+  a.out = h;
+  a.status = status;
+  CUtensorMap tmA, tmB;
+  int rc = make_map(&tmA, p->act, x, p->H, p->T, bk, 1);
+  if (rc != MOE_OK) return rc;
+  rc = make_map(&tmB, p->act, w13, p->H, 2ll * p->I * p->E, bk, 128);
+  if (rc != MOE_OK) return rc;
+  const long long max_tiles = (a.cap / kBlockM) * a.n_tiles;
+  const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
+  return cuda_status(launch_gemm_gate_up(p->act, a, tmA, tmB, grid, s));
+}
+
+int run_gemm2(const moe_problem_t* p, const void* h, const void* w2, const float* topk_weights,
+              const int32_t* sorted_ids, const int32_t* block_info, const int32_t* num_blocks,
+              float* y, int splits, int32_t* status, cudaStream_t s) {
+  GemmArgs a = base_args(p);
+  const int bk = p->act == MOE_BF16 ? 64 : 32;
+  a.n_tiles = (p->H + 255) / 256;
+  a.k_tiles = p->I / bk;
+  a.splits = splits;
+  a.band = std::min(kBand, a.n_tiles);
+  a.sorted_ids = sorted_ids;
+  a.block_info = block_info;
+  a.num_blocks = num_blocks;
+  a.topk_weights = topk_weights;
+  a.out = y;
+  a.status = status;
+  CUtensorMap tmA, tmB;
+  int rc = make_map(&tmA, p->act, h, p->I, a.cap, bk, 128);
+  if (rc != MOE_OK) return rc;
+  rc = make_map(&tmB, p->act, w2, p->I, 1ll * p->H * p->E, bk, 256);
+  if (rc != MOE_OK) return rc;
+  const long long max_tiles = (a.cap / kBlockM) * a.n_tiles * splits;
+  const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
+  return cuda_status(launch_gemm_down(p->act, a, tmA, tmB, grid, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MOE_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_BAD_ID: return "expert id outside [0, E)";
+    case MOE_ERR_TIMEOUT: return "pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int moe_abi_version(void) { return kAbiVersion; }
+
+int moe_resolve_block_m(const moe_problem_t* p) {
+  if (check_problem(p) != MOE_OK) return -1;
+  return block_m_of(p);
+}
+
+size_t moe_align_capacity(int T, int K, int E, int block_m) {
+  if (T < 0 || K <= 0 || E <= 0 || block_m <= 0) return 0;
+  return static_cast<size_t>(capacity(T, K, E, block_m));
+}
+
+int moe_gemm2_default_splits(const moe_problem_t* p) {
+  if (check_problem(p) != MOE_OK) return -1;
+  return default_splits(p);
+}
+
+size_t moe_workspace_size(const moe_problem_t* p) {
+  if (check_problem(p) != MOE_OK) return 0;
+  Layout L;
+  layout_of(p, &L);
+  return L.total;
+}
+
+int moe_workspace_offsets(const moe_problem_t* p, size_t offsets[MOE_WS_NUM],
+                          size_t sizes[MOE_WS_NUM]) {
+  const int rc = check_problem(p);
+  if (rc != MOE_OK) return rc;
+  if (offsets == nullptr) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  layout_of(p, &L);
+  for (int i = 0; i < MOE_WS_NUM; ++i) {
+    offsets[i] = L.off[i];
+    if (sizes != nullptr) sizes[i] = L.size[i];
+  }
+  return MOE_OK;
+}
+
+int moe_align(const int32_t* topk_ids, int T, int K, int E, int block_m, int32_t* counts,
+              int32_t* offsets, int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
+              int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream) {
+  if (T < 0 || K <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128)
+    return MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(T) * K >= (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !counts || !offsets || !padded_offsets || !sorted_ids || !inv_perm ||
+      !block_info || !num_blocks)
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(block_info) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  return run_align(topk_ids, T, K, E, block_m, counts, offsets, padded_offsets, sorted_ids,
+                   inv_perm, block_info, num_blocks, dev_status,
+                   static_cast<cudaStream_t>(stream));
+}
+
+int moe_quantize_x_fp8(const void* x, int x_dtype, int T, int H, uint8_t* xq, float* row_scale,
+                       void* stream) {
+  if (T < 0 || H <= 0 || (H & 1) != 0) return MOE_ERR_INVALID_ARG;
+  if (x_dtype != MOE_BF16 && x_dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !xq || !row_scale) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_quantize_x(x, x_dtype, T, H, xq, row_scale, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_scale,
+                   const void* w13, const uint8_t* w13_scale, const int32_t* sorted_ids,
+                   const int32_t* block_info, const int32_t* num_blocks, void* h,
+                   int32_t* dev_status, void* stream) {
+  (void)x_row_scale;
+  (void)w13_scale;
+  int rc = check_problem(p);
+  if (rc != MOE_OK) return rc;
+  rc = check_gemm_shapes(p);
+  if (rc != MOE_OK) return rc;
+  if (p->T == 0) return MOE_OK;
+  if (!x || !w13 || !sorted_ids || !block_info || !num_blocks || !h) return MOE_ERR_INVALID_ARG;
+  return run_gemm1(p, x, w13, sorted_ids, block_info, num_blocks, h, dev_status,
+                   static_cast<cudaStream_t>(stream));
+}
+
+int moe_gemm2_weighted(const moe_problem_t* p, const void* h, const void* w2,
+                       const uint8_t* w2_scale, const float* topk_weights,
+                       const int32_t* sorted_ids, const int32_t* block_info,
+                       const int32_t* num_blocks, float* y, int k_splits, int32_t* dev_status,
+                       void* stream) {
+  (void)w2_scale;
+  int rc = check_problem(p);
+  if (rc != MOE_OK) return rc;
+  rc = check_gemm_shapes(p);
+  if (rc != MOE_OK) return rc;
+  const int bk = p->act == MOE_BF16 ? 64 : 32;
+  if (k_splits < 1 || k_splits > p->I / bk) return MOE_ERR_INVALID_ARG;
+  if (p->T == 0) return MOE_OK;
+  if (!h || !w2 || !topk_weights || !sorted_ids || !block_info || !num_blocks || !y)
+    return MOE_ERR_INVALID_ARG;
+  return run_gemm2(p, h, w2, topk_weights, sorted_ids, block_info, num_blocks, y, k_splits,
+                   dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int moe_combine(const float* y, int k_splits, size_t cap, const int32_t* inv_perm, int T, int K,
+                int H, int out_dtype, void* out, int32_t* dev_status, void* stream) {
+  if (T < 0 || K <= 0 || H <= 0 || k_splits < 1) return MOE_ERR_INVALID_ARG;
+  if (out_dtype != MOE_BF16 && out_dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (H % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y || !inv_perm || !out) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(y, k_splits, static_cast<long long>(cap), inv_perm, T, K, H,
+                                    out_dtype, out, dev_status,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
+                const float* topk_weights, const void* w13, const uint8_t* w13_scale,
+                const void* w2, const uint8_t* w2_scale, void* out, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  int rc = check_problem(p);
+  if (rc != MOE_OK) return rc;
+  rc = check_gemm_shapes(p);
+  if (rc != MOE_OK) return rc;
+  if (p->T == 0) return MOE_OK;
+  if (!x || !topk_ids || !topk_weights || !w13 || !w2 || !out || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  (void)w13_scale;
+  (void)w2_scale;
+  Layout L;
+  layout_of(p, &L);
+  if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto part = [&](int i) { return ws + L.off[i]; };
+  int32_t* status = reinterpret_cast<int32_t*>(part(MOE_WS_STATUS));
+  int32_t* sorted_ids = reinterpret_cast<int32_t*>(part(MOE_WS_SORTED_IDS));
+  int32_t* block_info = reinterpret_cast<int32_t*>(part(MOE_WS_BLOCK_INFO));
+  int32_t* num_blocks = reinterpret_cast<int32_t*>(part(MOE_WS_NUM_BLOCKS));
+  int32_t* inv_perm = reinterpret_cast<int32_t*>(part(MOE_WS_INV_PERM));
+  float* y = reinterpret_cast<float*>(part(MOE_WS_Y));
+  void* h = part(MOE_WS_H);
+  const int splits = default_splits(p);
+  const int bm = block_m_of(p);
+
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+  rc = run_align(topk_ids, p->T, p->K, p->E, bm, reinterpret_cast<int32_t*>(part(MOE_WS_COUNTS)),
+                 reinterpret_cast<int32_t*>(part(MOE_WS_OFFSETS)),
+                 reinterpret_cast<int32_t*>(part(MOE_WS_PADDED_OFFSETS)), sorted_ids, inv_perm,
+                 block_info, num_blocks, status, s);
+  if (rc != MOE_OK) return rc;
+  rc = run_gemm1(p, x, w13, sorted_ids, block_info, num_blocks, h, status, s);
+  if (rc != MOE_OK) return rc;
+  rc = run_gemm2(p, h, w2, topk_weights, sorted_ids, block_info, num_blocks, y, splits, status, s);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(launch_combine(y, splits, capacity(p->T, p->K, p->E, bm), inv_perm, p->T,
+                                    p->K, p->H, p->act, out, status, s));
+}
+
+int moe_get_device_status(const int32_t* dev_status, void* stream) {
+  if (dev_status == nullptr) return MOE_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return v == 0 ? MOE_OK : v;
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+"""Helpers for the GPU parity tests: input preparation for the oracle and the
+comparison rule.  The oracle gets host copies of the very inputs the GPU got;
+nothing the CUDA path computes is fed to the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from mixture_experts_grouped_02_gb300 import inputs as gen
+
+# bf16 (and tf32) output bounds stated for the workload: max-abs 2e-2 and
+# relative L2 1e-2 against the fp64 oracle.
+MAX_ABS = 2e-2
+REL_L2 = 1e-2
+
+
+def np_store(t):
+    return gen.to_numpy_storage(t)
+
+
+def generate(cfg, seed=0, device="cuda"):
+    return gen.generate(cfg, seed=seed, device=device)
+
+
+def oracle_problem(inp: gen.MoEInputs, E=None, quantize_x=False, h_e4m3=False, h_scale=1.0):
+    c = inp.cfg
+    xs = np_store(inp.x[:1])
+    ws = np_store(inp.w13[:1])
+    return oracle.make_problem(c.T, c.H, c.I, c.E if E is None else E, c.K, xs, ws,
+                               quantize_x=quantize_x, h_e4m3=h_e4m3, h_scale=h_scale)
+
+
+def oracle_forward_tokens(inp: gen.MoEInputs, tokens, mode=oracle.EXACT, **kw):
+    """Oracle output rows for `tokens`, copying to the host only the experts
+    those tokens use (ids are renumbered into that subset)."""
+    tokens = np.asarray(tokens, np.int32)
+    ids = inp.topk_ids.cpu().numpy()
+    used = np.unique(ids[tokens])
+    remap = np.full(inp.cfg.E, -1, np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    sub_ids = remap[ids]
+    sub_ids[sub_ids < 0] = 0  # rows of tokens not evaluated
+    sel = torch.as_tensor(used, device=inp.w13.device, dtype=torch.long)
+    w13 = np_store(inp.w13.index_select(0, sel))
+    w2 = np_store(inp.w2.index_select(0, sel))
+    s13 = None if inp.w13_scale is None else np_store(inp.w13_scale.index_select(0, sel))
+    s2 = None if inp.w2_scale is None else np_store(inp.w2_scale.index_select(0, sel))
+    P = oracle_problem(inp, E=len(used), **kw)
+    return oracle.forward(P, np_store(inp.x), sub_ids, inp.topk_weights.cpu().numpy(), w13, w2,
+                          s13, s2, mode=mode, tokens=tokens)
+
+
+def errors(gpu: torch.Tensor, ref: np.ndarray):
+    g = gpu.detach().to(torch.float64).cpu().numpy()
+    diff = g - ref
+    max_abs = float(np.abs(diff).max()) if diff.size else 0.0
+    denom = float(np.linalg.norm(ref))
+    rel = float(np.linalg.norm(diff) / denom) if denom > 0 else float(np.linalg.norm(diff))
+    return max_abs, rel
+
+
+def assert_close(gpu, ref, max_abs=MAX_ABS, rel_l2=REL_L2, what=""):
+    assert np.all(np.isfinite(gpu.detach().float().cpu().numpy())), f"{what}: non-finite output"
+    m, r = errors(gpu, ref)
+    assert m <= max_abs and r <= rel_l2, f"{what}: max-abs {m:.3g} (<= {max_abs}), " \
+                                         f"rel-L2 {r:.3g} (<= {rel_l2})"
+    return m, r
+
+
+def sample_tokens(T, n, seed=0):
+    rng = np.random.default_rng(seed)
+    picks = {0, T - 1}
+    while len(picks) < min(n, T):
+        picks.add(int(rng.integers(0, T)))
+    return np.array(sorted(picks), np.int32)

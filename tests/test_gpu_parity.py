@@ -1,0 +1,264 @@
+"""GPU parity: every stage of the CUDA path, called through the C ABI, against
+the fp64 CPU oracle on the same seeded inputs.
+
+Integer outputs (align) must match bit for bit; floating-point outputs must be
+within max-abs 2e-2 and relative L2 1e-2 of the oracle (bf16 and tf32)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_pins as pins
+from gpu_util import (assert_close, errors, generate, np_store, oracle_forward_tokens,
+                      oracle_problem, sample_tokens)
+import mixture_experts_grouped_02_gb300 as moe
+from mixture_experts_grouped_02_gb300 import _abi
+from mixture_experts_grouped_02_gb300 import inputs as gen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    _abi.lib()
+    yield
+    torch.cuda.synchronize()
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+# ------------------------------------------------------------------ align
+
+EXTRA_ALIGN = [(1, 8, 256, 128, "normal"), (3, 2, 1000, 16, "normal"),
+               (2000, 4, 1024, 64, "normal"), (4096, 2, 8, 128, "normal")]
+
+
+@pytest.mark.parametrize("case", pins.ALIGN_CASES + EXTRA_ALIGN,
+                         ids=lambda c: "T%d_K%d_E%d_bm%d_%s" % c)
+def test_align_bit_exact(case):
+    T, K, E, bm, kind = case
+    ids = pins.align_ids(T, K, E, kind)
+    ref = oracle.align(ids, E, bm)
+    st = _status()
+    got = moe.align(torch.from_numpy(ids).cuda(), E, bm, dev_status=st)
+    assert moe.moe_get_device_status(st) == 0
+    for k in ("counts", "offsets", "padded_offsets", "sorted_ids", "inv_perm"):
+        assert np.array_equal(got[k].cpu().numpy(), ref[k]), k
+    assert np.array_equal(got["block_info"].cpu().numpy(), ref["block_info"])
+    assert int(got["num_blocks"].item()) == ref["num_blocks"]
+
+
+def test_align_skewed_dsv3_routing():
+    cfg = gen.config("dsv3_prefill")
+    ids, _ = gen.route(gen.router_logits(cfg, 0), cfg.K)
+    ref = oracle.align(ids.numpy(), cfg.E, 128)
+    got = moe.align(ids.cuda(), cfg.E, 128)
+    assert (ref["counts"] == 0).sum() >= 0
+    for k in ("counts", "offsets", "padded_offsets", "sorted_ids", "inv_perm", "block_info"):
+        assert np.array_equal(got[k].cpu().numpy(), ref[k]), k
+
+
+def test_align_bad_id_sets_status():
+    ids = torch.tensor([[0, 1], [2, 9], [3, 4]], dtype=torch.int32, device="cuda")
+    st = _status()
+    got = moe.align(ids, 8, 16, dev_status=st)
+    assert moe.moe_get_device_status(st) == _abi.MOE_ERR_DEVICE_BAD_ID
+    assert int(got["num_blocks"].item()) == 0
+
+
+# ------------------------------------------------------------------ stages
+
+STAGE_CASES = [
+    # T, H, I, E, K, dtype
+    (300, 256, 320, 3, 2, "bf16"),   # 2 blocks per expert, ragged I tile
+    (77, 192, 256, 5, 2, "bf16"),
+    (40, 128, 256, 8, 2, "f32"),     # tf32 path
+]
+
+
+def _valid_rows(al, na):
+    s = al["sorted_ids"]
+    rows = np.nonzero(s < na)[0].astype(np.int32)
+    return rows
+
+
+def _expert_of_rows(al, rows, ids_flat):
+    return ids_flat[al["sorted_ids"][rows]].astype(np.int32)
+
+
+@pytest.mark.parametrize("case", STAGE_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s" % c)
+def test_gemm1_silu_stage(case):
+    T, H, I, E, K, dt = case
+    cfg = gen.MoEConfig("stage", T, H, I, E, K, dt, "normal")
+    inp = gen.generate(cfg, seed=21)
+    d = inp.to("cuda")
+    al_ref = oracle.align(inp.topk_ids.numpy(), E, 128)
+    al = moe.align(d.topk_ids, E, 128)
+    p = moe.make_problem(T, H, I, E, K, dt)
+    cap = moe.moe_align_capacity(T, K, E, 128)
+    h = torch.full((cap, I), float("nan"), dtype=d.x.dtype, device="cuda")
+    st = _status()
+    moe.moe_gemm1_silu(p, d.x, None, d.w13, None, al["sorted_ids"], al["block_info"],
+                       al["num_blocks"], h, st)
+    assert moe.moe_get_device_status(st) == 0
+    rows = _valid_rows(al_ref, T * K)
+    eor = _expert_of_rows(al_ref, rows, inp.topk_ids.numpy().ravel())
+    ref = oracle.gemm1_silu_rows(oracle_problem(inp), np_store(inp.x), np_store(inp.w13),
+                                 al_ref["sorted_ids"], eor, rows)
+    got = h[torch.from_numpy(rows).long().cuda()]
+    assert_close(got, ref, what="h")
+    # padding rows are never written
+    pad = np.nonzero(al_ref["sorted_ids"] >= T * K)[0]
+    if len(pad):
+        assert torch.isnan(h[torch.from_numpy(pad).long().cuda()].float()).all()
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3])
+@pytest.mark.parametrize("case", STAGE_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s" % c)
+def test_gemm2_weighted_stage(case, splits):
+    T, H, I, E, K, dt = case
+    cfg = gen.MoEConfig("stage", T, H, I, E, K, dt, "normal")
+    inp = gen.generate(cfg, seed=22)
+    d = inp.to("cuda")
+    cap = moe.moe_align_capacity(T, K, E, 128)
+    g = torch.Generator().manual_seed(5)
+    hin = torch.randn((cap, I), generator=g).to(inp.x.dtype)  # synthetic hidden rows
+    al_ref = oracle.align(inp.topk_ids.numpy(), E, 128)
+    al = moe.align(d.topk_ids, E, 128)
+    p = moe.make_problem(T, H, I, E, K, dt)
+    y = torch.full((splits, cap, H), float("nan"), dtype=torch.float32, device="cuda")
+    st = _status()
+    moe.moe_gemm2_weighted(p, hin.cuda(), d.w2, None, d.topk_weights, al["sorted_ids"],
+                           al["block_info"], al["num_blocks"], y, splits, st)
+    assert moe.moe_get_device_status(st) == 0
+    rows = _valid_rows(al_ref, T * K)
+    eor = _expert_of_rows(al_ref, rows, inp.topk_ids.numpy().ravel())
+    ref = oracle.gemm2_weighted_rows(oracle_problem(inp), np_store(hin), np_store(inp.w2),
+                                     inp.topk_weights.numpy(), al_ref["sorted_ids"], eor, rows)
+    got = y[:, torch.from_numpy(rows).long().cuda()].sum(0)
+    tol = 1e-4 if dt == "bf16" else 5e-3  # bf16 products are exact; tf32 rounds operands
+    assert_close(got, ref, max_abs=2e-2, rel_l2=tol, what="y")
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_combine_stage(splits, out_dtype):
+    T, K, E, H = 50, 3, 7, 96
+    ids = pins.align_ids(T, K, E, "normal", seed=3)
+    al_ref = oracle.align(ids, E, 16)
+    cap = moe.moe_align_capacity(T, K, E, 16)
+    g = torch.Generator().manual_seed(6)
+    y = torch.randn((cap, H), generator=g)
+    ref = oracle.combine(y.numpy(), al_ref["inv_perm"], T, K, H)
+    # two splits holding y/2 each sum to y exactly
+    ys = (y / splits).unsqueeze(0).repeat(splits, 1, 1).contiguous().cuda()
+    inv = torch.from_numpy(al_ref["inv_perm"]).cuda()
+    out = torch.empty((T, H), dtype=out_dtype, device="cuda")
+    moe.moe_combine(ys, splits, cap, inv, T, K, H, moe.dtype_code(out_dtype), out)
+    torch.cuda.synchronize()
+    tol = 1e-6 if out_dtype == torch.float32 else 8e-3
+    assert_close(out, ref, max_abs=2e-2, rel_l2=tol, what="out")
+
+
+# ------------------------------------------------------------------ forward
+
+FORWARD_CASES = [
+    # T, H, I, E, K, dtype, routing
+    (300, 256, 320, 3, 2, "bf16", "normal"),
+    (64, 320, 256, 16, 4, "bf16", "zipf"),     # ragged H tile, empty experts
+    (1, 256, 256, 8, 2, "bf16", "normal"),
+    (513, 128, 128, 2, 1, "bf16", "normal"),   # top-1
+    (33, 128, 256, 8, 2, "f32", "normal"),
+]
+
+
+def _run_forward(d, cfg, poison=True):
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype)
+    ws = moe.Workspace(p)
+    if poison:
+        ws.buffer.fill_(0xFF)  # NaN patterns everywhere the path does not write
+    out = torch.full((cfg.T, cfg.H), float("nan"), dtype=d.x.dtype, device="cuda")
+    moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, d.w13, None, d.w2, None, out, ws.buffer,
+                    ws.nbytes)
+    assert moe.moe_get_device_status(ws.status) == 0
+    return out, ws
+
+
+@pytest.mark.parametrize("case", FORWARD_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s_%s" % c)
+def test_forward_small(case):
+    cfg = gen.MoEConfig("fwd", *case)
+    inp = gen.generate(cfg, seed=31)
+    out, ws = _run_forward(inp.to("cuda"), cfg)
+    ref = oracle_forward_tokens(inp, np.arange(cfg.T))
+    assert_close(out, ref, what=cfg.name)
+
+
+def test_forward_tiny_config():
+    cfg = gen.config("tiny")
+    inp = gen.generate(cfg, seed=0)
+    out, _ = _run_forward(inp.to("cuda"), cfg)
+    ref = oracle_forward_tokens(inp, np.arange(cfg.T))
+    assert_close(out, ref, what="tiny")
+
+
+def test_forward_deterministic_and_padding_untouched():
+    cfg = gen.MoEConfig("fwd", 300, 256, 320, 3, 2, "bf16", "normal")
+    d = gen.generate(cfg, seed=32).to("cuda")
+    out1, ws = _run_forward(d, cfg)
+    out2, _ = _run_forward(d, cfg)
+    assert torch.equal(out1, out2)
+    h = ws.part(_abi.MOE_WS_H, torch.uint8)
+    cap = moe.moe_align_capacity(cfg.T, cfg.K, cfg.E, 128)
+    h = h[:cap * cfg.I * 2].view(cap, cfg.I * 2)
+    s = ws.part(_abi.MOE_WS_SORTED_IDS, torch.int32)[:cap].cpu().numpy()
+    pad = np.nonzero(s >= cfg.T * cfg.K)[0]
+    assert len(pad) > 0
+    assert (h[torch.from_numpy(pad).long().cuda()] == 0xFF).all()
+
+
+def test_forward_status_blocks_later_stages():
+    cfg = gen.MoEConfig("fwd", 64, 128, 128, 4, 2, "bf16", "normal")
+    d = gen.generate(cfg, seed=33).to("cuda")
+    d.topk_ids[5, 1] = 4  # outside [0, E)
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype)
+    ws = moe.Workspace(p)
+    out = torch.zeros((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, d.w13, None, d.w2, None, out, ws.buffer,
+                    ws.nbytes)
+    assert moe.moe_get_device_status(ws.status) == _abi.MOE_ERR_DEVICE_BAD_ID
+    assert (out == 0).all()  # combine did not run
+
+
+def test_forward_zero_tokens():
+    p = moe.make_problem(0, 128, 128, 4, 2, "bf16")
+    moe.moe_forward(p, 0, 0, 0, 0, None, 0, None, 0, 0, 0)
+
+
+# ------------------------------------------------------------- full sizes
+
+@pytest.mark.parametrize("name", [f"mixtral_decode_T{t}" for t in gen.DECODE_T] +
+                         [f"dsv3_decode_T{t}" for t in gen.DECODE_T])
+def test_forward_decode_full_size(name):
+    cfg = gen.config(name)
+    inp = generate(cfg, seed=0, device="cuda")
+    out, _ = _run_forward(inp, cfg, poison=False)
+    toks = sample_tokens(cfg.T, 8)
+    ref = oracle_forward_tokens(inp, toks)
+    assert_close(out[torch.from_numpy(toks).long().cuda()], ref, what=name)
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "dsv3_prefill"])
+def test_forward_prefill_full_size_sampled(name):
+    cfg = gen.config(name)
+    inp = generate(cfg, seed=0, device="cuda")
+    out, _ = _run_forward(inp, cfg, poison=False)
+    toks = sample_tokens(cfg.T, 6, seed=1)
+    ref = oracle_forward_tokens(inp, toks)
+    assert_close(out[torch.from_numpy(toks).long().cuda()], ref, what=name)
+    assert torch.isfinite(out.float()).all()
+    del inp, out
+    torch.cuda.empty_cache()
