@@ -109,7 +109,12 @@ def test_gemm1_silu_stage(case):
     ref = oracle.gemm1_silu_rows(oracle_problem(inp), np_store(inp.x), np_store(inp.w13),
                                  al_ref["sorted_ids"], eor, rows)
     got = h[torch.from_numpy(rows).long().cuda()]
-    assert_close(got, ref, what="h")
+    # h is stored in bf16 (tf32 operands in the f32 case): besides the bounds on
+    # the layer output, each element may carry one rounding of relative size
+    # 2^-8, which exceeds 2e-2 for |h| > 5.
+    g = got.double().cpu().numpy()
+    assert np.all(np.abs(g - ref) <= 2e-2 + 2.0 ** -8 * np.abs(ref)), np.abs(g - ref).max()
+    assert_close(got, ref, max_abs=np.inf, what="h")
     # padding rows are never written
     pad = np.nonzero(al_ref["sorted_ids"] >= T * K)[0]
     if len(pad):
