@@ -2,9 +2,10 @@
 //
 // One persistent, warp-specialised kernel template serves both:
 //
-//  * gate/up (GEMM1): A = 128 token rows gathered by index from x
-//    (TMA tile::gather4, four rows per instruction, one row index per
-//    sorted slot), B = 128 gate rows and the 128 matching up rows of w13[e]
+//  * gate/up (GEMM1): A = 128 token rows gathered by index from x by four
+//    producer warps (16-byte cp.async per lane, eight lanes per 128-byte row,
+//    written straight into the 128-byte swizzled layout, then a proxy fence
+//    and an mbarrier arrive), B = 128 gate rows and the 128 matching up rows of w13[e]
 //    stacked into one 256-row operand, so a single M=128 x N=256 MMA puts
 //    gate in accumulator columns 0..127 and up in 128..255 of the same TMEM
 //    lane.  The epilogue forms SiLU(gate) * up per lane and stores h.
@@ -18,9 +19,10 @@
 //    triton kernel use tma", review comment on TOKEN_INPUT_USE_TMA /
 //    MUL_ROUTED_WEIGHT.
 //
-// Roles (192 threads): warp 0 loads (TMA), warp 1 issues tcgen05.mma from one
-// thread and owns the TMEM allocation, warps 2-5 run the epilogue (warp w
-// reads TMEM lanes 32*(w%4) .. +31).  A 4-stage shared-memory ring of
+// Roles: the first P warps load (P = 4 for gate/up: the gather plus the TMA of
+// the weight tiles; P = 1 for down: TMA only), warp P issues tcgen05.mma from
+// one thread and owns the TMEM allocation, warps P+1 .. P+4 run the epilogue
+// (warp w reads TMEM lanes 32*(w%4) .. +31).  A 4-stage shared-memory ring of
 // 48 KB stages (16 KB A + 32 KB B, 128-byte swizzled K-major rows) is handed
 // over with full/empty mbarriers; two 256-column fp32 accumulators in TMEM
 // let the epilogue of one tile overlap the MMAs of the next.  Tiles are
@@ -67,7 +69,14 @@ struct Cfg {
   static constexpr int kTmemCols = 2 * kAccCols;          // two accumulators
   static constexpr uint32_t kIdesc = make_idesc(Elem<T>::kFmt, kBM, kBN);
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
-  static constexpr int kThreads = 192;
+  static constexpr int kProducerWarps = KIND == kGateUp ? 4 : 1;
+  static constexpr int kMmaWarp = kProducerWarps;
+  static constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
+  // gate/up: each producer thread marks a stage full only once its cp.async
+  // group for that stage has landed, kGatherLag stages after issuing it
+  static constexpr int kGatherLag = 2;
+  static constexpr uint32_t kFullArrivals = KIND == kGateUp ? kProducerWarps * 32 + 1 : 1;
+  static constexpr uint32_t kTxBytes = KIND == kGateUp ? kBBytes : kStageBytes;
 };
 
 struct Tile {
@@ -119,7 +128,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 }
 
 template <int KIND, typename T>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(Cfg<KIND, T>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB) {
   using C = Cfg<KIND, T>;
@@ -143,7 +152,7 @@ __global__ void __launch_bounds__(192, 1)
     s_skip = (a.status != nullptr && *reinterpret_cast<volatile int32_t*>(a.status) != 0);
     s_abort = 0;
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&full_bar[i]), C::kFullArrivals);
       mbar_init(smem_u32(&empty_bar[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -156,9 +165,9 @@ __global__ void __launch_bounds__(192, 1)
   }
   __syncthreads();
   if (s_skip) return;
-  if (warp == 1) tmem_alloc(smem_u32(&s_tmem_base), C::kTmemCols);
+  if (warp == C::kMmaWarp) tmem_alloc(smem_u32(&s_tmem_base), C::kTmemCols);
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
+    if constexpr (KIND == kDown) tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
   tc_fence_before_sync();
@@ -170,27 +179,89 @@ __global__ void __launch_bounds__(192, 1)
   const int total = num_blocks * a.n_tiles * a.splits;
   const uint64_t to = a.timeout_ns;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp < C::kProducerWarps) {
+    if constexpr (KIND == kGateUp) {
+      // -------------------------------------------------- gather producer
+      // thread pt copies 16-byte chunk (pt % 8) of rows pt/8 + 16 j, j < 8,
+      // into the swizzled A tile: chunk c of row r sits at chunk c ^ (r % 8)
+      const int pt = threadIdx.x;
+      const int chunk = pt & 7;
+      const int row0 = pt >> 3;
+      constexpr int kElemsPerChunk = 16 / sizeof(T);
+      const T* x = static_cast<const T*>(a.x);
+      uint32_t stage = 0, phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(tile, num_blocks, a);
+        const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
+        const int e = bi.x, r0 = bi.z, valid = bi.w;
+        int kb, ke;
+        split_range(a, t.split, kb, ke);
+        const T* src[8];
+        uint32_t dst_off[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = row0 + 16 * j;
+          // padding slots read token 0; their products are never stored
+          const int tok = r < valid ? a.sorted_ids[r0 + r] / a.K : 0;
+          src[j] = x + static_cast<long long>(tok) * a.H + chunk * kElemsPerChunk;
+          dst_off[j] = r * C::kRowBytes + ((chunk ^ (r & 7)) << 4);
+        }
+        for (int kt = kb; kt < ke; ++kt) {
+          if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, to)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          if (pt == 0) {
+            mbar_arrive_expect_tx(fb, C::kTxBytes);
+            const uint32_t b_dst = smemB + stage * C::kBBytes;
+            const int grow = e * 2 * a.I + t.nt * 128;
+            tma_load_2d(b_dst, &tmB, fb, kt * C::kBK, grow);
+            tma_load_2d(b_dst + 128 * C::kRowBytes, &tmB, fb, kt * C::kBK, grow + a.I);
+          }
+          const uint32_t a_dst = smemA + stage * C::kABytes;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) cp_async_16(a_dst + dst_off[j], src[j] + kt * C::kBK);
+          cp_async_commit();
+          ++issued;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (issued > C::kGatherLag) {
+            // the group issued kGatherLag stages ago has landed: publish it to
+            // the tensor core (async proxy) and mark it full
+            cp_async_wait<C::kGatherLag>();
+            fence_proxy_async_smem();
+            const long long n = issued - 1 - C::kGatherLag;
+            mbar_arrive(smem_u32(&full_bar[n % C::kStages]));
+          }
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      for (long long n = issued > C::kGatherLag ? issued - C::kGatherLag : 0; n < issued; ++n)
+        mbar_arrive(smem_u32(&full_bar[n % C::kStages]));
+      if (!ok && pt == 0) {
+        // let the weight copies already issued land before the CTA exits
+        const long long first = issued > C::kStages ? issued - C::kStages : 0;
+        for (long long n = first; n < issued; ++n)
+          drain_wait(smem_u32(&full_bar[n % C::kStages]),
+                     static_cast<uint32_t>((n / C::kStages) & 1), to / 4);
+      }
+    } else {
+    // ---------------------------------------------------------- TMA producer
     uint32_t stage = 0, phase = 0;
     long long issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const Tile t = decode_tile(tile, num_blocks, a);
       const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
-      const int e = bi.x, r0 = bi.z, valid = bi.w;
+      const int e = bi.x, r0 = bi.z;
       int kb, ke;
       split_range(a, t.split, kb, ke);
-      int rows[4] = {0, 0, 0, 0};
-      if constexpr (KIND == kGateUp) {
-        // token row of each of this lane's four slots; padding slots read
-        // token 0 (their products are never stored)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = lane * 4 + q;
-          if (r < valid) rows[q] = a.sorted_ids[r0 + r] / a.K;
-        }
-      }
       for (int kt = kb; kt < ke; ++kt) {
         int good = 1;
         if (lane == 0) good = mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, to);
@@ -199,25 +270,11 @@ __global__ void __launch_bounds__(192, 1)
           ok = false;
           break;
         }
-        const uint32_t fb = smem_u32(&full_bar[stage]);
-        if (lane == 0) mbar_arrive_expect_tx(fb, C::kStageBytes);
-        __syncwarp();
-        const uint32_t a_dst = smemA + stage * C::kABytes;
-        const uint32_t b_dst = smemB + stage * C::kBBytes;
-        const int kcol = kt * C::kBK;
-        if constexpr (KIND == kGateUp) {
-          tma_gather4(a_dst + lane * 4 * C::kRowBytes, &tmA, fb, kcol, rows[0], rows[1], rows[2],
-                      rows[3]);
-          if (lane == 0) {
-            const int grow = e * 2 * a.I + t.nt * 128;
-            tma_load_2d(b_dst, &tmB, fb, kcol, grow);
-            tma_load_2d(b_dst + 128 * C::kRowBytes, &tmB, fb, kcol, grow + a.I);
-          }
-        } else {
-          if (lane == 0) {
-            tma_load_2d(a_dst, &tmA, fb, kcol, r0);
-            tma_load_2d(b_dst, &tmB, fb, kcol, e * a.H + t.nt * C::kBN);
-          }
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          mbar_arrive_expect_tx(fb, C::kTxBytes);
+          tma_load_2d(smemA + stage * C::kABytes, &tmA, fb, kt * C::kBK, r0);
+          tma_load_2d(smemB + stage * C::kBBytes, &tmB, fb, kt * C::kBK, e * a.H + t.nt * C::kBN);
         }
         ++issued;
         if (++stage == C::kStages) {
@@ -233,7 +290,8 @@ __global__ void __launch_bounds__(192, 1)
         drain_wait(smem_u32(&full_bar[n % C::kStages]),
                    static_cast<uint32_t>((n / C::kStages) & 1), to / 4);
     }
-  } else if (warp == 1) {
+    }
+  } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -376,7 +434,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && s_abort) report_error(a.status, MOE_ERR_TIMEOUT);
-  if (warp == 1) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }

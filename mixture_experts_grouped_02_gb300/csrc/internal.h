@@ -41,6 +41,7 @@ struct GemmArgs {
   int splits;    // reduction splits (down projection); 1 for gate/up
   int band;      // N tiles per raster band
   long long cap; // rows of the padded sorted list
+  const void* x;               // gate/up: token rows (T, H), gathered by cp.async
   const int32_t* sorted_ids;
   const int32_t* block_info;
   const int32_t* num_blocks;
@@ -57,8 +58,8 @@ cudaError_t launch_combine(const float* y, int splits, long long cap, const int3
 cudaError_t launch_quantize_x(const void* x, int x_dtype, int T, int H, uint8_t* xq,
                               float* row_scale, cudaStream_t s);
 
-// dtype: MOE_BF16 or MOE_F32.  tmA: gate/up -> x rows (box 1 row, gather4);
-// down -> h (box 128 rows).  tmB: w13 (box 128 rows) / w2 (box 256 rows).
+// dtype: MOE_BF16 or MOE_F32.  tmA: down -> h (box 128 rows; unused by
+// gate/up, which gathers x itself).  tmB: w13 (box 128 rows) / w2 (box 256 rows).
 cudaError_t launch_gemm_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmA,
                                 const CUtensorMap& tmB, int grid, cudaStream_t s);
 cudaError_t launch_gemm_down(int dtype, const GemmArgs& a, const CUtensorMap& tmA,

@@ -231,11 +231,12 @@ int run_gemm1(const moe_problem_t* p, const void* x, const void* w13, const int3
   a.num_blocks = num_blocks;
   a.out = h;
   a.status = status;
-  CUtensorMap tmA, tmB;
-  int rc = make_map(&tmA, p->act, x, p->H, p->T, bk, 1);
+  a.x = x;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  CUtensorMap tmB;
+  const int rc = make_map(&tmB, p->act, w13, p->H, 2ll * p->I * p->E, bk, 128);
   if (rc != MOE_OK) return rc;
-  rc = make_map(&tmB, p->act, w13, p->H, 2ll * p->I * p->E, bk, 128);
-  if (rc != MOE_OK) return rc;
+  const CUtensorMap& tmA = tmB;  // the gate/up kernel gathers x without a tensor map
   const long long max_tiles = (a.cap / kBlockM) * a.n_tiles;
   const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
   return cuda_status(launch_gemm_gate_up(p->act, a, tmA, tmB, grid, s));
