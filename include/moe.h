@@ -220,6 +220,31 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                 const void* w2, const uint8_t* w2_scale, void* out, void* workspace,
                 size_t workspace_bytes, void* stream);
 
+/* ---- the whole forward without a caller workspace ---------------------------
+ * No counterpart on the pages: an addition of this library for callers that
+ * cannot allocate device memory where they run the layer (a host framework
+ * that owns and pre-carves all device memory, a serving loop that must not
+ * allocate after start-up, a caller with no room to keep a workspace).
+ * Same arguments and result as moe_forward, minus the workspace: the
+ * intermediates go to one static device array of MOE_STATIC_SCRATCH_BYTES
+ * inside the library, held on every GPU that loads it until the process
+ * exits.  Allocates nothing (no cudaMalloc, no allocating library call).
+ *  - Problems whose moe_workspace_size exceeds MOE_STATIC_SCRATCH_BYTES are
+ *    rejected with MOE_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls on a device share the array, which keeps the last call's
+ *    contents; the status word that must start at zero is cleared by each
+ *    call.  Calls whose execution overlaps on the GPU race on the array:
+ *    issue them in one stream order.
+ * The device status word of the last call is at offset 0 of the array and
+ * is reported by the call's own errors only; use moe_forward with a
+ * workspace to read it with moe_get_device_status. */
+#define MOE_STATIC_SCRATCH_BYTES (64u << 20)
+int moe_forward_noalloc(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
+                        const float* topk_weights, const void* w13, const uint8_t* w13_scale,
+                        const void* w2, const uint8_t* w2_scale, void* out, void* stream);
+
 /* Synchronise `stream` and return the device status word at dev_status
  * (MOE_OK when it is 0), or MOE_ERR_CUDA if the stream itself failed. */
 int moe_get_device_status(const int32_t* dev_status, void* stream);

@@ -34,7 +34,9 @@ MOE_F32, MOE_BF16, MOE_E4M3, MOE_E2M1_MX = 0, 1, 2, 3
 EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_align_capacity",
            "moe_gemm2_default_splits", "moe_workspace_size", "moe_workspace_offsets", "moe_align",
            "moe_quantize_x_fp8", "moe_gemm1_silu", "moe_gemm2_weighted", "moe_combine",
-           "moe_forward", "moe_get_device_status")
+           "moe_forward", "moe_forward_noalloc", "moe_get_device_status")
+
+MOE_STATIC_SCRATCH_BYTES = 64 << 20
 
 
 class MoEError(RuntimeError):
@@ -103,6 +105,8 @@ def _declare(L):
     L.moe_combine.argtypes = [vp, i32, sz, vp, i32, i32, i32, i32, vp, vp, vp]
     L.moe_forward.restype = i32
     L.moe_forward.argtypes = [PP] + [vp] * 9 + [sz, vp]
+    L.moe_forward_noalloc.restype = i32
+    L.moe_forward_noalloc.argtypes = [PP] + [vp] * 9
     L.moe_get_device_status.restype = i32
     L.moe_get_device_status.argtypes = [vp, vp]
 
@@ -210,6 +214,16 @@ def moe_forward(p: Problem, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_sc
     _check(lib().moe_forward(ctypes.byref(p), _p(x), _p(topk_ids), _p(topk_weights), _p(w13),
                              _p(w13_scale), _p(w2), _p(w2_scale), _p(out), _p(workspace),
                              int(workspace_bytes), _stream(stream)), "moe_forward")
+
+
+def moe_forward_noalloc(p: Problem, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
+                        out, stream=None):
+    """moe_forward with the intermediates in the library's static scratch
+    array (MOE_STATIC_SCRATCH_BYTES per GPU) instead of a workspace: for
+    callers that cannot allocate device memory where they run the layer."""
+    _check(lib().moe_forward_noalloc(ctypes.byref(p), _p(x), _p(topk_ids), _p(topk_weights),
+                                     _p(w13), _p(w13_scale), _p(w2), _p(w2_scale), _p(out),
+                                     _stream(stream)), "moe_forward_noalloc")
 
 
 def moe_get_device_status(dev_status, stream=None) -> int:
