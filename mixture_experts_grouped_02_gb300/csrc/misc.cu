@@ -12,8 +12,9 @@ namespace {
 // one rounding to the output type.  Source: the index_add of the "Current
 // PyTorch path" in "factor_moe_fused_gemm.cu" and its
 // weighted_scatter_add_kernel, made deterministic: each token owns its row,
-// so no atomics and a fixed summation order.  One CTA per token row (grid
-// stride), 16-byte loads of y.
+// so no atomics and a fixed summation order.  CTA (x, y) handles token rows
+// x, x + gridDim.x, ... and the y-th run of 1024 columns of them, so that a
+// handful of tokens still spreads over many SMs; 16-byte loads of y.
 template <typename OutT>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int splits,
                                                       long long cap,
@@ -22,9 +23,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int32_t* status) {
   if (status != nullptr && *status != 0) return;
   const int h4 = H >> 2;
+  const int c_end = min(h4, static_cast<int>(blockIdx.y + 1) * 256);
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     const int32_t* slots = inv_perm + static_cast<long long>(t) * K;
-    for (int c = threadIdx.x; c < h4; c += blockDim.x) {
+    for (int c = blockIdx.y * 256 + threadIdx.x; c < c_end; c += blockDim.x) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int k = 0; k < K; ++k) {
         const long long row = slots[k];
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(256) quantize_x_kernel(const void* __restrict_
 cudaError_t launch_combine(const float* y, int splits, long long cap, const int32_t* inv_perm,
                            int T, int K, int H, int out_dtype, void* out, int32_t* status,
                            cudaStream_t s) {
-  const int grid = T < 65535 ? T : 65535;
+  const dim3 grid(T < 65535 ? T : 65535, (H / 4 + 255) / 256);
   if (out_dtype == MOE_BF16)
     combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(y, splits, cap, inv_perm, T, K, H,
                                                         reinterpret_cast<__nv_bfloat16*>(out),

@@ -267,3 +267,26 @@ def test_forward_prefill_full_size_sampled(name):
     assert torch.isfinite(out.float()).all()
     del inp, out
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------- fp8 step
+
+@pytest.mark.parametrize("shape", [(2048, 2880), (1, 64), (37, 4096)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_quantize_x_fp8_bit_exact(shape, dtype):
+    """e4m3 codes and fp32 row scales match the oracle bit for bit: both sides
+    form amax/448 and x/s in fp32 and round to nearest-even, saturating."""
+    T, H = shape
+    g = torch.Generator().manual_seed(T + H)
+    x = torch.randn((T, H), generator=g) * torch.logspace(-3, 3, T).unsqueeze(1)
+    if T > 2:
+        x[1] = 0.0  # all-zero row: scale 1
+        x[2, :5] = torch.tensor([1e30, -1e30, 0.5, -0.0, 3.0])  # extreme row
+    x = x.to(dtype)
+    xq_ref, s_ref = oracle.quantize_x_fp8(np_store(x))
+    xq = torch.empty((T, H), dtype=torch.uint8, device="cuda")
+    s = torch.empty(T, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_x_fp8(x.cuda(), moe.dtype_code(dtype), T, H, xq, s)
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
