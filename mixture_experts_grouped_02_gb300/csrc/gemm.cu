@@ -37,6 +37,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace moe {
 namespace {
@@ -79,37 +80,6 @@ struct Cfg {
   static constexpr uint32_t kTxBytes = KIND == kGateUp ? kBBytes : kStageBytes;
 };
 
-struct Tile {
-  int mb, nt, split;
-};
-
-__device__ __forceinline__ Tile decode_tile(int tile, int num_blocks, const GemmArgs& a) {
-  Tile t;
-  const int per_split = num_blocks * a.n_tiles;
-  t.split = tile / per_split;
-  const int rem = tile - t.split * per_split;
-  const int band = a.band;
-  const int full_bands = a.n_tiles / band;
-  const int band_tiles = num_blocks * band;
-  const int b = rem / band_tiles;
-  if (b < full_bands) {
-    const int w = rem - b * band_tiles;
-    t.mb = w / band;
-    t.nt = b * band + w % band;
-  } else {
-    const int tail = a.n_tiles - full_bands * band;
-    const int w = rem - full_bands * band_tiles;
-    t.mb = w / tail;
-    t.nt = full_bands * band + w % tail;
-  }
-  return t;
-}
-
-__device__ __forceinline__ void split_range(const GemmArgs& a, int split, int& kb, int& ke) {
-  kb = static_cast<int>((static_cast<long long>(a.k_tiles) * split) / a.splits);
-  ke = static_cast<int>((static_cast<long long>(a.k_tiles) * (split + 1)) / a.splits);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -117,14 +87,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return g / (1.0f + __expf(-g)) * u;
-}
-
-// Wait without looking at the abort flag (used only while draining).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > timeout_ns) return;
-  }
 }
 
 template <int KIND, typename T>

@@ -51,6 +51,30 @@ struct GemmArgs {
   unsigned long long timeout_ns;
 };
 
+// Arguments of one block-scaled (fp8 activations x mxfp4 weights) grouped
+// GEMM launch.  The reduction dimension is Kdim = H (gate/up) or I (down).
+struct MxArgs {
+  int T, H, I, E, K;
+  int Kdim;
+  int n_tiles, k_tiles, splits, band;
+  long long cap;
+  const uint8_t* a;            // gate/up: xq (T, H) e4m3; down: hq (cap, I) e4m3
+  const float* x_row_scale;    // gate/up: per-token fp32 scale of xq
+  const uint8_t* w;            // packed e2m1: w13 (E, 2I, H/2) or w2 (E, H, I/2)
+  const uint8_t* w_scale;      // e8m0: (E, 2I, H/32) or (E, H, I/32)
+  const int32_t* sorted_ids;
+  const int32_t* block_info;
+  const int32_t* num_blocks;
+  const float* topk_weights;   // down: routing weight per flat index
+  void* out;                   // gate/up: hq (cap, I) e4m3; down: y (splits, cap, H) fp32
+  float h_scale;               // hq = e4m3(a / h_scale)
+  int32_t* status;
+  unsigned long long timeout_ns;
+};
+
+cudaError_t launch_mx_gate_up(const MxArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_mx_down(const MxArgs& a, int grid, cudaStream_t s);
+
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const float* y, int splits, long long cap, const int32_t* inv_perm,
                            int T, int K, int H, int out_dtype, void* out, int32_t* status,

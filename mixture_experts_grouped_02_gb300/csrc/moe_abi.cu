@@ -49,15 +49,29 @@ int check_problem(const moe_problem_t* p) {
 
 int block_m_of(const moe_problem_t* p) { return p->block_m == 0 ? kBlockM : p->block_m; }
 
-// The GEMMs read 128-byte k-tiles (64 bf16 / 32 fp32) and write 32-column
-// output chunks; the GEMM tile is 128 sorted rows.
+bool is_mx(const moe_problem_t* p) { return p->weight == MOE_E2M1_MX; }
+
+// The bf16/fp32 GEMMs read 128-byte k-tiles (64 bf16 / 32 fp32) and write
+// 32-column output chunks; the block-scaled GEMMs need whole 32-element scale
+// blocks along K (the end of K inside a 128-element tile is zero-filled).
+// The GEMM tile is 128 sorted rows.
 int check_gemm_shapes(const moe_problem_t* p) {
-  if (p->weight == MOE_E2M1_MX) return MOE_ERR_UNSUPPORTED;
+  if (block_m_of(p) != kBlockM) return MOE_ERR_UNSUPPORTED;
+  if (is_mx(p)) {
+    if (p->H % 32 != 0 || p->I % 32 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!(p->h_scale >= 0.0f) || p->h_scale > 3.0e38f) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+  }
   const int bk = p->act == MOE_BF16 ? 64 : 32;
   if (p->H % bk != 0 || p->I % bk != 0) return MOE_ERR_UNSUPPORTED;
-  if (block_m_of(p) != kBlockM) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
+
+float h_scale_of(const moe_problem_t* p) { return p->h_scale > 0.0f ? p->h_scale : 1.0f; }
+
+// Down-projection tiling: N columns per tile and K elements per k-tile.
+int down_tile_n(const moe_problem_t* p) { return is_mx(p) ? 192 : 256; }
+int down_tile_k(const moe_problem_t* p) { return is_mx(p) ? 128 : (p->act == MOE_BF16 ? 64 : 32); }
 
 size_t act_bytes(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
 
@@ -97,9 +111,8 @@ int default_splits(const moe_problem_t* p) {
   const long long cap = capacity(p->T, p->K, p->E, bm);
   const long long est_blocks =
       std::min(cap / bm, (na + bm - 1) / bm + std::min<long long>(p->E, na));
-  const long long n_tiles = (p->H + 255) / 256;
-  const int bk = p->act == MOE_BF16 ? 64 : 32;
-  const long long k_tiles = std::max(1, p->I / bk);
+  const long long n_tiles = (p->H + down_tile_n(p) - 1) / down_tile_n(p);
+  const long long k_tiles = std::max(1, (p->I + down_tile_k(p) - 1) / down_tile_k(p));
   const long long work = std::max(1ll, est_blocks * n_tiles);
   const long long target = 2ll * sm_count();
   if (work >= target) return 1;
@@ -267,6 +280,71 @@ int run_gemm2(const moe_problem_t* p, const void* h, const void* w2, const float
   return cuda_status(launch_gemm_down(p->act, a, tmA, tmB, grid, s));
 }
 
+MxArgs mx_args(const moe_problem_t* p) {
+  MxArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.T = p->T;
+  a.H = p->H;
+  a.I = p->I;
+  a.E = p->E;
+  a.K = p->K;
+  a.cap = capacity(p->T, p->K, p->E, kBlockM);
+  a.h_scale = h_scale_of(p);
+  a.timeout_ns = kWaitTimeoutNs;
+  return a;
+}
+
+bool aligned(const void* ptr, uintptr_t n) { return (reinterpret_cast<uintptr_t>(ptr) % n) == 0; }
+
+int run_gemm1_mx(const moe_problem_t* p, const void* xq, const float* x_row_scale, const void* w13,
+                 const uint8_t* w13_scale, const int32_t* sorted_ids, const int32_t* block_info,
+                 const int32_t* num_blocks, void* hq, int32_t* status, cudaStream_t s) {
+  if (!aligned(xq, 16) || !aligned(hq, 16) || !aligned(w13, 8)) return MOE_ERR_INVALID_ARG;
+  MxArgs a = mx_args(p);
+  a.Kdim = p->H;
+  a.n_tiles = (p->I + 95) / 96;
+  a.k_tiles = (p->H + 127) / 128;
+  a.splits = 1;
+  a.band = std::min(kBand, a.n_tiles);
+  a.a = static_cast<const uint8_t*>(xq);
+  a.x_row_scale = x_row_scale;
+  a.w = static_cast<const uint8_t*>(w13);
+  a.w_scale = w13_scale;
+  a.sorted_ids = sorted_ids;
+  a.block_info = block_info;
+  a.num_blocks = num_blocks;
+  a.out = hq;
+  a.status = status;
+  const long long max_tiles = (a.cap / kBlockM) * a.n_tiles;
+  const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
+  return cuda_status(launch_mx_gate_up(a, grid, s));
+}
+
+int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const uint8_t* w2_scale,
+                 const float* topk_weights, const int32_t* sorted_ids, const int32_t* block_info,
+                 const int32_t* num_blocks, float* y, int splits, int32_t* status,
+                 cudaStream_t s) {
+  if (!aligned(hq, 16) || !aligned(w2, 8) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+  MxArgs a = mx_args(p);
+  a.Kdim = p->I;
+  a.n_tiles = (p->H + 191) / 192;
+  a.k_tiles = (p->I + 127) / 128;
+  a.splits = splits;
+  a.band = std::min(kBand, a.n_tiles);
+  a.a = static_cast<const uint8_t*>(hq);
+  a.w = static_cast<const uint8_t*>(w2);
+  a.w_scale = w2_scale;
+  a.sorted_ids = sorted_ids;
+  a.block_info = block_info;
+  a.num_blocks = num_blocks;
+  a.topk_weights = topk_weights;
+  a.out = y;
+  a.status = status;
+  const long long max_tiles = (a.cap / kBlockM) * a.n_tiles * splits;
+  const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
+  return cuda_status(launch_mx_down(a, grid, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -354,14 +432,17 @@ int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_sca
                    const void* w13, const uint8_t* w13_scale, const int32_t* sorted_ids,
                    const int32_t* block_info, const int32_t* num_blocks, void* h,
                    int32_t* dev_status, void* stream) {
-  (void)x_row_scale;
-  (void)w13_scale;
   int rc = check_problem(p);
   if (rc != MOE_OK) return rc;
   rc = check_gemm_shapes(p);
   if (rc != MOE_OK) return rc;
   if (p->T == 0) return MOE_OK;
   if (!x || !w13 || !sorted_ids || !block_info || !num_blocks || !h) return MOE_ERR_INVALID_ARG;
+  if (is_mx(p)) {
+    if (!x_row_scale || !w13_scale) return MOE_ERR_INVALID_ARG;
+    return run_gemm1_mx(p, x, x_row_scale, w13, w13_scale, sorted_ids, block_info, num_blocks, h,
+                        dev_status, static_cast<cudaStream_t>(stream));
+  }
   return run_gemm1(p, x, w13, sorted_ids, block_info, num_blocks, h, dev_status,
                    static_cast<cudaStream_t>(stream));
 }
@@ -371,16 +452,20 @@ int moe_gemm2_weighted(const moe_problem_t* p, const void* h, const void* w2,
                        const int32_t* sorted_ids, const int32_t* block_info,
                        const int32_t* num_blocks, float* y, int k_splits, int32_t* dev_status,
                        void* stream) {
-  (void)w2_scale;
   int rc = check_problem(p);
   if (rc != MOE_OK) return rc;
   rc = check_gemm_shapes(p);
   if (rc != MOE_OK) return rc;
-  const int bk = p->act == MOE_BF16 ? 64 : 32;
-  if (k_splits < 1 || k_splits > p->I / bk) return MOE_ERR_INVALID_ARG;
+  const int k_tiles = (p->I + down_tile_k(p) - 1) / down_tile_k(p);
+  if (k_splits < 1 || k_splits > k_tiles) return MOE_ERR_INVALID_ARG;
   if (p->T == 0) return MOE_OK;
   if (!h || !w2 || !topk_weights || !sorted_ids || !block_info || !num_blocks || !y)
     return MOE_ERR_INVALID_ARG;
+  if (is_mx(p)) {
+    if (!w2_scale) return MOE_ERR_INVALID_ARG;
+    return run_gemm2_mx(p, h, w2, w2_scale, topk_weights, sorted_ids, block_info, num_blocks, y,
+                        k_splits, dev_status, static_cast<cudaStream_t>(stream));
+  }
   return run_gemm2(p, h, w2, topk_weights, sorted_ids, block_info, num_blocks, y, k_splits,
                    dev_status, static_cast<cudaStream_t>(stream));
 }
@@ -408,8 +493,7 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
   if (p->T == 0) return MOE_OK;
   if (!x || !topk_ids || !topk_weights || !w13 || !w2 || !out || !workspace)
     return MOE_ERR_INVALID_ARG;
-  (void)w13_scale;
-  (void)w2_scale;
+  if (is_mx(p) && (!w13_scale || !w2_scale)) return MOE_ERR_INVALID_ARG;
   Layout L;
   layout_of(p, &L);
   if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -433,10 +517,22 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                  reinterpret_cast<int32_t*>(part(MOE_WS_PADDED_OFFSETS)), sorted_ids, inv_perm,
                  block_info, num_blocks, status, s);
   if (rc != MOE_OK) return rc;
-  rc = run_gemm1(p, x, w13, sorted_ids, block_info, num_blocks, h, status, s);
-  if (rc != MOE_OK) return rc;
-  rc = run_gemm2(p, h, w2, topk_weights, sorted_ids, block_info, num_blocks, y, splits, status, s);
-  if (rc != MOE_OK) return rc;
+  if (is_mx(p)) {
+    uint8_t* xq = part(MOE_WS_XQ);
+    float* xs = reinterpret_cast<float*>(part(MOE_WS_X_SCALE));
+    if (launch_quantize_x(x, p->act, p->T, p->H, xq, xs, s) != cudaSuccess) return MOE_ERR_CUDA;
+    rc = run_gemm1_mx(p, xq, xs, w13, w13_scale, sorted_ids, block_info, num_blocks, h, status, s);
+    if (rc != MOE_OK) return rc;
+    rc = run_gemm2_mx(p, h, w2, w2_scale, topk_weights, sorted_ids, block_info, num_blocks, y,
+                      splits, status, s);
+    if (rc != MOE_OK) return rc;
+  } else {
+    rc = run_gemm1(p, x, w13, sorted_ids, block_info, num_blocks, h, status, s);
+    if (rc != MOE_OK) return rc;
+    rc = run_gemm2(p, h, w2, topk_weights, sorted_ids, block_info, num_blocks, y, splits, status,
+                   s);
+    if (rc != MOE_OK) return rc;
+  }
   return cuda_status(launch_combine(y, splits, capacity(p->T, p->K, p->E, bm), inv_perm, p->T,
                                     p->K, p->H, p->act, out, status, s));
 }

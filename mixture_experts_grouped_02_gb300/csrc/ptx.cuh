@@ -109,6 +109,21 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 16-byte copy of which only the first `src_bytes` (0 or 16) come from
+// global memory; the rest of the 16 bytes are zero-filled.
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// 8-byte copy (through L1), zero-filled beyond `src_bytes` (0 or 8).
+__device__ __forceinline__ void cp_async_8_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -187,6 +202,47 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 block-scaled MMAs: A e4m3, B e2m1,
+// K-major, scale factors UE8M0 (bit 23), N/8 (bits 17-22), M/16 (bits
+// 24-28); the scale-factor byte used inside each 32-bit TMEM word is chosen
+// per MMA by the B id (bits 4-5) and the A id (bits 29-30).
+__host__ __device__ constexpr uint32_t make_idesc_mx_e4m3_e2m1(int M, int N) {
+  return (0u << 7)                                  // A format: e4m3
+         | (5u << 10)                               // B format: e2m1
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (1u << 23)                               // scale type: ue8m0
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ uint32_t idesc_with_sf_ids(uint32_t idesc, uint32_t sfa, uint32_t sfb) {
+  return idesc | (sfb << 4) | (sfa << 29);
+}
+
+// D (+)= (A * scale_A) x (B * scale_B)^T with one e8m0 scale per 32 K
+// elements of each row, scales read from TMEM.
+__device__ __forceinline__ void umma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Four consecutive 32-bit TMEM columns of the calling warp's 32 lanes.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
+                                         uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued

@@ -290,3 +290,120 @@ def test_quantize_x_fp8_bit_exact(shape, dtype):
     torch.cuda.synchronize()
     assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
     assert np.array_equal(xq.cpu().numpy(), xq_ref)
+
+
+# ------------------------------------------------------------- mxfp4 path
+# Bounds for the fp8 x mxfp4 path: against the oracle that rounds h to e4m3
+# the way the GPU stores it (EMULATE), max-abs 6e-2 and rel-L2 2e-2; against
+# the unrounded oracle (EXACT), rel-L2 6e-2 (one e4m3 rounding of h carries
+# up to 2^-4 relative error per element).
+MX_MAX_ABS, MX_REL_EMU, MX_REL_EXACT = 6e-2, 2e-2, 6e-2
+
+MX_CASES = [
+    # T, H, I, E, K
+    (40, 256, 192, 4, 2),     # whole k-tiles, two N tiles of 96
+    (150, 320, 288, 3, 2),    # K ending half-way through a 128-element tile, 2 M blocks
+    (7, 2880, 192, 8, 4),     # the low-precision hidden size
+]
+
+
+def _mx_problem(case, seed):
+    T, H, I, E, K = case
+    cfg = gen.MoEConfig("mx", T, H, I, E, K, "mxfp4", "uniform")
+    return cfg, gen.generate(cfg, seed=seed)
+
+
+@pytest.mark.parametrize("case", MX_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d" % c)
+def test_mx_gemm1_stage(case):
+    cfg, inp = _mx_problem(case, 41)
+    T, H, I, E, K = case
+    d = inp.to("cuda")
+    xq_ref, s_ref = oracle.quantize_x_fp8(np_store(inp.x))  # fp8 codes as the method forms them
+    al_ref = oracle.align(inp.topk_ids.numpy(), E, 128)
+    al = moe.align(d.topk_ids, E, 128)
+    p = moe.make_problem(T, H, I, E, K, "bf16", "mxfp4", h_scale=0.5)
+    cap = moe.moe_align_capacity(T, K, E, 128)
+    hq = torch.zeros((cap, I), dtype=torch.uint8, device="cuda")
+    st = _status()
+    moe.moe_gemm1_silu(p, torch.from_numpy(xq_ref).cuda(), torch.from_numpy(s_ref).cuda(), d.w13,
+                       d.w13_scale, al["sorted_ids"], al["block_info"], al["num_blocks"], hq, st)
+    assert moe.moe_get_device_status(st) == 0
+    rows = _valid_rows(al_ref, T * K)
+    eor = _expert_of_rows(al_ref, rows, inp.topk_ids.numpy().ravel())
+    P = oracle_problem(inp, quantize_x=True, h_e4m3=True, h_scale=0.5)
+    emu = oracle.gemm1_silu_rows(P, np_store(inp.x), np_store(inp.w13), al_ref["sorted_ids"], eor,
+                                 rows, w13_scale=np_store(inp.w13_scale), mode=oracle.EMULATE)
+    got = oracle.e4m3_to_float(hq[torch.from_numpy(rows).long().cuda()].cpu().numpy()) * 0.5
+    # the stored codes equal the oracle's rounding of the same values, except
+    # where the fp32 and fp64 sums straddle a rounding boundary (one step)
+    step = np.maximum(np.abs(emu) * 2.0 ** -3, 2.0 ** -9 * 0.5)
+    assert np.all(np.abs(got - emu) <= step * 1.001)
+    assert (got != emu).mean() < 1e-3
+    exact = oracle.gemm1_silu_rows(P, np_store(inp.x), np_store(inp.w13), al_ref["sorted_ids"],
+                                   eor, rows, w13_scale=np_store(inp.w13_scale))
+    assert np.linalg.norm(got - exact) / np.linalg.norm(exact) < MX_REL_EXACT
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+@pytest.mark.parametrize("case", MX_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d" % c)
+def test_mx_gemm2_stage(case, splits):
+    cfg, inp = _mx_problem(case, 42)
+    T, H, I, E, K = case
+    d = inp.to("cuda")
+    cap = moe.moe_align_capacity(T, K, E, 128)
+    rng = np.random.default_rng(7)
+    codes = rng.integers(0, 256, (cap, I)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38  # no NaN codes: 1.0 instead
+    al_ref = oracle.align(inp.topk_ids.numpy(), E, 128)
+    al = moe.align(d.topk_ids, E, 128)
+    p = moe.make_problem(T, H, I, E, K, "bf16", "mxfp4", h_scale=0.25)
+    y = torch.full((splits, cap, H), float("nan"), dtype=torch.float32, device="cuda")
+    st = _status()
+    moe.moe_gemm2_weighted(p, torch.from_numpy(codes).cuda(), d.w2, d.w2_scale, d.topk_weights,
+                           al["sorted_ids"], al["block_info"], al["num_blocks"], y, splits, st)
+    assert moe.moe_get_device_status(st) == 0
+    rows = _valid_rows(al_ref, T * K)
+    eor = _expert_of_rows(al_ref, rows, inp.topk_ids.numpy().ravel())
+    P = oracle_problem(inp, h_e4m3=True, h_scale=0.25)
+    ref = oracle.gemm2_weighted_rows(P, codes, np_store(inp.w2), inp.topk_weights.numpy(),
+                                     al_ref["sorted_ids"], eor, rows,
+                                     w2_scale=np_store(inp.w2_scale), h_is_e4m3=True)
+    got = y[:, torch.from_numpy(rows).long().cuda()].sum(0)
+    # e4m3 x e2m1 x e8m0 products are exact; only the fp32 summation differs
+    assert_close(got, ref, max_abs=2e-2, rel_l2=1e-4, what="y")
+
+
+def _run_forward_mx(d, cfg, h_scale=1.0):
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "bf16", "mxfp4", h_scale=h_scale)
+    ws = moe.Workspace(p)
+    ws.buffer.fill_(0xFF)
+    out = torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, d.w13, d.w13_scale, d.w2, d.w2_scale, out,
+                    ws.buffer, ws.nbytes)
+    assert moe.moe_get_device_status(ws.status) == 0
+    return out
+
+
+def _check_mx(out, inp, toks, h_scale=1.0):
+    emu = oracle_forward_tokens(inp, toks, mode=oracle.EMULATE, quantize_x=True, h_e4m3=True,
+                                h_scale=h_scale)
+    exact = oracle_forward_tokens(inp, toks, mode=oracle.EXACT, quantize_x=True, h_e4m3=True,
+                                  h_scale=h_scale)
+    got = out[torch.from_numpy(np.asarray(toks)).long().cuda()]
+    assert_close(got, emu, max_abs=MX_MAX_ABS, rel_l2=MX_REL_EMU, what="vs emulate")
+    assert_close(got, exact, max_abs=np.inf, rel_l2=MX_REL_EXACT, what="vs exact")
+
+
+@pytest.mark.parametrize("case", MX_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d" % c)
+def test_forward_mx_small(case):
+    cfg, inp = _mx_problem(case, 43)
+    out = _run_forward_mx(inp.to("cuda"), cfg, h_scale=0.5)
+    _check_mx(out, inp, np.arange(cfg.T), h_scale=0.5)
+
+
+def test_forward_lowp_full_size_sampled():
+    cfg = gen.config("lowp")
+    inp = generate(cfg, seed=0, device="cuda")
+    out = _run_forward_mx(inp, cfg)
+    assert torch.isfinite(out.float()).all()
+    _check_mx(out, inp, sample_tokens(cfg.T, 8, seed=2))
