@@ -75,6 +75,20 @@ def max_over_ranks(v: float, ws: int, device) -> float:
     return float(t.item())
 
 
+def rank_batch_seed(rank: int) -> int:
+    """Every rank serves the same model (weights drawn with seed 0) and routes
+    its own batch: rank 0 draws x and routing with seed 0, rank r > 0 with
+    1000 + r, so that replicas do not repeat one another's work."""
+    return 0 if rank == 0 else 1000 + rank
+
+
+def aggregate(ms_per_step_local: float, tokens_per_rank: int, ws: int, device):
+    """Whole-job throughput of ws replicas: the step time is the slowest
+    rank's, the tokens are all ranks' (weak scaling)."""
+    ms = max_over_ranks(ms_per_step_local, ws, device)
+    return ms, tokens_per_rank * ws / (ms * 1e-3)
+
+
 def barrier(ws):
     if ws > 1:
         import torch.distributed as dist
@@ -183,6 +197,8 @@ def bytes_algorithmic(cfg, inp):
     esz = inp.x.element_size()
     w_per_expert = (inp.w13[0].numel() * inp.w13.element_size() +
                     inp.w2[0].numel() * inp.w2.element_size())
+    if inp.w13_scale is not None:
+        w_per_expert += inp.w13_scale[0].numel() + inp.w2_scale[0].numel()
     return active * w_per_expert + 2 * cfg.T * cfg.H * esz + 8 * cfg.T * cfg.K, active
 
 
@@ -191,9 +207,13 @@ def kernel_rooflines(cfg, inp, active, gemm1_ms, gemm2_ms, hbm_gbs, bf16_tflops)
     fractions.  Bytes: weights of the active experts, the activation rows read
     once, the intermediate written once (h for gate/up, y for down)."""
     na, H, I = cfg.T * cfg.K, cfg.H, cfg.I
-    esz = inp.x.element_size()
+    mx = cfg.dtype == "mxfp4"
+    esz = 1 if mx else inp.x.element_size()  # the GEMMs read e4m3 x and h on the mx path
     w13_e = inp.w13[0].numel() * inp.w13.element_size()
     w2_e = inp.w2[0].numel() * inp.w2.element_size()
+    if mx:  # the e8m0 scales travel with the e2m1 values
+        w13_e += inp.w13_scale[0].numel()
+        w2_e += inp.w2_scale[0].numel()
     out = {}
     for name, ms, flops, nbytes in (
             ("gemm_gate_up", gemm1_ms, 4 * na * H * I,
@@ -213,20 +233,23 @@ def cpu_oracle_rate(cfg, inp_cpu, seconds):
     import oracle
     threads = len(os.sched_getaffinity(0))
     oracle.lib()
+    mx = cfg.dtype == "mxfp4"
     P = oracle.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, gen.to_numpy_storage(inp_cpu.x[:1]),
-                            gen.to_numpy_storage(inp_cpu.w13[:1]))
+                            gen.to_numpy_storage(inp_cpu.w13[:1]), quantize_x=mx, h_e4m3=mx)
     args = (gen.to_numpy_storage(inp_cpu.x), inp_cpu.topk_ids.numpy(),
             inp_cpu.topk_weights.numpy(), gen.to_numpy_storage(inp_cpu.w13),
             gen.to_numpy_storage(inp_cpu.w2))
+    scales = dict(w13_scale=gen.to_numpy_storage(inp_cpu.w13_scale),
+                  w2_scale=gen.to_numpy_storage(inp_cpu.w2_scale))
     probe = np.arange(min(cfg.T, threads), dtype=np.int32)
     t = time.perf_counter()
-    oracle.forward(P, *args, tokens=probe)
+    oracle.forward(P, *args, tokens=probe, **scales)
     dt = time.perf_counter() - t
     n = int(min(cfg.T, max(len(probe), len(probe) * seconds / max(dt, 1e-3))))
     n = max(threads, n // threads * threads) if n >= threads else n
     toks = np.arange(n, dtype=np.int32)
     t = time.perf_counter()
-    oracle.forward(P, *args, tokens=toks)
+    oracle.forward(P, *args, tokens=toks, **scales)
     dt = time.perf_counter() - t
     return n / dt, f"first {n} of {cfg.T} tokens ({n * cfg.K} assignments), fp64, {dt:.1f} s", \
         threads
@@ -270,10 +293,12 @@ def run_ours(args, ws, rank, local):
     # weights are the same model on every rank; each rank routes its own batch
     inp = gen.generate(cfg, seed=0, device=dev)
     if rank > 0:
-        inp.x = gen.draw_x(cfg, seed=1000 + rank, device=dev)
-        inp.topk_ids, inp.topk_weights = gen.route(gen.router_logits(cfg, 1000 + rank, dev),
-                                                   cfg.K)
-    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype)
+        seed = rank_batch_seed(rank)
+        inp.x = gen.draw_x(cfg, seed=seed, device=dev)
+        inp.topk_ids, inp.topk_weights = gen.route(gen.router_logits(cfg, seed, dev), cfg.K)
+    mx = cfg.dtype == "mxfp4"
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "bf16" if mx else cfg.dtype,
+                         "mxfp4" if mx else None)
     wsp = moe.Workspace(p, dev)
     part = lambda i, dt=torch.int32: wsp.part(i, dt)
     st = wsp.status
@@ -283,30 +308,39 @@ def run_ours(args, ws, rank, local):
     binfo, nblk = part(_abi.MOE_WS_BLOCK_INFO), part(_abi.MOE_WS_NUM_BLOCKS)
     h = part(_abi.MOE_WS_H, torch.uint8)
     y = part(_abi.MOE_WS_Y, torch.float32)
+    xq = part(_abi.MOE_WS_XQ, torch.uint8) if mx else None
+    xs = part(_abi.MOE_WS_X_SCALE, torch.float32) if mx else None
     splits = moe.moe_gemm2_default_splits(p)
     cap = moe.moe_align_capacity(cfg.T, cfg.K, cfg.E, 128)
     out = torch.empty((cfg.T, cfg.H), dtype=inp.x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
     st.zero_()
 
+    # exactly the launches moe_forward makes, one C-ABI call per stage
+    stages = []
+    if mx:
+        stages.append(("quantize_x", lambda: moe.moe_quantize_x_fp8(
+            inp.x, _abi.MOE_BF16, cfg.T, cfg.H, xq, xs, stream)))
+    stages.append(("align", lambda: moe.moe_align(
+        inp.topk_ids, cfg.T, cfg.K, cfg.E, 128, counts, offs, poffs, sorted_ids, inv, binfo, nblk,
+        st, stream)))
+    stages.append(("gemm_gate_up", lambda: moe.moe_gemm1_silu(
+        p, xq if mx else inp.x, xs, inp.w13, inp.w13_scale, sorted_ids, binfo, nblk, h, st,
+        stream)))
+    stages.append(("gemm_down", lambda: moe.moe_gemm2_weighted(
+        p, h, inp.w2, inp.w2_scale, inp.topk_weights, sorted_ids, binfo, nblk, y, splits, st,
+        stream)))
+    stages.append(("combine", lambda: moe.moe_combine(
+        y, splits, cap, inv, cfg.T, cfg.K, cfg.H, p.act, out, st, stream)))
+    names = [n for n, _ in stages]
+
     def step(ev=None):
-        # exactly the launches moe_forward makes, with events between stages
         if ev is not None:
             ev[0].record(stream)
-        moe.moe_align(inp.topk_ids, cfg.T, cfg.K, cfg.E, 128, counts, offs, poffs, sorted_ids,
-                      inv, binfo, nblk, st, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        moe.moe_gemm1_silu(p, inp.x, None, inp.w13, None, sorted_ids, binfo, nblk, h, st, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        moe.moe_gemm2_weighted(p, h, inp.w2, None, inp.topk_weights, sorted_ids, binfo, nblk, y,
-                               splits, st, stream)
-        if ev is not None:
-            ev[3].record(stream)
-        moe.moe_combine(y, splits, cap, inv, cfg.T, cfg.K, cfg.H, p.act, out, st, stream)
-        if ev is not None:
-            ev[4].record(stream)
+        for i, (_, f) in enumerate(stages):
+            f()
+            if ev is not None:
+                ev[i + 1].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -318,7 +352,8 @@ def run_ours(args, ws, rank, local):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+           for _ in range(args.steps)]
     barrier(ws)
     torch.cuda.synchronize(dev)
     t0 = time.time()
@@ -332,17 +367,17 @@ def run_ours(args, ws, rank, local):
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
 
-    stage = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
+    stage = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(len(stages))]
                       for i in range(args.steps)])  # ms
-    total_ms = float(evs[0][0].elapsed_time(evs[-1][4]))
-    ms_step = max_over_ranks(total_ms / args.steps, ws, dev)
+    stage_ms = {n: float(stage[:, j].mean()) for j, n in enumerate(names)}
+    total_ms = float(evs[0][0].elapsed_time(evs[-1][len(stages)]))
+    ms_step, value = aggregate(total_ms / args.steps, cfg.T, ws, dev)
     tokens_all = cfg.T * ws
-    value = tokens_all / (ms_step * 1e-3)
     flops = cfg.flops
     tflops = flops * ws / (ms_step * 1e-3) / 1e12
     bytes_alg, active = bytes_algorithmic(cfg, inp)
-    gemm1_ms = float(stage[:, 1].mean())
-    gemm2_ms = float(stage[:, 2].mean())
+    gemm1_ms = stage_ms["gemm_gate_up"]
+    gemm2_ms = stage_ms["gemm_down"]
     hbm_gbs, bf16_tflops, peak_kind = peaks()
     kern = kernel_rooflines(cfg, inp, active, gemm1_ms, gemm2_ms, hbm_gbs, bf16_tflops)
     dom = max(kern, key=lambda k: kern[k]["ms"])
@@ -374,8 +409,8 @@ def run_ours(args, ws, rank, local):
         x_d.copy_(x_h, non_blocking=True)
         ids_d.copy_(ids_h, non_blocking=True)
         w_d.copy_(w_h, non_blocking=True)
-        moe.moe_forward(p, x_d, ids_d, w_d, inp.w13, None, inp.w2, None, out, wsp.buffer,
-                        wsp.nbytes, stream)
+        moe.moe_forward(p, x_d, ids_d, w_d, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, out,
+                        wsp.buffer, wsp.nbytes, stream)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -396,8 +431,7 @@ def run_ours(args, ws, rank, local):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        inp_cpu = gen.MoEInputs(cfg, inp.x.cpu(), inp.w13.cpu(), inp.w2.cpu(),
-                                inp.topk_ids.cpu(), inp.topk_weights.cpu())
+        inp_cpu = inp.to("cpu")
         rate, sample, threads = cpu_oracle_rate(cfg, inp_cpu, args.cpu_seconds)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": sample}
@@ -407,7 +441,8 @@ def run_ours(args, ws, rank, local):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if cfg.dtype == "bf16" else cfg.dtype, "data": "synthetic",
+            "dtype": {"bf16": "bf16", "f32": "f32 (tf32 MMA)",
+                      "mxfp4": "e4m3 x mxfp4 (fp32 acc)"}[cfg.dtype], "data": "synthetic",
             "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
                        "top_k": cfg.K, "global_batch_tokens": tokens_all,
                        "parallelism": f"replicas{ws}",
@@ -415,15 +450,14 @@ def run_ours(args, ws, rank, local):
                              (bytes_alg / 1e9)},
             "tflops": tflops,
             "hbm_gbs_algorithmic": bytes_alg * ws / (ms_step * 1e-3) / 1e9,
-            "stage_ms": {"align": float(stage[:, 0].mean()), "gemm_gate_up": gemm1_ms,
-                         "gemm_down": gemm2_ms, "combine": float(stage[:, 3].mean())},
+            "stage_ms": stage_ms,
             "roofline": roof,
             "kernels": kern,
             "active_experts": active,
             "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": len(stages) * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

@@ -5,7 +5,7 @@
 //  * gate/up (GEMM1): A = 128 token rows gathered by index from x by four
 //    producer warps (16-byte cp.async per lane, eight lanes per 128-byte row,
 //    written straight into the 128-byte swizzled layout, then a proxy fence
-//    and an mbarrier arrive), B = 128 gate rows and the 128 matching up rows of w13[e]
+//    and an mbarrier arrive once the copies of two later stages are issued), B = 128 gate rows and the 128 matching up rows of w13[e]
 //    stacked into one 256-row operand, so a single M=128 x N=256 MMA puts
 //    gate in accumulator columns 0..127 and up in 128..255 of the same TMEM
 //    lane.  The epilogue forms SiLU(gate) * up per lane and stores h.
@@ -74,8 +74,11 @@ struct Cfg {
   static constexpr int kMmaWarp = kProducerWarps;
   static constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
   // gate/up: each producer thread marks a stage full only once its cp.async
-  // group for that stage has landed, kGatherLag stages after issuing it
-  static constexpr int kGatherLag = 2;
+  // group for that stage has landed, kGatherLag stages after issuing it.  The
+  // lag leaves one stage of slack: stage n is published while the tensor core
+  // still works on n - 1 (a lag of kStages - 1 would publish n only after n - 1
+  // is freed and the next copies are issued, idling the tensor core each stage)
+  static constexpr int kGatherLag = kStages - 2;
   static constexpr uint32_t kFullArrivals = KIND == kGateUp ? kProducerWarps * 32 + 1 : 1;
   static constexpr uint32_t kTxBytes = KIND == kGateUp ? kBBytes : kStageBytes;
 };

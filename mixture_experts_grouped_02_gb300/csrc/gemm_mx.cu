@@ -23,8 +23,9 @@
 //    gathered token rows for gate/up, contiguous h rows for down -- and
 //    8-byte packed chunks of B straight from the weights' natural packed
 //    layout; the ragged end of K is zero-filled), and write the stage's B
-//    scale factors into tensor memory with tcgen05.st; they publish the stage
-//    (proxy fence, tcgen05 fence, mbarrier arrive) two stages later;
+//    scale factors (fetched one stage ahead) into tensor memory with
+//    tcgen05.st; they publish the stage (proxy fence, tcgen05 fence, mbarrier
+//    arrive) once the copies of kStages - 2 later stages are issued;
 //  * warp 4 issues the MMAs from one thread; warps 5-8 run the epilogue;
 //  * tensor memory: two 192-column fp32 accumulators, 4 columns of unit A
 //    scales, and per stage and MMA half 4 columns of B scales.
@@ -66,7 +67,10 @@ struct MxCfg {
   static constexpr int kProducerWarps = 4;
   static constexpr int kMmaWarp = kProducerWarps;
   static constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
-  static constexpr int kLag = 2;
+  // a producer thread publishes stage n once stage n + kLag is issued; the lag
+  // leaves one stage of slack so that n is published while the tensor core
+  // still works on n - 1
+  static constexpr int kLag = kStages - 2;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
   static constexpr uint32_t kIdesc = make_idesc_mx_e4m3_e2m1(kBM, kHalf);
 };
@@ -79,11 +83,17 @@ __device__ __forceinline__ uint32_t sfb_col(int stage, int half) {
 
 // Scales of K blocks 4*kt .. 4*kt+3 of one weight row, one byte each
 // (blocks past the row's end read as 127, a unit scale; their values are 0).
+// Rows of an even number of blocks are read as two 16-bit words.
 __device__ __forceinline__ uint32_t scale_word(const uint8_t* srow, int kt, int nblocks) {
+  const int b0 = kt * 4;
+  if ((nblocks & 1) == 0 && b0 + 4 <= nblocks) {
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(srow + b0);
+    return static_cast<uint32_t>(__ldg(p)) | (static_cast<uint32_t>(__ldg(p + 1)) << 16);
+  }
   uint32_t w = 0;
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    const int blk = kt * 4 + b;
+    const int blk = b0 + b;
     const uint32_t v = blk < nblocks ? static_cast<uint32_t>(__ldg(srow + blk)) : 127u;
     w |= v << (8 * b);
   }
@@ -211,6 +221,13 @@ __global__ void __launch_bounds__(MxCfg::kThreads, 1) mx_gemm_kernel(const __gri
         for (int c = 0; c < 3; ++c)
           srow[h][c] = a.w_scale + wrow_of(h * C::kHalf + 32 * c + lane) * nblocks_k;
 
+      // scale words of the next stage are fetched one stage ahead
+      uint32_t sw[2][3];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 3; ++c) sw[h][c] = kb < ke ? scale_word(srow[h][c], kb, nblocks_k) : 0u;
+
       for (int kt = kb; kt < ke; ++kt) {
         if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, to)) {
           ok = false;
@@ -235,10 +252,15 @@ __global__ void __launch_bounds__(MxCfg::kThreads, 1) mx_gemm_kernel(const __gri
         cp_async_commit();
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          tmem_st4(tmem_base + sf_lane + sfb_col(stage, h), scale_word(srow[h][0], kt, nblocks_k),
-                   scale_word(srow[h][1], kt, nblocks_k), scale_word(srow[h][2], kt, nblocks_k),
+          tmem_st4(tmem_base + sf_lane + sfb_col(stage, h), sw[h][0], sw[h][1], sw[h][2],
                    0x7F7F7F7Fu);
         tmem_wait_st();
+        if (kt + 1 < ke) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 3; ++c) sw[h][c] = scale_word(srow[h][c], kt + 1, nblocks_k);
+        }
         ++issued;
         if (++stage == C::kStages) {
           stage = 0;
