@@ -310,6 +310,11 @@ def run_ours(args, ws, rank, local):
     y = part(_abi.MOE_WS_Y, torch.float32)
     xq = part(_abi.MOE_WS_XQ, torch.uint8) if mx else None
     xs = part(_abi.MOE_WS_X_SCALE, torch.float32) if mx else None
+    # model weights as the kernels read them (mxfp4: packed once, at load time)
+    w13, s13, w2, s2 = inp.w13, None, inp.w2, None
+    if mx:
+        w13, s13 = moe.pack_mx(inp.w13, inp.w13_scale, 2)
+        w2, s2 = moe.pack_mx(inp.w2, inp.w2_scale, 1)
     splits = moe.moe_gemm2_default_splits(p)
     cap = moe.moe_align_capacity(cfg.T, cfg.K, cfg.E, 128)
     out = torch.empty((cfg.T, cfg.H), dtype=inp.x.dtype, device=dev)
@@ -318,18 +323,16 @@ def run_ours(args, ws, rank, local):
 
     # exactly the launches moe_forward makes, one C-ABI call per stage
     stages = []
-    if mx:
-        stages.append(("quantize_x", lambda: moe.moe_quantize_x_fp8(
-            inp.x, _abi.MOE_BF16, cfg.T, cfg.H, xq, xs, stream)))
     stages.append(("align", lambda: moe.moe_align(
         inp.topk_ids, cfg.T, cfg.K, cfg.E, 128, counts, offs, poffs, sorted_ids, inv, binfo, nblk,
         st, stream)))
+    if mx:
+        stages.append(("quantize_gather_x", lambda: moe.moe_quantize_gather_x_fp8(
+            inp.x, _abi.MOE_BF16, cfg.T, cfg.H, cfg.K, inv, xq, xs, st, stream)))
     stages.append(("gemm_gate_up", lambda: moe.moe_gemm1_silu(
-        p, xq if mx else inp.x, xs, inp.w13, inp.w13_scale, sorted_ids, binfo, nblk, h, st,
-        stream)))
+        p, xq if mx else inp.x, xs, w13, s13, sorted_ids, binfo, nblk, h, st, stream)))
     stages.append(("gemm_down", lambda: moe.moe_gemm2_weighted(
-        p, h, inp.w2, inp.w2_scale, inp.topk_weights, sorted_ids, binfo, nblk, y, splits, st,
-        stream)))
+        p, h, w2, s2, inp.topk_weights, sorted_ids, binfo, nblk, y, splits, st, stream)))
     stages.append(("combine", lambda: moe.moe_combine(
         y, splits, cap, inv, cfg.T, cfg.K, cfg.H, p.act, out, st, stream)))
     names = [n for n, _ in stages]
@@ -409,8 +412,8 @@ def run_ours(args, ws, rank, local):
         x_d.copy_(x_h, non_blocking=True)
         ids_d.copy_(ids_h, non_blocking=True)
         w_d.copy_(w_h, non_blocking=True)
-        moe.moe_forward(p, x_d, ids_d, w_d, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, out,
-                        wsp.buffer, wsp.nbytes, stream)
+        moe.moe_forward(p, x_d, ids_d, w_d, w13, s13, w2, s2, out, wsp.buffer, wsp.nbytes,
+                        stream)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):

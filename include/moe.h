@@ -85,7 +85,7 @@ typedef enum {
     MOE_WS_INV_PERM = 5,       /* int32[T*K]                                */
     MOE_WS_BLOCK_INFO = 6,     /* int32[cap/block_m][4]                     */
     MOE_WS_NUM_BLOCKS = 7,     /* int32[1]                                  */
-    MOE_WS_XQ = 8,             /* e4m3[T][H]   (MX weights only)            */
+    MOE_WS_XQ = 8,             /* e4m3[cap][H], sorted (MX weights only)    */
     MOE_WS_X_SCALE = 9,        /* fp32[T]      (MX weights only)            */
     MOE_WS_H = 10,             /* act or e4m3 [cap][I]                      */
     MOE_WS_Y = 11,             /* fp32[splits][cap][H]                      */
@@ -148,6 +148,32 @@ int moe_align(const int32_t* topk_ids, int T, int K, int E, int block_m, int32_t
               int32_t* offsets, int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
               int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream);
 
+/* ---- mxfp4 weight packing (once, when the model is loaded) -----------------
+ * Source: "MOE Bmm1 Fused Gather" -- its matmul takes the e2m1 weights in a
+ * pre-shuffled value layout and the e8m0 scales in a swizzled scale layout,
+ * both made for its kernel's tiles before the kernel runs.  This library's
+ * block-scaled GEMMs likewise read MX weights in a packed form:
+ *   natural form of a weight tensor with E experts, R rows, K elements along
+ *   the reduction: values (E, R, K/2) bytes, e2m1 pairs, lower K index in the
+ *   low nibble; scales (E, R, K/32) e8m0 bytes.
+ *   packed values: (E, R, Kp/2) bytes, Kp = K rounded up to 128, zero
+ *   nibbles past K (so that one TMA copy per 128-element K tile expands a
+ *   tile into the 16-byte slots the MMA reads 4-bit operands from);
+ *   packed scales: 512-byte images (E, sections, G, Kp/128, 512): the R rows
+ *   of an expert form `sections` equal sections (2 for w13: gate rows and up
+ *   rows; 1 for w2), each cut into G = 2*ceil((R/sections)/192) groups of 96
+ *   rows; byte 16*l + 4*c + b of image (e, s, g, t) is the scale of section
+ *   row 96*g + 32*c + l, K block 4*t + b for c < 3, and 127 where that row or
+ *   block does not exist -- the layout tensor memory takes the scales in.
+ * moe_mx_packed_bytes returns the total bytes (0 on bad arguments) and the
+ * two parts; K must be a multiple of 32.  moe_pack_mx_weights writes the
+ * packed form on `stream` (all pointers device memory; the packed values
+ * must be 32-byte and the images 16-byte aligned to be used). */
+size_t moe_mx_packed_bytes(int E, int R, int K, int sections, size_t* value_bytes,
+                           size_t* scale_bytes);
+int moe_pack_mx_weights(const uint8_t* w, const uint8_t* w_scale, int E, int R, int K,
+                        int sections, uint8_t* w_packed, uint8_t* scale_packed, void* stream);
+
 /* ---- fp8 activation step ------------------------------------------------
  * Source: "MOE Bmm1 Fused Gather" (Triton Gluon example), pack_e4m3x2
  * (fp32 -> e4m3, round to nearest even, saturating).  Reading: one scale
@@ -158,6 +184,15 @@ int moe_align(const int32_t* topk_ids, int T, int K, int E, int block_m, int32_t
 int moe_quantize_x_fp8(const void* x, int x_dtype, int T, int H, uint8_t* xq, float* row_scale,
                        void* stream);
 
+/* The same step with the token gather fused in, for the block-scaled GEMMs:
+ * each token's codes are written to every slot of the expert-sorted list the
+ * token occupies, xq_sorted[inv_perm[t*K + k], :] (cap rows of H bytes; rows
+ * of padding slots are not written), scales as above in token order.
+ * inv_perm as written by moe_align.  Skipped when *dev_status != 0. */
+int moe_quantize_gather_x_fp8(const void* x, int x_dtype, int T, int H, int K,
+                              const int32_t* inv_perm, uint8_t* xq_sorted, float* row_scale,
+                              int32_t* dev_status, void* stream);
+
 /* ---- gather + GEMM1 + SiLU*up -------------------------------------------
  * Source: "factor_moe_fused_gemm.cu", fused_silu_gate_kernel (gate = first
  * half of the w13 rows, up = second half, SiLU(g) = g / (1 + e^-g)) and
@@ -167,10 +202,13 @@ int moe_quantize_x_fp8(const void* x, int x_dtype, int T, int H, uint8_t* xq, fl
  * For every slot s of a block b < *num_blocks with i = sorted_ids[s] < N_a
  * and e = block_info[b].expert:
  *   h[s, j] = SiLU(W13[e, j, :] . x[i / K, :]) * (W13[e, I + j, :] . x[i / K, :])
- * x    (T, H) act; for MX weights, e4m3 codes with x_row_scale (T) fp32
- * w13  (E, 2I, H) weight dtype (MX: (E, 2I, H/2) bytes + w13_scale (E, 2I, H/32))
+ * x    (T, H) act; for MX weights, the e4m3 codes in sorted order (cap, H)
+ *      as written by moe_quantize_gather_x_fp8, with x_row_scale (T) fp32
+ * w13  (E, 2I, H) weight dtype (MX: packed values + scale images of
+ *      moe_pack_mx_weights with R = 2I, K = H, sections = 2)
  * h    (cap, I) act (MX: e4m3 codes of a / h_scale); rows of padding slots
- *      are not written.  H and I must be multiples of 64 (32 for MOE_F32).
+ *      are not written.  H and I must be multiples of 64 (32 for MOE_F32 and
+ *      for MX weights).
  * sorted_ids/block_info/num_blocks as written by moe_align with the same
  * block_m.  dev_status may be NULL. */
 int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_scale,
@@ -188,8 +226,9 @@ int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_sca
  * so that sum_q y[q, s, :] is the routing-weighted expert output.  Splits
  * cut I into k_splits nearly equal runs of 64 columns (k_splits <= I/64).
  * h (cap, I) as written by moe_gemm1_silu; w2 (E, H, I) weight dtype (MX:
- * (E, H, I/2) + w2_scale (E, H, I/32)); y (k_splits, cap, H) fp32, padding
- * rows not written. */
+ * packed by moe_pack_mx_weights with R = H, K = I, sections = 1);
+ * y (k_splits, cap, H) fp32, padding rows not written.  MX splits cut the
+ * 128-element K tiles. */
 int moe_gemm2_weighted(const moe_problem_t* p, const void* h, const void* w2,
                        const uint8_t* w2_scale, const float* topk_weights,
                        const int32_t* sorted_ids, const int32_t* block_info,
@@ -207,13 +246,14 @@ int moe_combine(const float* y, int k_splits, size_t cap, const int32_t* inv_per
                 int H, int out_dtype, void* out, int32_t* dev_status, void* stream);
 
 /* ---- the whole forward -----------------------------------------------------
- * Runs [fp8 step (MX only)] -> align -> GEMM1 -> GEMM2 -> combine on
+ * Runs align -> [fp8 step with the gather (MX only)] -> GEMM1 -> GEMM2 ->
+ * combine on
  * `stream`, with every intermediate in `workspace` (device memory of at
  * least moe_workspace_size(p) bytes, 256-byte aligned, owned by the caller,
  * reusable across calls but not shared by calls in flight at once).
  *   x (T, H) act; topk_ids (T, K) int32; topk_weights (T, K) fp32;
- *   w13 (E, 2I, H), w2 (E, H, I) (MX: packed + scales as above);
- *   out (T, H) act.
+ *   w13 (E, 2I, H), w2 (E, H, I) (MX: packed values and scale images of
+ *   moe_pack_mx_weights); out (T, H) act.
  * The status word at MOE_WS_STATUS is cleared at the start of each call. */
 int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                 const float* topk_weights, const void* w13, const uint8_t* w13_scale,

@@ -12,12 +12,15 @@ import torch
 
 from . import _abi
 from ._abi import (MOE_BF16, MOE_E2M1_MX, MOE_E4M3, MOE_F32, MoEError, Problem, moe_abi_version,
-                   moe_align, moe_align_capacity, moe_combine, moe_forward, moe_gemm1_silu,
-                   moe_gemm2_default_splits, moe_gemm2_weighted, moe_get_device_status,
-                   moe_quantize_x_fp8, moe_resolve_block_m, moe_workspace_offsets,
-                   moe_workspace_size)
+                   moe_align, moe_align_capacity, moe_combine, moe_forward, moe_forward_noalloc,
+                   moe_gemm1_silu, moe_gemm2_default_splits, moe_gemm2_weighted,
+                   moe_get_device_status, moe_mx_packed_bytes, moe_pack_mx_weights,
+                   moe_quantize_gather_x_fp8, moe_quantize_x_fp8, moe_resolve_block_m,
+                   moe_workspace_offsets, moe_workspace_size)
 
 __all__ = ["MoEError", "Problem", "make_problem", "dtype_code", "align", "Workspace", "forward",
+           "pack_mx", "moe_forward_noalloc", "moe_mx_packed_bytes", "moe_pack_mx_weights",
+           "moe_quantize_gather_x_fp8",
            "moe_abi_version", "moe_align", "moe_align_capacity", "moe_combine", "moe_forward",
            "moe_gemm1_silu", "moe_gemm2_default_splits", "moe_gemm2_weighted",
            "moe_get_device_status", "moe_quantize_x_fp8", "moe_resolve_block_m",
@@ -58,6 +61,22 @@ def align(topk_ids: torch.Tensor, E: int, block_m: int = 128, dev_status=None, s
     return out
 
 
+def pack_mx(w: torch.Tensor, w_scale: torch.Tensor, sections: int, stream=None):
+    """Packed (values, scale images) of an mxfp4 weight tensor in natural form
+    (E, R, K/2) + (E, R, K/32), as the block-scaled GEMMs read it; done once
+    when the model is loaded."""
+    E, R, half_k = w.shape
+    K = 2 * half_k
+    vb, sb = moe_mx_packed_bytes(E, R, K, sections)
+    Kp = (K + 127) // 128 * 128
+    vals = torch.empty((E, R, Kp // 2), dtype=torch.uint8, device=w.device)
+    imgs = torch.empty(sb, dtype=torch.uint8, device=w.device)
+    assert vals.numel() == vb
+    moe_pack_mx_weights(w.contiguous(), w_scale.contiguous(), E, R, K, sections, vals, imgs,
+                        stream)
+    return vals, imgs
+
+
 class Workspace:
     """A device buffer sized for one problem, with views of its parts."""
 
@@ -82,8 +101,7 @@ def forward(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=None, o
             workspace: Workspace | None = None, weight=None, h_scale=1.0, stream=None):
     """out = MoE expert FFN of x routed by (topk_ids, topk_weights)."""
     T, H = x.shape
-    E = w13.shape[0]
-    I = w2.shape[2] * (2 if weight in ("mxfp4", MOE_E2M1_MX) else 1)
+    E, I = w13.shape[0], w13.shape[1] // 2
     K = topk_ids.shape[1]
     p = make_problem(T, H, I, E, K, x.dtype, weight, 0, h_scale)
     if workspace is None:

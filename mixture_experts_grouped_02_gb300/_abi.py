@@ -34,7 +34,8 @@ MOE_F32, MOE_BF16, MOE_E4M3, MOE_E2M1_MX = 0, 1, 2, 3
 EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_align_capacity",
            "moe_gemm2_default_splits", "moe_workspace_size", "moe_workspace_offsets", "moe_align",
            "moe_quantize_x_fp8", "moe_gemm1_silu", "moe_gemm2_weighted", "moe_combine",
-           "moe_forward", "moe_forward_noalloc", "moe_get_device_status")
+           "moe_forward", "moe_forward_noalloc", "moe_get_device_status", "moe_mx_packed_bytes",
+           "moe_pack_mx_weights", "moe_quantize_gather_x_fp8")
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -97,6 +98,8 @@ def _declare(L):
     L.moe_align.argtypes = [vp, i32, i32, i32, i32] + [vp] * 8 + [vp]
     L.moe_quantize_x_fp8.restype = i32
     L.moe_quantize_x_fp8.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+    L.moe_quantize_gather_x_fp8.restype = i32
+    L.moe_quantize_gather_x_fp8.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     L.moe_gemm1_silu.restype = i32
     L.moe_gemm1_silu.argtypes = [PP] + [vp] * 10
     L.moe_gemm2_weighted.restype = i32
@@ -109,6 +112,10 @@ def _declare(L):
     L.moe_forward_noalloc.argtypes = [PP] + [vp] * 9
     L.moe_get_device_status.restype = i32
     L.moe_get_device_status.argtypes = [vp, vp]
+    L.moe_mx_packed_bytes.restype = sz
+    L.moe_mx_packed_bytes.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.moe_pack_mx_weights.restype = i32
+    L.moe_pack_mx_weights.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
 
 
 def status_string(status: int) -> str:
@@ -186,6 +193,13 @@ def moe_quantize_x_fp8(x, x_dtype, T, H, xq, row_scale, stream=None):
                                     _stream(stream)), "moe_quantize_x_fp8")
 
 
+def moe_quantize_gather_x_fp8(x, x_dtype, T, H, K, inv_perm, xq_sorted, row_scale,
+                              dev_status=None, stream=None):
+    _check(lib().moe_quantize_gather_x_fp8(_p(x), x_dtype, T, H, K, _p(inv_perm), _p(xq_sorted),
+                                           _p(row_scale), _p(dev_status), _stream(stream)),
+           "moe_quantize_gather_x_fp8")
+
+
 def moe_gemm1_silu(p: Problem, x, x_row_scale, w13, w13_scale, sorted_ids, block_info,
                    num_blocks, h, dev_status=None, stream=None):
     _check(lib().moe_gemm1_silu(ctypes.byref(p), _p(x), _p(x_row_scale), _p(w13), _p(w13_scale),
@@ -224,6 +238,19 @@ def moe_forward_noalloc(p: Problem, x, topk_ids, topk_weights, w13, w13_scale, w
     _check(lib().moe_forward_noalloc(ctypes.byref(p), _p(x), _p(topk_ids), _p(topk_weights),
                                      _p(w13), _p(w13_scale), _p(w2), _p(w2_scale), _p(out),
                                      _stream(stream)), "moe_forward_noalloc")
+
+
+def moe_mx_packed_bytes(E, R, K, sections):
+    vb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    total = lib().moe_mx_packed_bytes(E, R, K, sections, ctypes.byref(vb), ctypes.byref(sb))
+    if total == 0:
+        raise MoEError(MOE_ERR_INVALID_ARG, "moe_mx_packed_bytes")
+    return vb.value, sb.value
+
+
+def moe_pack_mx_weights(w, w_scale, E, R, K, sections, w_packed, scale_packed, stream=None):
+    _check(lib().moe_pack_mx_weights(_p(w), _p(w_scale), E, R, K, sections, _p(w_packed),
+                                     _p(scale_packed), _stream(stream)), "moe_pack_mx_weights")
 
 
 def moe_get_device_status(dev_status, stream=None) -> int:

@@ -2,11 +2,13 @@
 // fp8 (e4m3) activations times mxfp4 weights (e2m1 values, one e8m0 scale per
 // 32 K elements), tcgen05 block-scaled MMAs (kind::mxf8f6f4) on sm_103a.
 //
-// Sources: "MOE Bmm1 Fused Gather" -- mma_partition issues block-scaled MMAs
-// of e2m1 weights against e4m3 activations with the weight scales copied into
-// tensor memory before each MMA, and ws_matmul_kernel fills the activation
-// scale tensor with the e8m0 code 127 (unit scales; here the per-row fp8 scale
-// of x is applied in the epilogue instead); pack_e4m3x2 (fp32 -> e4m3, round
+// Sources: "MOE Bmm1 Fused Gather" -- load_weights brings a weight tile and
+// its scale tile in by TMA, mma_partition copies the scales into tensor
+// memory (tcgen05_copy) and issues block-scaled MMAs of e2m1 weights against
+// e4m3 activations, and ws_matmul_kernel fills the activation scale tensor
+// with the e8m0 code 127 (unit scales; here the per-row fp8 scale of x is
+// applied in the epilogue instead); the weights arrive pre-arranged for the
+// kernel (its MX4 value and scale layouts); pack_e4m3x2 (fp32 -> e4m3, round
 // to nearest even, saturating) for the hidden activation.  The SiLU*up and
 // routing-weight epilogues are those of gemm.cu.
 //
@@ -14,28 +16,23 @@
 //  * tile = 128 sorted rows x 192 weight rows, as two MMAs of N = 96:
 //    gate/up: 96 gate rows and the matching 96 up rows of w13[e];
 //    down: 192 rows of w2[e];
-//  * 5 shared-memory stages of 40 KB, 128 K elements each: A = 128 rows of
-//    e4m3 (128 B, 128-byte swizzled K-major), B = 192 rows of e2m1 in the
-//    padded form the block-scaled MMA reads 4-bit operands in (16 values =
-//    8 packed bytes at the start of each 16-byte slot, the other 8 bytes
-//    zero), swizzled the same way;
-//  * producer warps 0-3 fill a stage with cp.async (16-byte chunks of A --
-//    gathered token rows for gate/up, contiguous h rows for down -- and
-//    8-byte packed chunks of B straight from the weights' natural packed
-//    layout; the ragged end of K is zero-filled), and write the stage's B
-//    scale factors (fetched one stage ahead) into tensor memory with
-//    tcgen05.st; they publish the stage (proxy fence, tcgen05 fence, mbarrier
-//    arrive) once the copies of kStages - 2 later stages are issued;
-//  * warp 4 issues the MMAs from one thread; warps 5-8 run the epilogue;
+//  * 5 shared-memory stages of 128 K elements: A = 128 rows of e4m3 (128 B,
+//    128-byte swizzled K-major), B = 192 rows of e2m1 expanded by the TMA
+//    unit into the 16-byte slots the block-scaled MMA reads 4-bit operands
+//    from (16 values in the first 8 bytes), swizzled the same way, and two
+//    512-byte scale images (one per MMA half);
+//  * one producer thread fills a stage with TMA: A as a plain tile of sorted
+//    rows (gate/up: the fp8 step has already written each token's codes to
+//    the slots it occupies, so the gather happened there; down: hq; the end
+//    of K past the tensor reads as zeros), the weight tile and the two scale
+//    images (bulk copies), all completing one mbarrier;
+//  * the MMA thread copies each stage's scale images into tensor memory
+//    (tcgen05.cp, 32 x 128 bits replicated into the four lane quarters:
+//    column c of lane l holds the 4 K-block scales of row 32c + l) and
+//    issues the MMAs, choosing the scale byte of each 32-element K block by
+//    the instruction descriptor's scale ids;
 //  * tensor memory: two 192-column fp32 accumulators, 4 columns of unit A
-//    scales, and per stage and MMA half 4 columns of B scales.
-//
-// Scale factors in tensor memory: one 32-bit word per lane and column holds
-// the scales of 4 consecutive 32-element K blocks of one row (byte j = block
-// j, chosen per MMA by the instruction descriptor's scale ids); the rows of a
-// 128-row scale matrix are spread over 4 columns, column c of lane l holding
-// row 32c + l, and the same words are written into each of the 4 lane
-// quarters so that every quarter of the tensor core reads all of them.
+//    scales, 4 columns of B scales per stage and MMA half.
 //
 // All waits are bounded as in gemm.cu.
 #include <cuda_bf16.h>
@@ -49,6 +46,7 @@ namespace {
 
 enum MxKind { kMxGateUp = 0, kMxDown = 1 };
 
+template <int KIND>
 struct MxCfg {
   static constexpr int kBM = kBlockM;                 // 128 sorted rows
   static constexpr int kHalf = 96;                    // weight rows per MMA
@@ -58,46 +56,29 @@ struct MxCfg {
   static constexpr int kUmmaK = 32;                   // K per MMA (one scale block)
   static constexpr int kStages = 5;
   static constexpr int kABytes = kBM * kRowBytes;     // 16 KB
-  static constexpr int kBBytes = kBN * kRowBytes;     // 24 KB
+  static constexpr int kBBytes = kBN * kRowBytes;     // 24 KB in shared memory
+  static constexpr int kBDataBytes = kBN * kBK / 2;   // 12 KB of packed values
+  static constexpr int kSfImage = 512;                // one 96-row x 4-block scale image
+  static constexpr int kSfBytes = 2 * kSfImage;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kAccCols = kBN;                // 192 fp32 columns
   static constexpr int kSfaCol = 2 * kAccCols;        // 384: unit A scales (4 columns)
   static constexpr int kSfbCol0 = kSfaCol + 4;        // 388: B scales, 4 columns per stage/half
   static constexpr int kTmemCols = 512;
-  static constexpr int kProducerWarps = 4;
+  static constexpr int kProducerWarps = 1;
   static constexpr int kMmaWarp = kProducerWarps;
   static constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
-  // a producer thread publishes stage n once stage n + kLag is issued; the lag
-  // leaves one stage of slack so that n is published while the tensor core
-  // still works on n - 1
-  static constexpr int kLag = kStages - 2;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+  // bytes the TMA unit and the bulk copies deliver per stage
+  static constexpr uint32_t kTxBytes = kABytes + kBDataBytes + kSfBytes;
+  static constexpr int kSmemBytes = kStages * (kStageBytes + kSfBytes) + 1024;
   static constexpr uint32_t kIdesc = make_idesc_mx_e4m3_e2m1(kBM, kHalf);
 };
-static_assert(MxCfg::kSfbCol0 + MxCfg::kStages * 2 * 4 <= MxCfg::kTmemCols, "TMEM budget");
-static_assert(MxCfg::kLag < MxCfg::kStages, "publication lag must stay inside the ring");
+static_assert(MxCfg<0>::kSfbCol0 + MxCfg<0>::kStages * 2 * 4 <= MxCfg<0>::kTmemCols,
+              "TMEM budget");
 
+template <int KIND>
 __device__ __forceinline__ uint32_t sfb_col(int stage, int half) {
-  return MxCfg::kSfbCol0 + (stage * 2 + half) * 4;
-}
-
-// Scales of K blocks 4*kt .. 4*kt+3 of one weight row, one byte each
-// (blocks past the row's end read as 127, a unit scale; their values are 0).
-// Rows of an even number of blocks are read as two 16-bit words.
-__device__ __forceinline__ uint32_t scale_word(const uint8_t* srow, int kt, int nblocks) {
-  const int b0 = kt * 4;
-  if ((nblocks & 1) == 0 && b0 + 4 <= nblocks) {
-    const uint16_t* p = reinterpret_cast<const uint16_t*>(srow + b0);
-    return static_cast<uint32_t>(__ldg(p)) | (static_cast<uint32_t>(__ldg(p + 1)) << 16);
-  }
-  uint32_t w = 0;
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const int blk = b0 + b;
-    const uint32_t v = blk < nblocks ? static_cast<uint32_t>(__ldg(srow + blk)) : 127u;
-    w |= v << (8 * b);
-  }
-  return w;
+  return MxCfg<KIND>::kSfbCol0 + (stage * 2 + half) * 4;
 }
 
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
@@ -111,9 +92,19 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return g / (1.0f + __expf(-g)) * u;
 }
 
+// Scale image of (expert, section, 96-row group, K tile).
+__device__ __forceinline__ const uint8_t* sf_image(const MxArgs& a, int e, int sec, int grp,
+                                                   int kt) {
+  const long long idx =
+      ((static_cast<long long>(e) * a.sections + sec) * a.groups + grp) * a.kp_tiles + kt;
+  return a.w_scale + idx * 512;
+}
+
 template <int KIND>
-__global__ void __launch_bounds__(MxCfg::kThreads, 1) mx_gemm_kernel(const __grid_constant__ MxArgs a) {
-  using C = MxCfg;
+__global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ MxArgs a, const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmW) {
+  using C = MxCfg<KIND>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::kStages];
   __shared__ __align__(8) uint64_t empty_bar[C::kStages];
@@ -128,13 +119,14 @@ __global__ void __launch_bounds__(MxCfg::kThreads, 1) mx_gemm_kernel(const __gri
   const int lane = threadIdx.x & 31;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t smemA = smem_base;
-  const uint32_t smemB = smem_base + C::kStages * C::kABytes;
+  const uint32_t smemB = smemA + C::kStages * C::kABytes;
+  const uint32_t smemS = smemB + C::kStages * C::kBBytes;
 
   if (threadIdx.x == 0) {
     s_skip = (a.status != nullptr && *reinterpret_cast<volatile int32_t*>(a.status) != 0);
     s_abort = 0;
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(smem_u32(&full_bar[i]), C::kProducerWarps * 32);
+      mbar_init(smem_u32(&full_bar[i]), 1);
       mbar_init(smem_u32(&empty_bar[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -144,8 +136,8 @@ __global__ void __launch_bounds__(MxCfg::kThreads, 1) mx_gemm_kernel(const __gri
     mbar_init(smem_u32(&drain_bar), 1);
     fence_barrier_init();
   }
-  // the padding half of every 16-byte slot of the B stages stays zero: the
-  // copies below only ever write the first 8 bytes of a slot
+  // the TMA unit writes only the first 8 bytes of each 16-byte slot of B;
+  // the other 8 stay zero
   {
     uint4* b = reinterpret_cast<uint4*>(smem_raw + (smemB - smem_u32(smem_raw)));
     for (int i = threadIdx.x; i < C::kStages * C::kBBytes / 16; i += blockDim.x)
@@ -155,13 +147,17 @@ __global__ void __launch_bounds__(MxCfg::kThreads, 1) mx_gemm_kernel(const __gri
   __syncthreads();
   if (s_skip) return;
   if (warp == C::kMmaWarp) tmem_alloc(smem_u32(&s_tmem_base), C::kTmemCols);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmW);
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = s_tmem_base;
-  if (warp < C::kProducerWarps) {  // unit activation scales, every lane quarter
-    tmem_st4(tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + C::kSfaCol, 0x7F7F7F7Fu,
-             0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  if (warp > C::kMmaWarp) {  // unit activation scales, one lane quarter per epilogue warp
+    tmem_st4(tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kSfaCol,
+             0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
     tmem_wait_st();
   }
   tc_fence_before_sync();
@@ -171,115 +167,61 @@ __global__ void __launch_bounds__(MxCfg::kThreads, 1) mx_gemm_kernel(const __gri
   const int num_blocks = *a.num_blocks;
   const int total = num_blocks * a.n_tiles * a.splits;
   const uint64_t to = a.timeout_ns;
-  const int nblocks_k = a.Kdim / 32;  // scale blocks per weight row
-  const long long wpitch = a.Kdim / 2;
+
+  // A tile, weight tile and scale images of one stage; thread-0 work
+  auto load_stage = [&](const Tile& t, int e, int r0, int kt, uint32_t stage) {
+    const uint32_t fb = smem_u32(&full_bar[stage]);
+    const uint32_t b_dst = smemB + stage * C::kBBytes;
+    const uint32_t s_dst = smemS + stage * C::kSfBytes;
+    mbar_arrive_expect_tx(fb, C::kTxBytes);
+    tma_load_2d(smemA + stage * C::kABytes, &tmA, fb, kt * C::kBK, r0);
+    if constexpr (KIND == kMxGateUp) {
+      const int row = e * 2 * a.I + t.nt * C::kHalf;
+      tma_load_2d(b_dst, &tmW, fb, kt * C::kBK, row);
+      tma_load_2d(b_dst + C::kHalf * C::kRowBytes, &tmW, fb, kt * C::kBK, row + a.I);
+      bulk_load(s_dst, sf_image(a, e, 0, t.nt, kt), C::kSfImage, fb);
+      bulk_load(s_dst + C::kSfImage, sf_image(a, e, 1, t.nt, kt), C::kSfImage, fb);
+    } else {
+      tma_load_2d(b_dst, &tmW, fb, kt * C::kBK, e * a.H + t.nt * C::kBN);
+      bulk_load(s_dst, sf_image(a, e, 0, 2 * t.nt, kt), C::kSfImage, fb);
+      bulk_load(s_dst + C::kSfImage, sf_image(a, e, 0, 2 * t.nt + 1, kt), C::kSfImage, fb);
+    }
+  };
 
   if (warp < C::kProducerWarps) {
-    // ------------------------------------------------------------ producer
-    const int pt = threadIdx.x;      // 0..127
-    const int ch = pt & 7;           // chunk of the 128-element k-tile (16 elements)
-    const int rb = pt >> 3;          // rows rb + 16 j
-    const uint32_t sf_lane = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t stage = 0, phase = 0;
-    long long issued = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const Tile t = decode_tile(tile, num_blocks, a);
-      const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
-      const int e = bi.x, r0 = bi.z, valid = bi.w;
-      int kb, ke;
-      split_range(a, t.split, kb, ke);
-      const uint8_t* arow[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = rb + 16 * j;
-        if constexpr (KIND == kMxGateUp) {
-          const int tok = r < valid ? a.sorted_ids[r0 + r] / a.K : 0;
-          arow[j] = a.a + static_cast<long long>(tok) * a.H;
-        } else {
-          arow[j] = a.a + static_cast<long long>(r0 + r) * a.I;
+      // ------------------------------------------------------- TMA producer
+      uint32_t stage = 0, phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(tile, num_blocks, a);
+        const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
+        const int e = bi.x, r0 = bi.z;
+        int kb, ke;
+        split_range(a, t.split, kb, ke);
+        for (int kt = kb; kt < ke; ++kt) {
+          int good = 1;
+          if (lane == 0)
+            good = mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, to);
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) load_stage(t, e, r0, kt, stage);
+          ++issued;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
       }
-      // weight row of tile row n (0..191); rows past the expert's end are
-      // clamped to its last row (their products are never stored)
-      auto wrow_of = [&](int n) -> long long {
-        if constexpr (KIND == kMxGateUp) {
-          const int h = n >= C::kHalf ? 1 : 0;
-          const int jj = min(t.nt * C::kHalf + (n - h * C::kHalf), a.I - 1);
-          return static_cast<long long>(e) * 2 * a.I + h * a.I + jj;
-        } else {
-          return static_cast<long long>(e) * a.H + min(t.nt * C::kBN + n, a.H - 1);
-        }
-      };
-      const uint8_t* brow[12];
-#pragma unroll
-      for (int j = 0; j < 12; ++j) brow[j] = a.w + wrow_of(rb + 16 * j) * wpitch;
-      const uint8_t* srow[2][3];
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int c = 0; c < 3; ++c)
-          srow[h][c] = a.w_scale + wrow_of(h * C::kHalf + 32 * c + lane) * nblocks_k;
-
-      // scale words of the next stage are fetched one stage ahead
-      uint32_t sw[2][3];
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int c = 0; c < 3; ++c) sw[h][c] = kb < ke ? scale_word(srow[h][c], kb, nblocks_k) : 0u;
-
-      for (int kt = kb; kt < ke; ++kt) {
-        if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, to)) {
-          ok = false;
-          break;
-        }
-        const uint32_t a_dst = smemA + stage * C::kABytes;
-        const uint32_t b_dst = smemB + stage * C::kBBytes;
-        const int ka = kt * C::kBK + ch * 16;
-        const bool in_k = ka < a.Kdim;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = rb + 16 * j;
-          cp_async_16_zfill(a_dst + r * C::kRowBytes + ((ch ^ (r & 7)) << 4),
-                            in_k ? arow[j] + ka : arow[j], in_k ? 16u : 0u);
-        }
-#pragma unroll
-        for (int j = 0; j < 12; ++j) {
-          const int n = rb + 16 * j;
-          cp_async_8_zfill(b_dst + n * C::kRowBytes + ((ch ^ (n & 7)) << 4),
-                           in_k ? brow[j] + ka / 2 : brow[j], in_k ? 8u : 0u);
-        }
-        cp_async_commit();
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          tmem_st4(tmem_base + sf_lane + sfb_col(stage, h), sw[h][0], sw[h][1], sw[h][2],
-                   0x7F7F7F7Fu);
-        tmem_wait_st();
-        if (kt + 1 < ke) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int c = 0; c < 3; ++c) sw[h][c] = scale_word(srow[h][c], kt + 1, nblocks_k);
-        }
-        ++issued;
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-        if (issued > C::kLag) {
-          cp_async_wait<C::kLag>();
-          fence_proxy_async_smem();
-          tc_fence_before_sync();
-          const long long n = issued - 1 - C::kLag;
-          mbar_arrive(smem_u32(&full_bar[n % C::kStages]));
-        }
+      if (!ok && lane == 0) {
+        const long long first = issued > C::kStages ? issued - C::kStages : 0;
+        for (long long n = first; n < issued; ++n)
+          drain_wait(smem_u32(&full_bar[n % C::kStages]),
+                     static_cast<uint32_t>((n / C::kStages) & 1), to / 4);
       }
-    }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    for (long long n = issued > C::kLag ? issued - C::kLag : 0; n < issued; ++n)
-      mbar_arrive(smem_u32(&full_bar[n % C::kStages]));
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -304,6 +246,11 @@ __global__ void __launch_bounds__(MxCfg::kThreads, 1) mx_gemm_kernel(const __gri
           tc_fence_after_sync();
           const uint32_t a_base = smemA + stage * C::kABytes;
           const uint32_t b_base = smemB + stage * C::kBBytes;
+          const uint32_t s_base = smemS + stage * C::kSfBytes;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tmem_cp_32x128b_x4(tmem_base + sfb_col<KIND>(stage, h),
+                               rows16_desc(s_base + h * C::kSfImage));
 #pragma unroll
           for (int k = 0; k < C::kBK / C::kUmmaK; ++k) {
             const uint64_t ad = sw128_kmajor_desc(a_base + k * 32);
@@ -314,7 +261,7 @@ __global__ void __launch_bounds__(MxCfg::kThreads, 1) mx_gemm_kernel(const __gri
               const uint64_t bd =
                   sw128_kmajor_desc(b_base + h * C::kHalf * C::kRowBytes + k * 32);
               umma_mxf8f6f4(d_tmem + h * C::kHalf, ad, bd, idesc, sfa,
-                            tmem_base + sfb_col(stage, h), accum);
+                            tmem_base + sfb_col<KIND>(stage, h), accum);
             }
           }
           umma_commit(smem_u32(&empty_bar[stage]));
@@ -420,23 +367,84 @@ __global__ void __launch_bounds__(MxCfg::kThreads, 1) mx_gemm_kernel(const __gri
 }
 
 template <int KIND>
-cudaError_t launch(const MxArgs& a, int grid, cudaStream_t s) {
+cudaError_t launch(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW, int grid,
+                   cudaStream_t s) {
+  using C = MxCfg<KIND>;
   auto kern = mx_gemm_kernel<KIND>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         MxCfg::kSmemBytes);
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  kern<<<grid, MxCfg::kThreads, MxCfg::kSmemBytes, s>>>(a);
+  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(a, tmA, tmW);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ packing
+
+// Packed values: rows of Kp = round_up(K, 128) e2m1 elements, zero beyond K.
+__global__ void pack_values_kernel(const uint8_t* __restrict__ w, long long rows, int K, int Kp,
+                                   uint8_t* __restrict__ out) {
+  const long long out_pitch = Kp / 2, in_pitch = K / 2;
+  const long long n = rows * out_pitch;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = i / out_pitch, col = i - row * out_pitch;
+    out[i] = col < in_pitch ? w[row * in_pitch + col] : 0;
+  }
+}
+
+// Scale images: byte l*16 + c*4 + b of image (e, section, group, kt) is the
+// scale of section row 96 g + 32 c + l, K block 4 kt + b (c < 3), else 127.
+// Groups come in pairs (a 192-row tile reads two), so rows past the section's
+// end exist as unit scales.
+__global__ void pack_scales_kernel(const uint8_t* __restrict__ sc, int E, int R, int K,
+                                   int sections, int groups, int kp_tiles,
+                                   uint8_t* __restrict__ out) {
+  const int nblk = K / 32;
+  const int rows_per_sec = R / sections;
+  const long long n = static_cast<long long>(E) * sections * groups * kp_tiles * 512;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int byte = static_cast<int>(i & 511);
+    long long img = i >> 9;
+    const int kt = static_cast<int>(img % kp_tiles);
+    img /= kp_tiles;
+    const int g = static_cast<int>(img % groups);
+    img /= groups;
+    const int sec = static_cast<int>(img % sections);
+    const int e = static_cast<int>(img / sections);
+    const int l = byte >> 4, c = (byte >> 2) & 3, b = byte & 3;
+    const int srow = 96 * g + 32 * c + l;
+    const int blk = 4 * kt + b;
+    uint8_t v = 127;
+    if (c < 3 && srow < rows_per_sec && blk < nblk) {
+      const long long row = static_cast<long long>(e) * R + sec * rows_per_sec + srow;
+      v = sc[row * nblk + blk];
+    }
+    out[i] = v;
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_mx_gate_up(const MxArgs& a, int grid, cudaStream_t s) {
-  return launch<kMxGateUp>(a, grid, s);
+cudaError_t launch_mx_gate_up(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                              int grid, cudaStream_t s) {
+  return launch<kMxGateUp>(a, tmA, tmW, grid, s);
 }
 
-cudaError_t launch_mx_down(const MxArgs& a, int grid, cudaStream_t s) {
-  return launch<kMxDown>(a, grid, s);
+cudaError_t launch_mx_down(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                           int grid, cudaStream_t s) {
+  return launch<kMxDown>(a, tmA, tmW, grid, s);
+}
+
+cudaError_t launch_pack_mx(const uint8_t* w, const uint8_t* w_scale, int E, int R, int K,
+                           int sections, uint8_t* w_packed, uint8_t* s_packed, cudaStream_t s) {
+  const int Kp = (K + 127) / 128 * 128;
+  const int groups = mx_scale_groups(R / sections);
+  pack_values_kernel<<<1184, 256, 0, s>>>(w, static_cast<long long>(E) * R, K, Kp, w_packed);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  pack_scales_kernel<<<1184, 256, 0, s>>>(w_scale, E, R, K, sections, groups, Kp / 128, s_packed);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -58,10 +58,12 @@ struct MxArgs {
   int Kdim;
   int n_tiles, k_tiles, splits, band;
   long long cap;
-  const uint8_t* a;            // gate/up: xq (T, H) e4m3; down: hq (cap, I) e4m3
+  const uint8_t* a;            // gate/up: xq in sorted order (cap, H); down: hq (cap, I)
   const float* x_row_scale;    // gate/up: per-token fp32 scale of xq
-  const uint8_t* w;            // packed e2m1: w13 (E, 2I, H/2) or w2 (E, H, I/2)
-  const uint8_t* w_scale;      // e8m0: (E, 2I, H/32) or (E, H, I/32)
+  const uint8_t* w_scale;      // scale images (E, sections * groups, kp_tiles, 512 B)
+  int sections;                // 2 for w13 (gate rows, up rows), 1 for w2
+  int groups;                  // 96-row groups per section
+  int kp_tiles;                // 128-element K tiles per padded weight row
   const int32_t* sorted_ids;
   const int32_t* block_info;
   const int32_t* num_blocks;
@@ -72,8 +74,20 @@ struct MxArgs {
   unsigned long long timeout_ns;
 };
 
-cudaError_t launch_mx_gate_up(const MxArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_mx_down(const MxArgs& a, int grid, cudaStream_t s);
+// tmW: packed e2m1 values of w13 / w2, (E*R rows) x (Kp elements), box
+// 128 x 96 (gate/up) or 128 x 192 (down), expanded to 16-byte slots in shared
+// memory.  tmA: the e4m3 A rows in sorted order, xq (cap x H bytes) for
+// gate/up, hq (cap x I bytes) for down, box 128 x 128.
+cudaError_t launch_mx_gate_up(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                              int grid, cudaStream_t s);
+cudaError_t launch_mx_down(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                           int grid, cudaStream_t s);
+cudaError_t launch_pack_mx(const uint8_t* w, const uint8_t* w_scale, int E, int R, int K,
+                           int sections, uint8_t* w_packed, uint8_t* s_packed, cudaStream_t s);
+
+// 96-row scale groups per section of `rows` weight rows (an even number).
+inline int mx_scale_groups(int rows) { return 2 * ((rows + 191) / 192); }
+inline int mx_padded_k(int K) { return (K + 127) / 128 * 128; }
 
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const float* y, int splits, long long cap, const int32_t* inv_perm,
@@ -81,6 +95,9 @@ cudaError_t launch_combine(const float* y, int splits, long long cap, const int3
                            cudaStream_t s);
 cudaError_t launch_quantize_x(const void* x, int x_dtype, int T, int H, uint8_t* xq,
                               float* row_scale, cudaStream_t s);
+cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, int K,
+                                     const int32_t* inv_perm, uint8_t* xq_sorted,
+                                     float* row_scale, const int32_t* status, cudaStream_t s);
 
 // dtype: MOE_BF16 or MOE_F32.  tmA: down -> h (box 128 rows; unused by
 // gate/up, which gathers x itself).  tmB: w13 (box 128 rows) / w2 (box 256 rows).

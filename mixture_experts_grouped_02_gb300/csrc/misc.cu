@@ -90,7 +90,51 @@ __global__ void __launch_bounds__(256) quantize_x_kernel(const void* __restrict_
   }
 }
 
+// The same quantisation, with each token's codes written to every slot of the
+// expert-sorted list the token occupies (xq_sorted[inv_perm[t*K + k]]), so that
+// the block-scaled gate/up GEMM reads contiguous rows: the token gather is
+// fused into this pass, which reads every row of x anyway.
+__global__ void __launch_bounds__(256) quantize_gather_x_kernel(
+    const void* __restrict__ x, int bf16, int T, int H, int K, const int32_t* __restrict__ inv_perm,
+    uint8_t* __restrict__ xq_sorted, float* __restrict__ row_scale, const int32_t* status) {
+  if (status != nullptr && *status != 0) return;
+  __shared__ float s_red[8];
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const long long base = static_cast<long long>(t) * H;
+    float amax = 0.0f;
+    for (int c = threadIdx.x; c < H; c += blockDim.x) amax = fmaxf(amax, fabsf(load_act(x, bf16, base + c)));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = s_red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, s_red[w]);
+    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    if (threadIdx.x == 0) row_scale[t] = s;
+    for (int c = 2 * threadIdx.x; c < H; c += 2 * blockDim.x) {
+      const float v0 = __fdiv_rn(load_act(x, bf16, base + c), s);
+      const float v1 = __fdiv_rn(load_act(x, bf16, base + c + 1), s);
+      uint16_t pk;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pk) : "f"(v1), "f"(v0));
+      for (int k = 0; k < K; ++k) {
+        const long long slot = inv_perm[static_cast<long long>(t) * K + k];
+        *reinterpret_cast<uint16_t*>(xq_sorted + slot * H + c) = pk;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, int K,
+                                     const int32_t* inv_perm, uint8_t* xq_sorted,
+                                     float* row_scale, const int32_t* status, cudaStream_t s) {
+  const int grid = T < 65535 ? T : 65535;
+  quantize_gather_x_kernel<<<grid, 256, 0, s>>>(x, x_dtype == MOE_BF16 ? 1 : 0, T, H, K, inv_perm,
+                                                xq_sorted, row_scale, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const float* y, int splits, long long cap, const int32_t* inv_perm,
                            int T, int K, int H, int out_dtype, void* out, int32_t* status,

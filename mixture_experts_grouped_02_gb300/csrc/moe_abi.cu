@@ -143,7 +143,7 @@ void layout_of(const moe_problem_t* p, Layout* L) {
   sz[MOE_WS_INV_PERM] = 4ull * na;
   sz[MOE_WS_BLOCK_INFO] = 16ull * (cap / bm);
   sz[MOE_WS_NUM_BLOCKS] = 4;
-  sz[MOE_WS_XQ] = mx ? 1ull * p->T * p->H : 0;
+  sz[MOE_WS_XQ] = mx ? static_cast<size_t>(cap) * p->H : 0;  // sorted rows
   sz[MOE_WS_X_SCALE] = mx ? 4ull * p->T : 0;
   sz[MOE_WS_H] = static_cast<size_t>(cap) * p->I * (mx ? 1 : act_bytes(p->act));
   sz[MOE_WS_Y] = 4ull * splits * static_cast<size_t>(cap) * p->H;
@@ -175,8 +175,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-// 2-D row-major tensor (outer rows of `inner` elements), 128-byte swizzled
-// boxes of box_inner x box_outer elements.
+// 2-D row-major tensor of `outer` rows of `inner` elements, `row_bytes`
+// apart, read in 128-byte swizzled boxes of box_inner x box_outer elements.
+int make_map_typed(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, long long inner,
+                   long long outer, long long row_bytes, int box_inner, int box_outer) {
+  auto enc = encoder();
+  if (enc == nullptr) return MOE_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 31u) != 0) return MOE_ERR_INVALID_ARG;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner),
+                             static_cast<cuuint32_t>(box_outer)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+// bf16 / fp32 row-major tensor (outer rows of `inner` elements).
 int make_map(CUtensorMap* tm, int dtype, const void* base, long long inner, long long outer,
              int box_inner, int box_outer) {
   auto enc = encoder();
@@ -299,17 +316,27 @@ bool aligned(const void* ptr, uintptr_t n) { return (reinterpret_cast<uintptr_t>
 int run_gemm1_mx(const moe_problem_t* p, const void* xq, const float* x_row_scale, const void* w13,
                  const uint8_t* w13_scale, const int32_t* sorted_ids, const int32_t* block_info,
                  const int32_t* num_blocks, void* hq, int32_t* status, cudaStream_t s) {
-  if (!aligned(xq, 16) || !aligned(hq, 16) || !aligned(w13, 8)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(xq, 32) || !aligned(hq, 16) || !aligned(w13, 32) || !aligned(w13_scale, 16))
+    return MOE_ERR_INVALID_ARG;
   MxArgs a = mx_args(p);
+  const int Hp = mx_padded_k(p->H);
   a.Kdim = p->H;
   a.n_tiles = (p->I + 95) / 96;
-  a.k_tiles = (p->H + 127) / 128;
+  a.k_tiles = Hp / 128;
   a.splits = 1;
   a.band = std::min(kBand, a.n_tiles);
   a.a = static_cast<const uint8_t*>(xq);
   a.x_row_scale = x_row_scale;
-  a.w = static_cast<const uint8_t*>(w13);
   a.w_scale = w13_scale;
+  a.sections = 2;
+  a.groups = mx_scale_groups(p->I);
+  a.kp_tiles = Hp / 128;
+  CUtensorMap tmA, tmW;
+  int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, p->H, a.cap, p->H, 128, 128);
+  if (rc != MOE_OK) return rc;
+  rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, Hp, 2ll * p->I * p->E,
+                      Hp / 2, 128, 96);
+  if (rc != MOE_OK) return rc;
   a.sorted_ids = sorted_ids;
   a.block_info = block_info;
   a.num_blocks = num_blocks;
@@ -317,23 +344,33 @@ int run_gemm1_mx(const moe_problem_t* p, const void* xq, const float* x_row_scal
   a.status = status;
   const long long max_tiles = (a.cap / kBlockM) * a.n_tiles;
   const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
-  return cuda_status(launch_mx_gate_up(a, grid, s));
+  return cuda_status(launch_mx_gate_up(a, tmA, tmW, grid, s));
 }
 
 int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const uint8_t* w2_scale,
                  const float* topk_weights, const int32_t* sorted_ids, const int32_t* block_info,
                  const int32_t* num_blocks, float* y, int splits, int32_t* status,
                  cudaStream_t s) {
-  if (!aligned(hq, 16) || !aligned(w2, 8) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(hq, 32) || !aligned(w2, 32) || !aligned(w2_scale, 16) || !aligned(y, 16))
+    return MOE_ERR_INVALID_ARG;
   MxArgs a = mx_args(p);
+  const int Ip = mx_padded_k(p->I);
   a.Kdim = p->I;
   a.n_tiles = (p->H + 191) / 192;
-  a.k_tiles = (p->I + 127) / 128;
+  a.k_tiles = Ip / 128;
   a.splits = splits;
   a.band = std::min(kBand, a.n_tiles);
   a.a = static_cast<const uint8_t*>(hq);
-  a.w = static_cast<const uint8_t*>(w2);
   a.w_scale = w2_scale;
+  a.sections = 1;
+  a.groups = mx_scale_groups(p->H);
+  a.kp_tiles = Ip / 128;
+  CUtensorMap tmA, tmW;
+  int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq, p->I, a.cap, p->I, 128, 128);
+  if (rc != MOE_OK) return rc;
+  rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, Ip, 1ll * p->H * p->E,
+                      Ip / 2, 128, 192);
+  if (rc != MOE_OK) return rc;
   a.sorted_ids = sorted_ids;
   a.block_info = block_info;
   a.num_blocks = num_blocks;
@@ -342,7 +379,7 @@ int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const u
   a.status = status;
   const long long max_tiles = (a.cap / kBlockM) * a.n_tiles * splits;
   const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
-  return cuda_status(launch_mx_down(a, grid, s));
+  return cuda_status(launch_mx_down(a, tmA, tmW, grid, s));
 }
 
 }  // namespace
@@ -426,6 +463,17 @@ int moe_quantize_x_fp8(const void* x, int x_dtype, int T, int H, uint8_t* xq, fl
   if (!x || !xq || !row_scale) return MOE_ERR_INVALID_ARG;
   return cuda_status(
       launch_quantize_x(x, x_dtype, T, H, xq, row_scale, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_quantize_gather_x_fp8(const void* x, int x_dtype, int T, int H, int K,
+                              const int32_t* inv_perm, uint8_t* xq_sorted, float* row_scale,
+                              int32_t* dev_status, void* stream) {
+  if (T < 0 || H <= 0 || (H & 1) != 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (x_dtype != MOE_BF16 && x_dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !inv_perm || !xq_sorted || !row_scale) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_gather_x(x, x_dtype, T, H, K, inv_perm, xq_sorted, row_scale,
+                                              dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_scale,
@@ -520,7 +568,9 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
   if (is_mx(p)) {
     uint8_t* xq = part(MOE_WS_XQ);
     float* xs = reinterpret_cast<float*>(part(MOE_WS_X_SCALE));
-    if (launch_quantize_x(x, p->act, p->T, p->H, xq, xs, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_quantize_gather_x(x, p->act, p->T, p->H, p->K, inv_perm, xq, xs, status, s) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
     rc = run_gemm1_mx(p, xq, xs, w13, w13_scale, sorted_ids, block_info, num_blocks, h, status, s);
     if (rc != MOE_OK) return rc;
     rc = run_gemm2_mx(p, h, w2, w2_scale, topk_weights, sorted_ids, block_info, num_blocks, y,
@@ -535,6 +585,28 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
   }
   return cuda_status(launch_combine(y, splits, capacity(p->T, p->K, p->E, bm), inv_perm, p->T,
                                     p->K, p->H, p->act, out, status, s));
+}
+
+size_t moe_mx_packed_bytes(int E, int R, int K, int sections, size_t* value_bytes,
+                           size_t* scale_bytes) {
+  if (E <= 0 || R <= 0 || K <= 0 || K % 32 != 0 || (sections != 1 && sections != 2) ||
+      R % sections != 0)
+    return 0;
+  const size_t Kp = static_cast<size_t>(mx_padded_k(K));
+  const size_t vb = static_cast<size_t>(E) * R * (Kp / 2);
+  const size_t sb =
+      static_cast<size_t>(E) * sections * mx_scale_groups(R / sections) * (Kp / 128) * 512;
+  if (value_bytes) *value_bytes = vb;
+  if (scale_bytes) *scale_bytes = sb;
+  return vb + sb;
+}
+
+int moe_pack_mx_weights(const uint8_t* w, const uint8_t* w_scale, int E, int R, int K,
+                        int sections, uint8_t* w_packed, uint8_t* scale_packed, void* stream) {
+  if (moe_mx_packed_bytes(E, R, K, sections, nullptr, nullptr) == 0) return MOE_ERR_INVALID_ARG;
+  if (!w || !w_scale || !w_packed || !scale_packed) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_mx(w, w_scale, E, R, K, sections, w_packed, scale_packed,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 int moe_get_device_status(const int32_t* dev_status, void* stream) {

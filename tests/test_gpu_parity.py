@@ -313,6 +313,58 @@ def _mx_problem(case, seed):
     return cfg, gen.generate(cfg, seed=seed)
 
 
+@pytest.mark.parametrize("T,H,K,E", [(2048, 2880, 4, 128), (37, 64, 2, 5)])
+def test_quantize_gather_x_fp8_bit_exact(T, H, K, E):
+    """Codes at every sorted slot of a token equal the oracle's codes of that
+    token, bit for bit; the row scales too."""
+    g = torch.Generator().manual_seed(T)
+    x = (torch.randn((T, H), generator=g) * 3).to(torch.bfloat16)
+    ids = pins.align_ids(T, K, E, "normal", seed=4)
+    al = oracle.align(ids, E, 128)
+    cap = len(al["sorted_ids"])
+    xq_ref, s_ref = oracle.quantize_x_fp8(np_store(x))
+    xs = torch.zeros((cap, H), dtype=torch.uint8, device="cuda")
+    s = torch.empty(T, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_gather_x_fp8(x.cuda(), moe.MOE_BF16, T, H, K,
+                                  torch.from_numpy(al["inv_perm"]).cuda(), xs, s)
+    torch.cuda.synchronize()
+    valid = al["sorted_ids"] < T * K
+    got = xs.cpu().numpy()
+    assert np.array_equal(got[valid], xq_ref[al["sorted_ids"][valid] // K])
+    assert np.all(got[~valid] == 0)  # padding slots untouched
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("E,R,K,sections", [(2, 200, 320, 2), (3, 300, 128, 1), (1, 96, 2880, 1)])
+def test_pack_mx_layout(E, R, K, sections):
+    """The packed values and scale images hold exactly the bytes the layout in
+    include/moe.h puts where (built here with numpy index arithmetic)."""
+    rng = np.random.default_rng(E * R + K)
+    w = rng.integers(0, 256, (E, R, K // 2)).astype(np.uint8)
+    sc = rng.integers(0, 256, (E, R, K // 32)).astype(np.uint8)
+    vals, imgs = moe.pack_mx(torch.from_numpy(w).cuda(), torch.from_numpy(sc).cuda(), sections)
+    torch.cuda.synchronize()
+    Kp = (K + 127) // 128 * 128
+    exp_vals = np.zeros((E, R, Kp // 2), np.uint8)
+    exp_vals[..., :K // 2] = w
+    assert np.array_equal(vals.cpu().numpy(), exp_vals)
+    rs = R // sections
+    G, KT = 2 * (-(-rs // 192)), Kp // 128
+    exp = np.full((E, sections, G, KT, 32, 4, 4), 127, np.uint8)
+    for g in range(G):
+        for c in range(3):
+            for l in range(32):
+                row = 96 * g + 32 * c + l
+                if row >= rs:
+                    continue
+                for kt in range(KT):
+                    for b in range(4):
+                        blk = 4 * kt + b
+                        if blk < K // 32:
+                            exp[:, :, g, kt, l, c, b] = sc[:, np.arange(sections) * rs + row, blk]
+    assert np.array_equal(imgs.cpu().numpy(), exp.ravel())
+
+
 @pytest.mark.parametrize("case", MX_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d" % c)
 def test_mx_gemm1_stage(case):
     cfg, inp = _mx_problem(case, 41)
@@ -325,8 +377,13 @@ def test_mx_gemm1_stage(case):
     cap = moe.moe_align_capacity(T, K, E, 128)
     hq = torch.zeros((cap, I), dtype=torch.uint8, device="cuda")
     st = _status()
-    moe.moe_gemm1_silu(p, torch.from_numpy(xq_ref).cuda(), torch.from_numpy(s_ref).cuda(), d.w13,
-                       d.w13_scale, al["sorted_ids"], al["block_info"], al["num_blocks"], hq, st)
+    w13p, s13p = moe.pack_mx(d.w13, d.w13_scale, 2)
+    # the oracle's codes placed at the sorted slots of their tokens
+    xs = np.zeros((cap, H), np.uint8)
+    valid = al_ref["sorted_ids"] < T * K
+    xs[valid] = xq_ref[al_ref["sorted_ids"][valid] // K]
+    moe.moe_gemm1_silu(p, torch.from_numpy(xs).cuda(), torch.from_numpy(s_ref).cuda(), w13p,
+                       s13p, al["sorted_ids"], al["block_info"], al["num_blocks"], hq, st)
     assert moe.moe_get_device_status(st) == 0
     rows = _valid_rows(al_ref, T * K)
     eor = _expert_of_rows(al_ref, rows, inp.topk_ids.numpy().ravel())
@@ -359,7 +416,8 @@ def test_mx_gemm2_stage(case, splits):
     p = moe.make_problem(T, H, I, E, K, "bf16", "mxfp4", h_scale=0.25)
     y = torch.full((splits, cap, H), float("nan"), dtype=torch.float32, device="cuda")
     st = _status()
-    moe.moe_gemm2_weighted(p, torch.from_numpy(codes).cuda(), d.w2, d.w2_scale, d.topk_weights,
+    w2p, s2p = moe.pack_mx(d.w2, d.w2_scale, 1)
+    moe.moe_gemm2_weighted(p, torch.from_numpy(codes).cuda(), w2p, s2p, d.topk_weights,
                            al["sorted_ids"], al["block_info"], al["num_blocks"], y, splits, st)
     assert moe.moe_get_device_status(st) == 0
     rows = _valid_rows(al_ref, T * K)
@@ -378,8 +436,10 @@ def _run_forward_mx(d, cfg, h_scale=1.0):
     ws = moe.Workspace(p)
     ws.buffer.fill_(0xFF)
     out = torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16, device="cuda")
-    moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, d.w13, d.w13_scale, d.w2, d.w2_scale, out,
-                    ws.buffer, ws.nbytes)
+    w13p, s13p = moe.pack_mx(d.w13, d.w13_scale, 2)
+    w2p, s2p = moe.pack_mx(d.w2, d.w2_scale, 1)
+    moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, w13p, s13p, w2p, s2p, out, ws.buffer,
+                    ws.nbytes)
     assert moe.moe_get_device_status(ws.status) == 0
     return out
 
