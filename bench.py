@@ -316,7 +316,8 @@ def run_ours(args, ws, rank, local):
         w13, s13 = moe.pack_mx(inp.w13, inp.w13_scale, 2)
         w2, s2 = moe.pack_mx(inp.w2, inp.w2_scale, 1)
     splits = moe.moe_gemm2_default_splits(p)
-    cap = moe.moe_align_capacity(cfg.T, cfg.K, cfg.E, 128)
+    bm = moe.moe_resolve_block_m(p)  # the align block the GEMMs of this problem tile by
+    cap = moe.moe_align_capacity(cfg.T, cfg.K, cfg.E, bm)
     out = torch.empty((cfg.T, cfg.H), dtype=inp.x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
     st.zero_()
@@ -324,13 +325,18 @@ def run_ours(args, ws, rank, local):
     # exactly the launches moe_forward makes, one C-ABI call per stage
     stages = []
     stages.append(("align", lambda: moe.moe_align(
-        inp.topk_ids, cfg.T, cfg.K, cfg.E, 128, counts, offs, poffs, sorted_ids, inv, binfo, nblk,
+        inp.topk_ids, cfg.T, cfg.K, cfg.E, bm, counts, offs, poffs, sorted_ids, inv, binfo, nblk,
         st, stream)))
     if mx:
         stages.append(("quantize_gather_x", lambda: moe.moe_quantize_gather_x_fp8(
             inp.x, _abi.MOE_BF16, cfg.T, cfg.H, cfg.K, inv, xq, xs, st, stream)))
+    elif bm == 256:  # CTA pairs: the gather as its own pass
+        x_sorted = part(_abi.MOE_WS_XQ, inp.x.dtype)
+        stages.append(("gather", lambda: moe.moe_gather_rows(
+            inp.x, p.act, cfg.T, cfg.H, cfg.K, inv, x_sorted, st, stream)))
+    a_rows = xq if mx else (x_sorted if bm == 256 else inp.x)
     stages.append(("gemm_gate_up", lambda: moe.moe_gemm1_silu(
-        p, xq if mx else inp.x, xs, w13, s13, sorted_ids, binfo, nblk, h, st, stream)))
+        p, a_rows, xs, w13, s13, sorted_ids, binfo, nblk, h, st, stream)))
     stages.append(("gemm_down", lambda: moe.moe_gemm2_weighted(
         p, h, w2, s2, inp.topk_weights, sorted_ids, binfo, nblk, y, splits, st, stream)))
     stages.append(("combine", lambda: moe.moe_combine(
@@ -447,7 +453,7 @@ def run_ours(args, ws, rank, local):
             "dtype": {"bf16": "bf16", "f32": "f32 (tf32 MMA)",
                       "mxfp4": "e4m3 x mxfp4 (fp32 acc)"}[cfg.dtype], "data": "synthetic",
             "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
-                       "top_k": cfg.K, "global_batch_tokens": tokens_all,
+                       "top_k": cfg.K, "global_batch_tokens": tokens_all, "block_m": bm,
                        "parallelism": f"replicas{ws}",
                        "l2": "inputs larger than L2 (expert weights %.2f GB)" %
                              (bytes_alg / 1e9)},

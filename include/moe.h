@@ -64,7 +64,9 @@ typedef enum {
  *   weight : dtype of w13/w2: equal to act, or MOE_E2M1_MX (then act must
  *            be MOE_BF16; x is cast to e4m3 with one fp32 scale per row and
  *            the hidden activation is stored as e4m3(a / h_scale)).
- *   block_m: rows per alignment block, 0 = automatic (128).
+ *   block_m: rows per alignment block, 0 = automatic: 256 (the GEMMs then
+ *            run on CTA pairs) when bf16/fp32 experts receive at least 768
+ *            rows on average, else 128.
  *   h_scale: scale of the e4m3 hidden activation (MX weights only; 0 => 1). */
 typedef struct {
     int T, H, I, E, K;
@@ -85,7 +87,8 @@ typedef enum {
     MOE_WS_INV_PERM = 5,       /* int32[T*K]                                */
     MOE_WS_BLOCK_INFO = 6,     /* int32[cap/block_m][4]                     */
     MOE_WS_NUM_BLOCKS = 7,     /* int32[1]                                  */
-    MOE_WS_XQ = 8,             /* e4m3[cap][H], sorted (MX weights only)    */
+    MOE_WS_XQ = 8,             /* A rows in sorted order [cap][H]: e4m3     */
+                               /* (MX weights) or act (256-row blocks)      */
     MOE_WS_X_SCALE = 9,        /* fp32[T]      (MX weights only)            */
     MOE_WS_H = 10,             /* act or e4m3 [cap][I]                      */
     MOE_WS_Y = 11,             /* fp32[splits][cap][H]                      */
@@ -193,6 +196,15 @@ int moe_quantize_gather_x_fp8(const void* x, int x_dtype, int T, int H, int K,
                               const int32_t* inv_perm, uint8_t* xq_sorted, float* row_scale,
                               int32_t* dev_status, void* stream);
 
+/* ---- gather step (256-row blocks) -------------------------------------------
+ * Token rows to sorted slots: x_sorted[inv_perm[t*K + k], :] = x[t, :] for
+ * every choice of every token (rows of padding slots are not written); x
+ * (T, H) in dtype (MOE_BF16 / MOE_F32), x_sorted (cap, H), inv_perm from
+ * moe_align.  The gate/up GEMM on CTA pairs (block_m 256) reads its token rows
+ * in this sorted form.  Skipped when *dev_status != 0. */
+int moe_gather_rows(const void* x, int dtype, int T, int H, int K, const int32_t* inv_perm,
+                    void* x_sorted, int32_t* dev_status, void* stream);
+
 /* ---- gather + GEMM1 + SiLU*up -------------------------------------------
  * Source: "factor_moe_fused_gemm.cu", fused_silu_gate_kernel (gate = first
  * half of the w13 rows, up = second half, SiLU(g) = g / (1 + e^-g)) and
@@ -202,15 +214,18 @@ int moe_quantize_gather_x_fp8(const void* x, int x_dtype, int T, int H, int K,
  * For every slot s of a block b < *num_blocks with i = sorted_ids[s] < N_a
  * and e = block_info[b].expert:
  *   h[s, j] = SiLU(W13[e, j, :] . x[i / K, :]) * (W13[e, I + j, :] . x[i / K, :])
- * x    (T, H) act; for MX weights, the e4m3 codes in sorted order (cap, H)
- *      as written by moe_quantize_gather_x_fp8, with x_row_scale (T) fp32
+ * x    (T, H) act, gathered by the kernel; with 256-row blocks (CTA pairs)
+ *      the rows in sorted order (cap, H) as written by moe_gather_rows; for
+ *      MX weights, the e4m3 codes in sorted order (cap, H) as written by
+ *      moe_quantize_gather_x_fp8, with x_row_scale (T) fp32
  * w13  (E, 2I, H) weight dtype (MX: packed values + scale images of
  *      moe_pack_mx_weights with R = 2I, K = H, sections = 2)
  * h    (cap, I) act (MX: e4m3 codes of a / h_scale); rows of padding slots
  *      are not written.  H and I must be multiples of 64 (32 for MOE_F32 and
  *      for MX weights).
  * sorted_ids/block_info/num_blocks as written by moe_align with the same
- * block_m.  dev_status may be NULL. */
+ * block_m (128, or 256 for the CTA-pair GEMMs of bf16/fp32 weights).
+ * dev_status may be NULL. */
 int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_scale,
                    const void* w13, const uint8_t* w13_scale, const int32_t* sorted_ids,
                    const int32_t* block_info, const int32_t* num_blocks, void* h,
@@ -246,8 +261,8 @@ int moe_combine(const float* y, int k_splits, size_t cap, const int32_t* inv_per
                 int H, int out_dtype, void* out, int32_t* dev_status, void* stream);
 
 /* ---- the whole forward -----------------------------------------------------
- * Runs align -> [fp8 step with the gather (MX only)] -> GEMM1 -> GEMM2 ->
- * combine on
+ * Runs align -> [fp8 step with the gather (MX) | gather (256-row blocks)]
+ * -> GEMM1 -> GEMM2 -> combine on
  * `stream`, with every intermediate in `workspace` (device memory of at
  * least moe_workspace_size(p) bytes, 256-byte aligned, owned by the caller,
  * reusable across calls but not shared by calls in flight at once).
@@ -284,6 +299,10 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
 int moe_forward_noalloc(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                         const float* topk_weights, const void* w13, const uint8_t* w13_scale,
                         const void* w2, const uint8_t* w2_scale, void* out, void* stream);
+
+/* Launch geometry of the current device: its SM count and how many CTA pairs
+ * of the bf16 gate/up kernel it holds at once (0 if unknown). */
+int moe_device_info(int* sm_count, int* pair_clusters);
 
 /* Synchronise `stream` and return the device status word at dev_status
  * (MOE_OK when it is 0), or MOE_ERR_CUDA if the stream itself failed. */

@@ -13,14 +13,14 @@ import torch
 from . import _abi
 from ._abi import (MOE_BF16, MOE_E2M1_MX, MOE_E4M3, MOE_F32, MoEError, Problem, moe_abi_version,
                    moe_align, moe_align_capacity, moe_combine, moe_forward, moe_forward_noalloc,
-                   moe_gemm1_silu, moe_gemm2_default_splits, moe_gemm2_weighted,
+                   moe_gather_rows, moe_gemm1_silu, moe_gemm2_default_splits, moe_gemm2_weighted,
                    moe_get_device_status, moe_mx_packed_bytes, moe_pack_mx_weights,
                    moe_quantize_gather_x_fp8, moe_quantize_x_fp8, moe_resolve_block_m,
                    moe_workspace_offsets, moe_workspace_size)
 
 __all__ = ["MoEError", "Problem", "make_problem", "dtype_code", "align", "Workspace", "forward",
            "pack_mx", "moe_forward_noalloc", "moe_mx_packed_bytes", "moe_pack_mx_weights",
-           "moe_quantize_gather_x_fp8",
+           "moe_quantize_gather_x_fp8", "moe_gather_rows",
            "moe_abi_version", "moe_align", "moe_align_capacity", "moe_combine", "moe_forward",
            "moe_gemm1_silu", "moe_gemm2_default_splits", "moe_gemm2_weighted",
            "moe_get_device_status", "moe_quantize_x_fp8", "moe_resolve_block_m",

@@ -35,7 +35,8 @@ EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_a
            "moe_gemm2_default_splits", "moe_workspace_size", "moe_workspace_offsets", "moe_align",
            "moe_quantize_x_fp8", "moe_gemm1_silu", "moe_gemm2_weighted", "moe_combine",
            "moe_forward", "moe_forward_noalloc", "moe_get_device_status", "moe_mx_packed_bytes",
-           "moe_pack_mx_weights", "moe_quantize_gather_x_fp8")
+           "moe_pack_mx_weights", "moe_quantize_gather_x_fp8", "moe_device_info",
+           "moe_gather_rows")
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -98,6 +99,8 @@ def _declare(L):
     L.moe_align.argtypes = [vp, i32, i32, i32, i32] + [vp] * 8 + [vp]
     L.moe_quantize_x_fp8.restype = i32
     L.moe_quantize_x_fp8.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+    L.moe_gather_rows.restype = i32
+    L.moe_gather_rows.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
     L.moe_quantize_gather_x_fp8.restype = i32
     L.moe_quantize_gather_x_fp8.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     L.moe_gemm1_silu.restype = i32
@@ -112,6 +115,8 @@ def _declare(L):
     L.moe_forward_noalloc.argtypes = [PP] + [vp] * 9
     L.moe_get_device_status.restype = i32
     L.moe_get_device_status.argtypes = [vp, vp]
+    L.moe_device_info.restype = i32
+    L.moe_device_info.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(i32)]
     L.moe_mx_packed_bytes.restype = sz
     L.moe_mx_packed_bytes.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     L.moe_pack_mx_weights.restype = i32
@@ -193,6 +198,11 @@ def moe_quantize_x_fp8(x, x_dtype, T, H, xq, row_scale, stream=None):
                                     _stream(stream)), "moe_quantize_x_fp8")
 
 
+def moe_gather_rows(x, dtype, T, H, K, inv_perm, x_sorted, dev_status=None, stream=None):
+    _check(lib().moe_gather_rows(_p(x), dtype, T, H, K, _p(inv_perm), _p(x_sorted),
+                                 _p(dev_status), _stream(stream)), "moe_gather_rows")
+
+
 def moe_quantize_gather_x_fp8(x, x_dtype, T, H, K, inv_perm, xq_sorted, row_scale,
                               dev_status=None, stream=None):
     _check(lib().moe_quantize_gather_x_fp8(_p(x), x_dtype, T, H, K, _p(inv_perm), _p(xq_sorted),
@@ -251,6 +261,13 @@ def moe_mx_packed_bytes(E, R, K, sections):
 def moe_pack_mx_weights(w, w_scale, E, R, K, sections, w_packed, scale_packed, stream=None):
     _check(lib().moe_pack_mx_weights(_p(w), _p(w_scale), E, R, K, sections, _p(w_packed),
                                      _p(scale_packed), _stream(stream)), "moe_pack_mx_weights")
+
+
+def moe_device_info():
+    """(SM count, CTA pairs of the gate/up pair kernel the device holds)."""
+    sms, pairs = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().moe_device_info(ctypes.byref(sms), ctypes.byref(pairs)), "moe_device_info")
+    return sms.value, pairs.value
 
 
 def moe_get_device_status(dev_status, stream=None) -> int:

@@ -95,6 +95,8 @@ cudaError_t launch_combine(const float* y, int splits, long long cap, const int3
                            cudaStream_t s);
 cudaError_t launch_quantize_x(const void* x, int x_dtype, int T, int H, uint8_t* xq,
                               float* row_scale, cudaStream_t s);
+cudaError_t launch_gather_rows(const void* x, int T, int row_bytes, int K, const int32_t* inv_perm,
+                               void* xs, const int32_t* status, cudaStream_t s);
 cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, int K,
                                      const int32_t* inv_perm, uint8_t* xq_sorted,
                                      float* row_scale, const int32_t* status, cudaStream_t s);
@@ -104,6 +106,16 @@ cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, i
 cudaError_t launch_gemm_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmA,
                                 const CUtensorMap& tmB, int grid, cudaStream_t s);
 cudaError_t launch_gemm_down(int dtype, const GemmArgs& a, const CUtensorMap& tmA,
+                             const CUtensorMap& tmB, int grid, cudaStream_t s);
+
+// CTA-pair variants for 256-row align blocks (grid = 2 x clusters).
+constexpr int kPairBlockM = 256;
+// CTA pairs the device holds at once for the gate/up (kind 0) or down (1)
+// pair kernel, 0 if it cannot be determined.
+int pair_max_active(int kind, int dtype);
+cudaError_t launch_pair_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmA,
+                                const CUtensorMap& tmB, int grid, cudaStream_t s);
+cudaError_t launch_pair_down(int dtype, const GemmArgs& a, const CUtensorMap& tmA,
                              const CUtensorMap& tmB, int grid, cudaStream_t s);
 
 }  // namespace moe

@@ -125,7 +125,37 @@ __global__ void __launch_bounds__(256) quantize_gather_x_kernel(
   }
 }
 
+// Token rows to sorted slots: xs[inv_perm[t*K + k], :] = x[t, :] for every
+// choice k of token t (rows of padding slots untouched).  The gather of the
+// gate/up GEMM done as its own pass, for the CTA-pair GEMMs whose A operand
+// then arrives by plain TMA tiles.  16-byte copies; a CTA per token row.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
+                                                          int T, int row_vec, int K,
+                                                          const int32_t* __restrict__ inv_perm,
+                                                          uint4* __restrict__ xs,
+                                                          const int32_t* status) {
+  if (status != nullptr && *status != 0) return;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const uint4* src = x + static_cast<long long>(t) * row_vec;
+    for (int c = threadIdx.x; c < row_vec; c += blockDim.x) {
+      const uint4 v = __ldg(src + c);
+      for (int k = 0; k < K; ++k) {
+        const long long slot = inv_perm[static_cast<long long>(t) * K + k];
+        xs[slot * row_vec + c] = v;
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const void* x, int T, int row_bytes, int K, const int32_t* inv_perm,
+                               void* xs, const int32_t* status, cudaStream_t s) {
+  const int grid = T < 65535 ? T : 65535;
+  gather_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(x), T, row_bytes / 16, K,
+                                          inv_perm, static_cast<uint4*>(xs), status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, int K,
                                      const int32_t* inv_perm, uint8_t* xq_sorted,

@@ -39,7 +39,7 @@ int check_problem(const moe_problem_t* p) {
   if (p->T < 0 || p->H <= 0 || p->I <= 0 || p->E <= 0 || p->K <= 0) return MOE_ERR_INVALID_ARG;
   if (!valid_dtype_pair(p->act, p->weight)) return MOE_ERR_INVALID_ARG;
   if (p->block_m != 0 && p->block_m != 16 && p->block_m != 32 && p->block_m != 64 &&
-      p->block_m != 128)
+      p->block_m != 128 && p->block_m != 256)
     return MOE_ERR_INVALID_ARG;
   if (p->E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   const long long na = static_cast<long long>(p->T) * p->K;
@@ -47,7 +47,16 @@ int check_problem(const moe_problem_t* p) {
   return MOE_OK;
 }
 
-int block_m_of(const moe_problem_t* p) { return p->block_m == 0 ? kBlockM : p->block_m; }
+// Rows per align block.  The bf16/fp32 GEMMs run on CTA pairs (256-row
+// blocks) when experts receive many tokens on average -- padding each expert
+// to 256 instead of 128 rows then costs little -- and on single CTAs
+// (128-row blocks) otherwise.
+int block_m_of(const moe_problem_t* p) {
+  if (p->block_m != 0) return p->block_m;
+  if (p->weight == MOE_E2M1_MX) return kBlockM;
+  const long long na = static_cast<long long>(p->T) * p->K;
+  return na >= 768ll * p->E ? kPairBlockM : kBlockM;
+}
 
 bool is_mx(const moe_problem_t* p) { return p->weight == MOE_E2M1_MX; }
 
@@ -56,7 +65,9 @@ bool is_mx(const moe_problem_t* p) { return p->weight == MOE_E2M1_MX; }
 // blocks along K (the end of K inside a 128-element tile is zero-filled).
 // The GEMM tile is 128 sorted rows.
 int check_gemm_shapes(const moe_problem_t* p) {
-  if (block_m_of(p) != kBlockM) return MOE_ERR_UNSUPPORTED;
+  const int bm = block_m_of(p);
+  if (bm != kBlockM && !(bm == kPairBlockM && p->weight != MOE_E2M1_MX))
+    return MOE_ERR_UNSUPPORTED;
   if (is_mx(p)) {
     if (p->H % 32 != 0 || p->I % 32 != 0) return MOE_ERR_UNSUPPORTED;
     if (!(p->h_scale >= 0.0f) || p->h_scale > 3.0e38f) return MOE_ERR_INVALID_ARG;
@@ -143,7 +154,9 @@ void layout_of(const moe_problem_t* p, Layout* L) {
   sz[MOE_WS_INV_PERM] = 4ull * na;
   sz[MOE_WS_BLOCK_INFO] = 16ull * (cap / bm);
   sz[MOE_WS_NUM_BLOCKS] = 4;
-  sz[MOE_WS_XQ] = mx ? static_cast<size_t>(cap) * p->H : 0;  // sorted rows
+  // A rows in sorted order: e4m3 codes (MX), activation rows (CTA pairs)
+  sz[MOE_WS_XQ] = mx ? static_cast<size_t>(cap) * p->H
+                     : (bm == kPairBlockM ? static_cast<size_t>(cap) * p->H * act_bytes(p->act) : 0);
   sz[MOE_WS_X_SCALE] = mx ? 4ull * p->T : 0;
   sz[MOE_WS_H] = static_cast<size_t>(cap) * p->I * (mx ? 1 : act_bytes(p->act));
   sz[MOE_WS_Y] = 4ull * splits * static_cast<size_t>(cap) * p->H;
@@ -242,9 +255,31 @@ GemmArgs base_args(const moe_problem_t* p) {
   a.I = p->I;
   a.E = p->E;
   a.K = p->K;
-  a.cap = capacity(p->T, p->K, p->E, kBlockM);
+  a.cap = capacity(p->T, p->K, p->E, block_m_of(p));
   a.timeout_ns = kWaitTimeoutNs;
   return a;
+}
+
+// Persistent grid: one CTA per SM, no more CTAs than tiles.  CTA pairs: no
+// more pairs than the device holds at once (cluster placement can leave SMs
+// without a partner), so that every pair is resident from the start.
+int pair_limit(int kind, int dtype) {
+  static std::mutex mu;
+  static int cache[2][2] = {{-1, -1}, {-1, -1}};
+  std::lock_guard<std::mutex> lk(mu);
+  int& v = cache[kind][dtype == MOE_BF16 ? 1 : 0];
+  if (v < 0) v = pair_max_active(kind, dtype);
+  return v;
+}
+
+int grid_for(long long tiles, bool pairs, int kind = 0, int dtype = MOE_BF16) {
+  const long long sms = sm_count();
+  if (!pairs) return static_cast<int>(std::max(1ll, std::min(sms, tiles)));
+  long long limit = sms / 2;
+  const int held = pair_limit(kind, dtype);
+  if (held > 0) limit = std::min<long long>(limit, held);
+  const long long clusters = std::max(1ll, std::min(limit, tiles));
+  return static_cast<int>(2 * clusters);
 }
 
 int run_gemm1(const moe_problem_t* p, const void* x, const void* w13, const int32_t* sorted_ids,
@@ -264,12 +299,20 @@ int run_gemm1(const moe_problem_t* p, const void* x, const void* w13, const int3
   a.x = x;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) return MOE_ERR_INVALID_ARG;
   CUtensorMap tmB;
-  const int rc = make_map(&tmB, p->act, w13, p->H, 2ll * p->I * p->E, bk, 128);
+  int rc = make_map(&tmB, p->act, w13, p->H, 2ll * p->I * p->E, bk, 128);
   if (rc != MOE_OK) return rc;
-  const CUtensorMap& tmA = tmB;  // the gate/up kernel gathers x without a tensor map
-  const long long max_tiles = (a.cap / kBlockM) * a.n_tiles;
-  const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
-  return cuda_status(launch_gemm_gate_up(p->act, a, tmA, tmB, grid, s));
+  const int bm = block_m_of(p);
+  const long long max_tiles = (a.cap / bm) * a.n_tiles;
+  if (bm == kPairBlockM) {
+    // CTA pairs read x in sorted order (cap rows) as plain TMA tiles
+    CUtensorMap tmA;
+    rc = make_map(&tmA, p->act, x, p->H, a.cap, bk, 128);
+    if (rc != MOE_OK) return rc;
+    return cuda_status(
+        launch_pair_gate_up(p->act, a, tmA, tmB, grid_for(max_tiles, true, 0, p->act), s));
+  }
+  const CUtensorMap& tmA = tmB;  // the single-CTA kernel gathers x without a tensor map
+  return cuda_status(launch_gemm_gate_up(p->act, a, tmA, tmB, grid_for(max_tiles, false), s));
 }
 
 int run_gemm2(const moe_problem_t* p, const void* h, const void* w2, const float* topk_weights,
@@ -290,11 +333,16 @@ int run_gemm2(const moe_problem_t* p, const void* h, const void* w2, const float
   CUtensorMap tmA, tmB;
   int rc = make_map(&tmA, p->act, h, p->I, a.cap, bk, 128);
   if (rc != MOE_OK) return rc;
-  rc = make_map(&tmB, p->act, w2, p->I, 1ll * p->H * p->E, bk, 256);
+  const int bm = block_m_of(p);
+  const bool pairs = bm == kPairBlockM;
+  // single CTA: one 256-row box of w2; pairs: each CTA loads 128 of the 256 rows
+  rc = make_map(&tmB, p->act, w2, p->I, 1ll * p->H * p->E, bk, pairs ? 128 : 256);
   if (rc != MOE_OK) return rc;
-  const long long max_tiles = (a.cap / kBlockM) * a.n_tiles * splits;
-  const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
-  return cuda_status(launch_gemm_down(p->act, a, tmA, tmB, grid, s));
+  const long long max_tiles = (a.cap / bm) * a.n_tiles * splits;
+  if (pairs)
+    return cuda_status(
+        launch_pair_down(p->act, a, tmA, tmB, grid_for(max_tiles, true, 1, p->act), s));
+  return cuda_status(launch_gemm_down(p->act, a, tmA, tmB, grid_for(max_tiles, false), s));
 }
 
 MxArgs mx_args(const moe_problem_t* p) {
@@ -441,7 +489,7 @@ int moe_align(const int32_t* topk_ids, int T, int K, int E, int block_m, int32_t
               int32_t* offsets, int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
               int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream) {
   if (T < 0 || K <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
-  if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128)
+  if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128 && block_m != 256)
     return MOE_ERR_INVALID_ARG;
   if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(T) * K >= (1ll << 30)) return MOE_ERR_UNSUPPORTED;
@@ -463,6 +511,20 @@ int moe_quantize_x_fp8(const void* x, int x_dtype, int T, int H, uint8_t* xq, fl
   if (!x || !xq || !row_scale) return MOE_ERR_INVALID_ARG;
   return cuda_status(
       launch_quantize_x(x, x_dtype, T, H, xq, row_scale, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_gather_rows(const void* x, int dtype, int T, int H, int K, const int32_t* inv_perm,
+                    void* x_sorted, int32_t* dev_status, void* stream) {
+  if (T < 0 || H <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  const long long row_bytes = static_cast<long long>(H) * act_bytes(dtype);
+  if (row_bytes % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !inv_perm || !x_sorted) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_sorted) & 15u))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_gather_rows(x, T, static_cast<int>(row_bytes), K, inv_perm, x_sorted,
+                                        dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_quantize_gather_x_fp8(const void* x, int x_dtype, int T, int H, int K,
@@ -577,7 +639,15 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                       splits, status, s);
     if (rc != MOE_OK) return rc;
   } else {
-    rc = run_gemm1(p, x, w13, sorted_ids, block_info, num_blocks, h, status, s);
+    const void* a_rows = x;
+    if (bm == kPairBlockM) {  // CTA pairs: the gather as its own pass
+      void* xs = part(MOE_WS_XQ);
+      if (launch_gather_rows(x, p->T, static_cast<int>(p->H * act_bytes(p->act)), p->K,
+                             inv_perm, xs, status, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      a_rows = xs;
+    }
+    rc = run_gemm1(p, a_rows, w13, sorted_ids, block_info, num_blocks, h, status, s);
     if (rc != MOE_OK) return rc;
     rc = run_gemm2(p, h, w2, topk_weights, sorted_ids, block_info, num_blocks, y, splits, status,
                    s);
@@ -607,6 +677,12 @@ int moe_pack_mx_weights(const uint8_t* w, const uint8_t* w_scale, int E, int R, 
   if (!w || !w_scale || !w_packed || !scale_packed) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_pack_mx(w, w_scale, E, R, K, sections, w_packed, scale_packed,
                                     static_cast<cudaStream_t>(stream)));
+}
+
+int moe_device_info(int* sm_count_out, int* pair_clusters_out) {
+  if (sm_count_out) *sm_count_out = sm_count();
+  if (pair_clusters_out) *pair_clusters_out = pair_limit(0, MOE_BF16);
+  return MOE_OK;
 }
 
 int moe_get_device_status(const int32_t* dev_status, void* stream) {

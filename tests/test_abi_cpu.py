@@ -51,6 +51,7 @@ def test_problem_validation():
     assert _abi.moe_workspace_size(ok) > 0
     for bad in (make_problem(-1, 128, 256, 8, 2), make_problem(16, 0, 256, 8, 2),
                 make_problem(16, 128, 256, 0, 2), make_problem(16, 128, 256, 8, 2, block_m=48),
+                make_problem(16, 128, 256, 8, 2, block_m=512),
                 make_problem(16, 128, 256, 2048, 2)):
         assert _abi.moe_workspace_size(bad) == 0
         assert _abi.moe_resolve_block_m(bad) == -1
@@ -67,8 +68,11 @@ def test_workspace_layout_is_disjoint_and_aligned():
         assert a1 <= b0
     assert spans[-1][1] <= total
     assert all(o % 1024 == 0 for o in off)
-    cap = _abi.moe_align_capacity(4096, 2, 8, 128)
+    bm = _abi.moe_resolve_block_m(p)
+    assert bm == 256  # many tokens per expert: CTA-pair GEMMs
+    cap = _abi.moe_align_capacity(4096, 2, 8, bm)
     assert size[_abi.MOE_WS_SORTED_IDS] == 4 * cap
+    assert size[_abi.MOE_WS_BLOCK_INFO] == 16 * (cap // bm)
     assert size[_abi.MOE_WS_H] == 2 * cap * 14336
     splits = _abi.moe_gemm2_default_splits(p)
     assert size[_abi.MOE_WS_Y] == 4 * splits * cap * 4096
@@ -78,7 +82,7 @@ def test_entry_points_reject_bad_arguments_before_launch():
     L = _abi.lib()
     vp = ctypes.c_void_p
     fake = vp(1 << 20)  # never dereferenced: every call below fails its checks first
-    # block_m outside {16, 32, 64, 128}
+    # block_m outside {16, 32, 64, 128, 256}
     assert L.moe_align(fake, 4, 2, 8, 48, *([fake] * 7), None, None) == _abi.MOE_ERR_INVALID_ARG
     # E above the supported maximum
     assert L.moe_align(fake, 4, 2, 4096, 128, *([fake] * 7), None, None) == \

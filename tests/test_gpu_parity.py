@@ -33,7 +33,8 @@ def _status():
 # ------------------------------------------------------------------ align
 
 EXTRA_ALIGN = [(1, 8, 256, 128, "normal"), (3, 2, 1000, 16, "normal"),
-               (2000, 4, 1024, 64, "normal"), (4096, 2, 8, 128, "normal")]
+               (2000, 4, 1024, 64, "normal"), (4096, 2, 8, 128, "normal"),
+               (4096, 2, 8, 256, "normal"), (700, 3, 5, 256, "skewed")]
 
 
 @pytest.mark.parametrize("case", pins.ALIGN_CASES + EXTRA_ALIGN,
@@ -89,19 +90,26 @@ def _expert_of_rows(al, rows, ids_flat):
     return ids_flat[al["sorted_ids"][rows]].astype(np.int32)
 
 
+@pytest.mark.parametrize("bm", [128, 256], ids=["cta", "pair"])
 @pytest.mark.parametrize("case", STAGE_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s" % c)
-def test_gemm1_silu_stage(case):
+def test_gemm1_silu_stage(case, bm):
     T, H, I, E, K, dt = case
     cfg = gen.MoEConfig("stage", T, H, I, E, K, dt, "normal")
     inp = gen.generate(cfg, seed=21)
     d = inp.to("cuda")
-    al_ref = oracle.align(inp.topk_ids.numpy(), E, 128)
-    al = moe.align(d.topk_ids, E, 128)
-    p = moe.make_problem(T, H, I, E, K, dt)
-    cap = moe.moe_align_capacity(T, K, E, 128)
+    al_ref = oracle.align(inp.topk_ids.numpy(), E, bm)
+    al = moe.align(d.topk_ids, E, bm)
+    p = moe.make_problem(T, H, I, E, K, dt, block_m=bm)
+    cap = moe.moe_align_capacity(T, K, E, bm)
     h = torch.full((cap, I), float("nan"), dtype=d.x.dtype, device="cuda")
     st = _status()
-    moe.moe_gemm1_silu(p, d.x, None, d.w13, None, al["sorted_ids"], al["block_info"],
+    x_in = d.x
+    if bm == 256:  # CTA pairs read the token rows at their sorted slots
+        xs = np.zeros((cap, H), np.float32)
+        valid = al_ref["sorted_ids"] < T * K
+        xs[valid] = inp.x.float().numpy()[al_ref["sorted_ids"][valid] // K]
+        x_in = torch.from_numpy(xs).to(d.x.dtype).cuda()
+    moe.moe_gemm1_silu(p, x_in, None, d.w13, None, al["sorted_ids"], al["block_info"],
                        al["num_blocks"], h, st)
     assert moe.moe_get_device_status(st) == 0
     rows = _valid_rows(al_ref, T * K)
@@ -121,19 +129,20 @@ def test_gemm1_silu_stage(case):
         assert torch.isnan(h[torch.from_numpy(pad).long().cuda()].float()).all()
 
 
+@pytest.mark.parametrize("bm", [128, 256], ids=["cta", "pair"])
 @pytest.mark.parametrize("splits", [1, 2, 3])
 @pytest.mark.parametrize("case", STAGE_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s" % c)
-def test_gemm2_weighted_stage(case, splits):
+def test_gemm2_weighted_stage(case, splits, bm):
     T, H, I, E, K, dt = case
     cfg = gen.MoEConfig("stage", T, H, I, E, K, dt, "normal")
     inp = gen.generate(cfg, seed=22)
     d = inp.to("cuda")
-    cap = moe.moe_align_capacity(T, K, E, 128)
+    cap = moe.moe_align_capacity(T, K, E, bm)
     g = torch.Generator().manual_seed(5)
     hin = torch.randn((cap, I), generator=g).to(inp.x.dtype)  # synthetic hidden rows
-    al_ref = oracle.align(inp.topk_ids.numpy(), E, 128)
-    al = moe.align(d.topk_ids, E, 128)
-    p = moe.make_problem(T, H, I, E, K, dt)
+    al_ref = oracle.align(inp.topk_ids.numpy(), E, bm)
+    al = moe.align(d.topk_ids, E, bm)
+    p = moe.make_problem(T, H, I, E, K, dt, block_m=bm)
     y = torch.full((splits, cap, H), float("nan"), dtype=torch.float32, device="cuda")
     st = _status()
     moe.moe_gemm2_weighted(p, hin.cuda(), d.w2, None, d.topk_weights, al["sorted_ids"],
@@ -180,8 +189,8 @@ FORWARD_CASES = [
 ]
 
 
-def _run_forward(d, cfg, poison=True):
-    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype)
+def _run_forward(d, cfg, poison=True, block_m=0):
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype, block_m=block_m)
     ws = moe.Workspace(p)
     if poison:
         ws.buffer.fill_(0xFF)  # NaN patterns everywhere the path does not write
@@ -192,13 +201,21 @@ def _run_forward(d, cfg, poison=True):
     return out, ws
 
 
+@pytest.mark.parametrize("bm", [0, 256], ids=["auto", "pair"])
 @pytest.mark.parametrize("case", FORWARD_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s_%s" % c)
-def test_forward_small(case):
+def test_forward_small(case, bm):
     cfg = gen.MoEConfig("fwd", *case)
     inp = gen.generate(cfg, seed=31)
-    out, ws = _run_forward(inp.to("cuda"), cfg)
+    out, ws = _run_forward(inp.to("cuda"), cfg, block_m=bm)
     ref = oracle_forward_tokens(inp, np.arange(cfg.T))
     assert_close(out, ref, what=cfg.name)
+
+
+def test_block_m_auto_picks_pairs_for_many_tokens_per_expert():
+    assert moe.moe_resolve_block_m(moe.make_problem(4096, 4096, 14336, 8, 2, "bf16")) == 256
+    assert moe.moe_resolve_block_m(moe.make_problem(8192, 7168, 2048, 256, 8, "bf16")) == 128
+    assert moe.moe_resolve_block_m(moe.make_problem(2048, 2880, 2880, 128, 4, "bf16",
+                                                    "mxfp4")) == 128
 
 
 def test_forward_tiny_config():
@@ -209,14 +226,15 @@ def test_forward_tiny_config():
     assert_close(out, ref, what="tiny")
 
 
-def test_forward_deterministic_and_padding_untouched():
+@pytest.mark.parametrize("bm", [128, 256], ids=["cta", "pair"])
+def test_forward_deterministic_and_padding_untouched(bm):
     cfg = gen.MoEConfig("fwd", 300, 256, 320, 3, 2, "bf16", "normal")
     d = gen.generate(cfg, seed=32).to("cuda")
-    out1, ws = _run_forward(d, cfg)
-    out2, _ = _run_forward(d, cfg)
+    out1, ws = _run_forward(d, cfg, block_m=bm)
+    out2, _ = _run_forward(d, cfg, block_m=bm)
     assert torch.equal(out1, out2)
     h = ws.part(_abi.MOE_WS_H, torch.uint8)
-    cap = moe.moe_align_capacity(cfg.T, cfg.K, cfg.E, 128)
+    cap = moe.moe_align_capacity(cfg.T, cfg.K, cfg.E, bm)
     h = h[:cap * cfg.I * 2].view(cap, cfg.I * 2)
     s = ws.part(_abi.MOE_WS_SORTED_IDS, torch.int32)[:cap].cpu().numpy()
     pad = np.nonzero(s >= cfg.T * cfg.K)[0]
@@ -311,6 +329,26 @@ def _mx_problem(case, seed):
     T, H, I, E, K = case
     cfg = gen.MoEConfig("mx", T, H, I, E, K, "mxfp4", "uniform")
     return cfg, gen.generate(cfg, seed=seed)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_gather_rows_bit_exact(dtype):
+    """Every sorted slot of a token holds that token's row, bit for bit;
+    padding slots are left alone."""
+    T, H, K, E = 300, 264, 2, 3
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn((T, H), generator=g).to(dtype)
+    ids = pins.align_ids(T, K, E, "normal", seed=5)
+    al = oracle.align(ids, E, 256)
+    cap = len(al["sorted_ids"])
+    xs = torch.zeros((cap, H), dtype=dtype, device="cuda")
+    moe.moe_gather_rows(x.cuda(), moe.dtype_code(dtype), T, H, K,
+                        torch.from_numpy(al["inv_perm"]).cuda(), xs)
+    torch.cuda.synchronize()
+    valid = al["sorted_ids"] < T * K
+    got = xs.cpu()
+    assert torch.equal(got[torch.from_numpy(valid)], x[al["sorted_ids"][valid] // K])
+    assert (got[torch.from_numpy(~valid)] == 0).all()
 
 
 @pytest.mark.parametrize("T,H,K,E", [(2048, 2880, 4, 128), (37, 64, 2, 5)])
