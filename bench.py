@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--config", default="mixtral_prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--block-m", type=int, default=0,
+                    help="align block (token tile) of the GEMMs; 0 picks it from the problem")
     return ap.parse_args()
 
 
@@ -298,7 +300,7 @@ def run_ours(args, ws, rank, local):
         inp.topk_ids, inp.topk_weights = gen.route(gen.router_logits(cfg, seed, dev), cfg.K)
     mx = cfg.dtype == "mxfp4"
     p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "bf16" if mx else cfg.dtype,
-                         "mxfp4" if mx else None)
+                         "mxfp4" if mx else None, block_m=args.block_m)
     wsp = moe.Workspace(p, dev)
     part = lambda i, dt=torch.int32: wsp.part(i, dt)
     st = wsp.status

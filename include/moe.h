@@ -65,8 +65,8 @@ typedef enum {
  *            be MOE_BF16; x is cast to e4m3 with one fp32 scale per row and
  *            the hidden activation is stored as e4m3(a / h_scale)).
  *   block_m: rows per alignment block, 0 = automatic: 256 (the GEMMs then
- *            run on CTA pairs) when bf16/fp32 experts receive at least 768
- *            rows on average, else 128.
+ *            run on CTA pairs) when bf16/fp32 experts receive at least 256
+ *            rows on average (T*K >= 256*E), else 128.
  *   h_scale: scale of the e4m3 hidden activation (MX weights only; 0 => 1). */
 typedef struct {
     int T, H, I, E, K;

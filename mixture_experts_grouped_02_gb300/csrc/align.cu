@@ -30,6 +30,19 @@ namespace {
 
 constexpr int kAlignWarps = 32;
 constexpr int kAlignThreads = kAlignWarps * 32;
+// Batches of 32 ids a warp loads at once before it works through them in
+// order: keeps several loads in flight instead of one round trip per batch.
+constexpr int kAlignUnroll = 8;
+
+// ids [base + 32u + lane] for u < kAlignUnroll, -1 at or past `hi`.
+__device__ __forceinline__ void load_ids(const int* ids, int base, int hi, int lane,
+                                         int (&e)[kAlignUnroll]) {
+#pragma unroll
+  for (int u = 0; u < kAlignUnroll; ++u) {
+    const int i = base + 32 * u + lane;
+    e[u] = i < hi ? __ldg(ids + i) : -1;
+  }
+}
 
 // Block-wide exclusive scan of two int values per thread (1024 threads).
 __device__ __forceinline__ void block_exclusive_scan2(int& a, int& b, int* s_tmp) {
@@ -95,19 +108,20 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
   int* my_hist = hist + warp * E;
 
   // 1. histogram
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    int e = -1;
-    if (i < hi) {
-      e = p.ids[i];
-      if (e < 0 || e >= E) {
+  for (int base0 = lo; base0 < hi; base0 += 32 * kAlignUnroll) {
+    int ev[kAlignUnroll];
+    load_ids(p.ids, base0, hi, lane, ev);
+#pragma unroll
+    for (int u = 0; u < kAlignUnroll; ++u) {
+      int e = ev[u];
+      if (base0 + 32 * u + lane < hi && (e < 0 || e >= E)) {
         s_bad = 1;
         e = -1;
       }
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) my_hist[e] += __popc(peers);
+      __syncwarp();
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) my_hist[e] += __popc(peers);
-    __syncwarp();
   }
   __syncthreads();
   if (s_bad) {
@@ -163,19 +177,24 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
   __syncthreads();
 
   // 3. stable scatter
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    const int e = i < hi ? p.ids[i] : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0) {
-      const unsigned lower = peers & ((1u << lane) - 1u);
-      const int slot = s_pad[e] + my_hist[e] + __popc(lower);
-      p.sorted_ids[slot] = i;
-      p.inv_perm[i] = slot;
+  for (int base0 = lo; base0 < hi; base0 += 32 * kAlignUnroll) {
+    int ev[kAlignUnroll];
+    load_ids(p.ids, base0, hi, lane, ev);
+#pragma unroll
+    for (int u = 0; u < kAlignUnroll; ++u) {
+      const int i = base0 + 32 * u + lane;
+      const int e = ev[u];
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0) {
+        const unsigned lower = peers & ((1u << lane) - 1u);
+        const int slot = s_pad[e] + my_hist[e] + __popc(lower);
+        p.sorted_ids[slot] = i;
+        p.inv_perm[i] = slot;
+      }
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) my_hist[e] += __popc(peers);
+      __syncwarp();
     }
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(peers) - 1) my_hist[e] += __popc(peers);
-    __syncwarp();
   }
 
   // 4a. padding slots of each expert, and the tail [padded_offsets[E], cap)

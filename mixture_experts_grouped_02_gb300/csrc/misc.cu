@@ -15,6 +15,8 @@ namespace {
 // so no atomics and a fixed summation order.  CTA (x, y) handles token rows
 // x, x + gridDim.x, ... and the y-th run of 1024 columns of them, so that a
 // handful of tokens still spreads over many SMs; 16-byte loads of y.
+constexpr int kCombineBatch = 8;
+
 template <typename OutT>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int splits,
                                                       long long cap,
@@ -28,16 +30,34 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     const int32_t* slots = inv_perm + static_cast<long long>(t) * K;
     for (int c = blockIdx.y * 256 + threadIdx.x; c < c_end; c += blockDim.x) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k = 0; k < K; ++k) {
-        const long long row = slots[k];
-        for (int q = 0; q < splits; ++q) {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(
-                                     y + (static_cast<long long>(q) * cap + row) * H) +
-                                 c);
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
+      if (splits == 1 && K <= kCombineBatch) {
+        // all K loads in flight at once, then the sum in k order
+        float4 v[kCombineBatch];
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k)
+          if (k < K)
+            v[k] = __ldg(reinterpret_cast<const float4*>(y + static_cast<long long>(slots[k]) * H) +
+                         c);
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k)
+          if (k < K) {
+            acc.x += v[k].x;
+            acc.y += v[k].y;
+            acc.z += v[k].z;
+            acc.w += v[k].w;
+          }
+      } else {
+        for (int k = 0; k < K; ++k) {
+          const long long row = slots[k];
+          for (int q = 0; q < splits; ++q) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(
+                                       y + (static_cast<long long>(q) * cap + row) * H) +
+                                   c);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+          }
         }
       }
       if constexpr (sizeof(OutT) == 2) {

@@ -59,6 +59,16 @@ def test_problem_validation():
     assert _abi.moe_workspace_size(bad_pair) == 0
 
 
+def test_block_m_auto_rule():
+    # 256-row blocks (CTA pairs) once experts average 256 rows, mx weights 128
+    assert _abi.moe_resolve_block_m(make_problem(4096, 4096, 14336, 8, 2, "bf16")) == 256
+    assert _abi.moe_resolve_block_m(make_problem(8192, 7168, 2048, 256, 8, "bf16")) == 256
+    assert _abi.moe_resolve_block_m(make_problem(8191, 7168, 2048, 256, 8, "bf16")) == 128
+    assert _abi.moe_resolve_block_m(make_problem(128, 4096, 14336, 8, 2, "bf16")) == 128
+    assert _abi.moe_resolve_block_m(make_problem(2048, 2880, 2880, 128, 4, "bf16", "mxfp4")) == 128
+    assert _abi.moe_resolve_block_m(make_problem(16, 128, 256, 8, 2, "f32", block_m=64)) == 64
+
+
 def test_workspace_layout_is_disjoint_and_aligned():
     p = make_problem(4096, 4096, 14336, 8, 2, "bf16")
     off, size = _abi.moe_workspace_offsets(p)

@@ -213,7 +213,9 @@ def test_forward_small(case, bm):
 
 def test_block_m_auto_picks_pairs_for_many_tokens_per_expert():
     assert moe.moe_resolve_block_m(moe.make_problem(4096, 4096, 14336, 8, 2, "bf16")) == 256
-    assert moe.moe_resolve_block_m(moe.make_problem(8192, 7168, 2048, 256, 8, "bf16")) == 128
+    assert moe.moe_resolve_block_m(moe.make_problem(8192, 7168, 2048, 256, 8, "bf16")) == 256
+    assert moe.moe_resolve_block_m(moe.make_problem(8191, 7168, 2048, 256, 8, "bf16")) == 128
+    assert moe.moe_resolve_block_m(moe.make_problem(128, 4096, 14336, 8, 2, "bf16")) == 128
     assert moe.moe_resolve_block_m(moe.make_problem(2048, 2880, 2880, 128, 4, "bf16",
                                                     "mxfp4")) == 128
 
