@@ -45,6 +45,14 @@ class Problem(ctypes.Structure):
         ("quantize_x", ctypes.c_int),
         ("h_e4m3", ctypes.c_int),
         ("h_scale", ctypes.c_double),
+        ("expert_base", ctypes.c_int),
+        ("local_experts", ctypes.c_int),
+        ("activation", ctypes.c_int),
+        ("swiglu_alpha", ctypes.c_double),
+        ("swiglu_limit", ctypes.c_double),
+        ("gate_up_interleaved", ctypes.c_int),
+        ("w13_bias", ctypes.c_void_p),
+        ("w2_bias", ctypes.c_void_p),
     ]
 
 
@@ -79,6 +87,9 @@ def _declare(L):
     ci = ctypes.c_int
     L.orc_align.restype = ci
     L.orc_align.argtypes = [i32p, ci, ci, ci, ci, i32p, i32p, i32p, i32p, i32p, i32p, i32p]
+    L.orc_align_local.restype = ci
+    L.orc_align_local.argtypes = [i32p, ci, ci, ci, ci, ci, ci, i32p, i32p, i32p, i32p, i32p, i32p,
+                                  i32p]
     L.orc_align_capacity.restype = ctypes.c_long
     L.orc_align_capacity.argtypes = [ci, ci, ci, ci]
     L.orc_moe_forward.restype = ci
@@ -133,30 +144,50 @@ def _dtype_code(a):
     raise TypeError(f"unsupported storage dtype {a.dtype}")
 
 
-def make_problem(T, H, I, E, K, x, w13, quantize_x=False, h_e4m3=False, h_scale=1.0):
-    return Problem(T, H, I, E, K, _dtype_code(x), _dtype_code(w13), int(quantize_x), int(h_e4m3),
-                   float(h_scale))
+ACT_SILU, ACT_SWIGLU_CLAMP = 0, 1
+
+
+def make_problem(T, H, I, E, K, x, w13, quantize_x=False, h_e4m3=False, h_scale=1.0,
+                 expert_base=0, local_experts=0, activation=ACT_SILU, swiglu_alpha=1.0,
+                 swiglu_limit=float("inf"), gate_up_interleaved=False, w13_bias=None,
+                 w2_bias=None):
+    """local_experts > 0: an expert-parallel shard holding experts
+    [expert_base, expert_base + local_experts); the weights passed with it
+    hold those experts only.  activation ACT_SWIGLU_CLAMP: the clamped
+    SwiGLU with swiglu_alpha / swiglu_limit; gate_up_interleaved: w13 rows
+    2j (gate) and 2j+1 (up); w13_bias (experts, 2I) in w13's row order and
+    w2_bias (experts, H), fp32, optional."""
+    b13 = _c(w13_bias, np.float32)
+    b2 = _c(w2_bias, np.float32)
+    P = Problem(T, H, I, E, K, _dtype_code(x), _dtype_code(w13), int(quantize_x), int(h_e4m3),
+                float(h_scale), int(expert_base), int(local_experts), int(activation),
+                float(swiglu_alpha), float(swiglu_limit), int(gate_up_interleaved),
+                None if b13 is None else b13.ctypes.data, None if b2 is None else b2.ctypes.data)
+    P._keep = (b13, b2)  # the arrays the pointers refer to live as long as P
+    return P
 
 
 def align_capacity(T, K, E, bm):
     return int(lib().orc_align_capacity(T, K, E, bm))
 
 
-def align(ids, E, bm):
-    """Align (T, K) top-k ids into per-expert, bm-padded sorted lists."""
+def align(ids, E, bm, expert_base=0, local_experts=0):
+    """Align (T, K) top-k ids into per-expert, bm-padded sorted lists (of the
+    shard's experts when local_experts > 0)."""
     ids = _c(ids, np.int32)
     T, K = ids.shape
-    cap = align_capacity(T, K, E, bm)
+    L = local_experts if local_experts > 0 else E
+    cap = align_capacity(T, K, L, bm)
     out = dict(
-        counts=np.zeros(E, np.int32),
-        offsets=np.zeros(E + 1, np.int32),
-        padded_offsets=np.zeros(E + 1, np.int32),
+        counts=np.zeros(L, np.int32),
+        offsets=np.zeros(L + 1, np.int32),
+        padded_offsets=np.zeros(L + 1, np.int32),
         sorted_ids=np.zeros(cap, np.int32),
         inv_perm=np.zeros(T * K, np.int32),
         block_info=np.zeros((cap // bm, 4), np.int32),
         num_blocks=np.zeros(1, np.int32),
     )
-    rc = lib().orc_align(_ptr(ids, ctypes.c_int32), T, K, E, bm,
+    rc = lib().orc_align_local(_ptr(ids, ctypes.c_int32), T, K, E, expert_base, L, bm,
                          *[_ptr(out[k], ctypes.c_int32) for k in
                            ("counts", "offsets", "padded_offsets", "sorted_ids", "inv_perm",
                             "block_info", "num_blocks")])

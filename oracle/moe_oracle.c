@@ -36,6 +36,9 @@
 #define ORC_MXFP4 3 /* OCP MX: e2m1 pairs packed low-nibble-first, one */
                     /* e8m0 scale per 32 consecutive K elements         */
 
+#define ORC_ACT_SILU 0          /* a = SiLU(g) * u                        */
+#define ORC_ACT_SWIGLU_CLAMP 1  /* [P2]'s GPT-OSS SwiGLU (clamped, alpha)   */
+
 #define ORC_EXACT 0   /* no intermediate rounding                        */
 #define ORC_EMULATE 1 /* round the activation a_j to its storage type    */
 
@@ -46,7 +49,20 @@ typedef struct {
     int quantize_x;  /* 1: x goes through the per-row e4m3 step first     */
     int h_e4m3;      /* 1: h is stored as e4m3(a / h_scale) (EMULATE)     */
     double h_scale;  /* scale of the e4m3 h (1.0 when unused)             */
+    int expert_base;   /* expert-parallel shard: first expert held here     */
+    int local_experts; /* experts held (weights hold these only); 0 = all E */
+    int activation;           /* ORC_ACT_SILU or ORC_ACT_SWIGLU_CLAMP        */
+    double swiglu_alpha;      /* sigmoid slope of ORC_ACT_SWIGLU_CLAMP       */
+    double swiglu_limit;      /* clamp of ORC_ACT_SWIGLU_CLAMP               */
+    int gate_up_interleaved;  /* w13 rows 2j = gate j, 2j+1 = up j           */
+    const float* w13_bias;    /* (experts held, 2I) in w13's row order, or 0 */
+    const float* w2_bias;     /* (experts held, H), or 0                     */
 } orc_problem;
+
+/* Experts of the shard (all E when local_experts is 0). */
+static int shard_size(const orc_problem* p) {
+    return p->local_experts > 0 ? p->local_experts : p->E;
+}
 
 /* ------------------------------------------------------------------ */
 /* Number formats, decoded from their definitions                      */
@@ -213,26 +229,51 @@ static double store_hidden(const orc_problem* p, int mode, double a) {
 /* One expert FFN on one token row                                     */
 /* ------------------------------------------------------------------ */
 
-/* a_j = SiLU(W13[e, j, :] . xrow) * (W13[e, I + j, :] . xrow), j < I.
- * Gate is the first half of w13's rows, up the second ([P3]
- * fused_silu_gate_kernel; "gate_up.chunk(2)" in the PyTorch path). */
+/* Rows of gate j and up j in w13.  [P3] (fused_silu_gate_kernel,
+ * "gate_up.chunk(2)" in the PyTorch path) puts gate in the first half of the
+ * rows and up in the second; [P2]'s GPT-OSS layout interleaves them (its
+ * epilogue unpacks adjacent (gate, linear) column pairs). */
+static int gate_row(const orc_problem* p, int j) { return p->gate_up_interleaved ? 2 * j : j; }
+static int up_row(const orc_problem* p, int j) {
+    return p->gate_up_interleaved ? 2 * j + 1 : p->I + j;
+}
+
+/* [P2] _swiglu_step1 / _swiglu_step2: the gate is clamped from above at
+ * `limit`, the linear branch to [-limit, limit], and
+ * out = gate * sigmoid(alpha * gate) * (linear + 1). */
+static double swiglu_clamped(const orc_problem* p, double g, double u) {
+    g = fmin(g, p->swiglu_limit);
+    u = fmax(fmin(u, p->swiglu_limit), -p->swiglu_limit);
+    return g / (1.0 + exp(-p->swiglu_alpha * g)) * (u + 1.0);
+}
+
+/* a_j = act(W13[e, gate_row(j), :] . xrow + b13[gate_row(j)],
+ *           W13[e, up_row(j), :] . xrow + b13[up_row(j)]), j < I,
+ * act(g, u) = SiLU(g) * u ([P3]) or the clamped SwiGLU above ([P2]); the
+ * bias (per expert and w13 row, [P2] apply_bias_and_scale) is added to the
+ * accumulator before the activation. */
 static void expert_hidden(const orc_problem* p, const void* w13, const uint8_t* w13_scale, int e,
                           const double* xrow, double* a, double* wrow) {
+    const float* b13 = p->w13_bias ? p->w13_bias + (size_t)e * 2 * p->I : NULL;
     for (int j = 0; j < p->I; ++j) {
-        load_weight_row(w13, w13_scale, p->w_dtype, 2 * p->I, p->H, e, j, wrow);
-        double g = dot(wrow, xrow, p->H);
-        load_weight_row(w13, w13_scale, p->w_dtype, 2 * p->I, p->H, e, p->I + j, wrow);
-        double u = dot(wrow, xrow, p->H);
-        a[j] = silu(g) * u;
+        load_weight_row(w13, w13_scale, p->w_dtype, 2 * p->I, p->H, e, gate_row(p, j), wrow);
+        double g = dot(wrow, xrow, p->H) + (b13 ? (double)b13[gate_row(p, j)] : 0.0);
+        load_weight_row(w13, w13_scale, p->w_dtype, 2 * p->I, p->H, e, up_row(p, j), wrow);
+        double u = dot(wrow, xrow, p->H) + (b13 ? (double)b13[up_row(p, j)] : 0.0);
+        if (p->activation == ORC_ACT_SWIGLU_CLAMP)
+            a[j] = swiglu_clamped(p, g, u);
+        else
+            a[j] = silu(g) * u;
     }
 }
 
-/* y_c = W2[e, c, :] . a, c < H. */
+/* y_c = W2[e, c, :] . a + b2[e, c], c < H (the bias, when given, belongs to
+ * the expert's second projection, before the routing weight). */
 static void expert_out(const orc_problem* p, const void* w2, const uint8_t* w2_scale, int e,
                        const double* a, double* y, double* wrow) {
     for (int c = 0; c < p->H; ++c) {
         load_weight_row(w2, w2_scale, p->w_dtype, p->H, p->I, e, c, wrow);
-        y[c] = dot(wrow, a, p->I);
+        y[c] = dot(wrow, a, p->I) + (p->w2_bias ? (double)p->w2_bias[(size_t)e * p->H + c] : 0.0);
     }
 }
 
@@ -247,6 +288,12 @@ static int max_int(int a, int b) { return a > b ? a : b; }
  *   e = ids[t,k], accumulated in k order, fp64.
  * This is the "Current PyTorch path" of [P3] written per token; the routing
  * weight multiplies the down-projection output ([P1] MUL_ROUTED_WEIGHT).
+ * Expert-parallel shard ([P2] init_routing_data: a shard keeps the
+ * histogram of its local experts only, make_expt_dict_uniform gives each
+ * shard a contiguous range): slots routed to an expert outside
+ * [expert_base, expert_base + local_experts) contribute nothing, and the
+ * weights are indexed by e - expert_base.  The shards' outputs sum to the
+ * unsharded output.
  * Returns 0, or -1 when an expert id is outside [0, E). */
 int orc_moe_forward(const orc_problem* p, int mode, const void* x, const int32_t* ids,
                     const float* topk_w, const void* w13, const uint8_t* w13_scale, const void* w2,
@@ -269,6 +316,8 @@ int orc_moe_forward(const orc_problem* p, int mode, const void* x, const int32_t
                 bad = 1;
                 continue;
             }
+            if (e < p->expert_base || e >= p->expert_base + shard_size(p)) continue;
+            e -= p->expert_base; /* index into this shard's weights */
             double w = (double)topk_w[(size_t)t * p->K + k];
             expert_hidden(p, w13, w13_scale, e, xrow, a, wrow);
             for (int j = 0; j < p->I; ++j) a[j] = store_hidden(p, mode, a[j]);
@@ -298,14 +347,15 @@ int orc_moe_forward_by_expert(const orc_problem* p, int mode, const void* x, con
     double* wrow = (double*)malloc(sizeof(double) * max_int(p->H, p->I));
     double* a = (double*)malloc(sizeof(double) * p->I);
     double* y = (double*)malloc(sizeof(double) * p->H);
-    for (int e = 0; e < p->E; ++e) {
+    for (int e = p->expert_base; e < p->expert_base + shard_size(p); ++e) {
+        int el = e - p->expert_base;
         for (size_t i = 0; i < na; ++i) {
             if (ids[i] != e) continue;
             int t = (int)(i / (size_t)p->K);
             load_token_row(p, x, t, xrow);
-            expert_hidden(p, w13, w13_scale, e, xrow, a, wrow);
+            expert_hidden(p, w13, w13_scale, el, xrow, a, wrow);
             for (int j = 0; j < p->I; ++j) a[j] = store_hidden(p, mode, a[j]);
-            expert_out(p, w2, w2_scale, e, a, y, wrow);
+            expert_out(p, w2, w2_scale, el, a, y, wrow);
             for (int c = 0; c < p->H; ++c) out[(size_t)t * p->H + c] += (double)topk_w[i] * y[c];
         }
     }
@@ -373,12 +423,16 @@ void orc_gemm2_weighted_rows(const orc_problem* p, const void* hin, int h_dtype,
 }
 
 /* Combine: out[t, :] = sum_{k} y[inv_perm[t*K + k], :] summed in k order
- * (the index_add of [P3]'s PyTorch path, in a fixed order). */
+ * (the index_add of [P3]'s PyTorch path, in a fixed order).  A negative
+ * slot (an assignment to another shard's expert) contributes nothing. */
 void orc_combine(const float* y, const int32_t* inv_perm, int T, int K, int H, double* out) {
     for (int t = 0; t < T; ++t)
         for (int c = 0; c < H; ++c) {
             double s = 0.0;
-            for (int k = 0; k < K; ++k) s += (double)y[(size_t)inv_perm[(size_t)t * K + k] * H + c];
+            for (int k = 0; k < K; ++k) {
+                int slot = inv_perm[(size_t)t * K + k];
+                if (slot >= 0) s += (double)y[(size_t)slot * H + c];
+            }
             out[(size_t)t * H + c] = s;
         }
 }
@@ -407,34 +461,43 @@ long orc_align_capacity(int T, int K, int E, int bm) {
  *   block_info[b]      = (expert, m-index, first slot, valid rows) for the
  *                        num_blocks = po[E]/bm blocks in expert order ([P1]
  *                        mblocks_to_tuple_info); (-1, 0, 0, 0) past them.
+ * Expert-parallel shard of L experts from `base` ([P2] init_routing_data
+ * keeps the local experts' histogram): every per-expert array above runs
+ * over the local experts e - base, ids of other experts are left out of
+ * the lists and get inv_perm[i] = -1, and the capacity counts min(L, T*K)
+ * active experts.  base = 0, L = E is the plain align.
  * The sorted order is built by scanning i in ascending order once per expert.
  * Returns 0, or -1 when an id is outside [0, E). */
-int orc_align(const int32_t* ids, int T, int K, int E, int bm, int32_t* counts, int32_t* offsets,
-              int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm, int32_t* block_info,
-              int32_t* num_blocks) {
+int orc_align_local(const int32_t* ids, int T, int K, int E, int base, int L, int bm,
+                    int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                    int32_t* sorted_ids, int32_t* inv_perm, int32_t* block_info,
+                    int32_t* num_blocks) {
     long na = (long)T * K;
-    long cap = orc_align_capacity(T, K, E, bm);
+    long cap = orc_align_capacity(T, K, L, bm);
     for (long i = 0; i < na; ++i)
         if (ids[i] < 0 || ids[i] >= E) return -1;
-    for (int e = 0; e < E; ++e) counts[e] = 0;
-    for (long i = 0; i < na; ++i) counts[ids[i]] += 1;
+    for (int e = 0; e < L; ++e) counts[e] = 0;
+    for (long i = 0; i < na; ++i) {
+        inv_perm[i] = -1;
+        if (ids[i] >= base && ids[i] < base + L) counts[ids[i] - base] += 1;
+    }
     offsets[0] = 0;
     padded_offsets[0] = 0;
-    for (int e = 0; e < E; ++e) {
+    for (int e = 0; e < L; ++e) {
         offsets[e + 1] = offsets[e] + counts[e];
         padded_offsets[e + 1] = padded_offsets[e] + (counts[e] + bm - 1) / bm * bm;
     }
     for (long s = 0; s < cap; ++s) sorted_ids[s] = (int32_t)na;
-    for (int e = 0; e < E; ++e) {
+    for (int e = base; e < base + L; ++e) {
         int r = 0;
         for (long i = 0; i < na; ++i) {
             if (ids[i] != e) continue;
-            sorted_ids[padded_offsets[e] + r] = (int32_t)i;
-            inv_perm[i] = padded_offsets[e] + r;
+            sorted_ids[padded_offsets[e - base] + r] = (int32_t)i;
+            inv_perm[i] = padded_offsets[e - base] + r;
             ++r;
         }
     }
-    int nb = padded_offsets[E] / bm;
+    int nb = padded_offsets[L] / bm;
     *num_blocks = nb;
     long max_blocks = cap / bm;
     for (long b = 0; b < max_blocks; ++b) {
@@ -445,7 +508,7 @@ int orc_align(const int32_t* ids, int T, int K, int E, int bm, int32_t* counts, 
         bi[3] = 0;
     }
     int b = 0;
-    for (int e = 0; e < E; ++e) {
+    for (int e = 0; e < L; ++e) {
         int nblk = (padded_offsets[e + 1] - padded_offsets[e]) / bm;
         for (int m = 0; m < nblk; ++m, ++b) {
             int32_t* bi = block_info + 4 * (long)b;
@@ -457,4 +520,12 @@ int orc_align(const int32_t* ids, int T, int K, int E, int bm, int32_t* counts, 
         }
     }
     return 0;
+}
+
+/* The plain align: one shard holding all E experts. */
+int orc_align(const int32_t* ids, int T, int K, int E, int bm, int32_t* counts, int32_t* offsets,
+              int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm, int32_t* block_info,
+              int32_t* num_blocks) {
+    return orc_align_local(ids, T, K, E, 0, E, bm, counts, offsets, padded_offsets, sorted_ids,
+                           inv_perm, block_info, num_blocks);
 }

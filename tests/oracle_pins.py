@@ -442,6 +442,188 @@ def pin_lowp_forward_loop_orders():
     assert 1e-4 < rel < 0.1, rel
 
 
+# ---------------------------------------------------------------- shard pins
+
+SHARDS = [(0, 3), (3, 3), (6, 2)]  # an uneven partition of E = 8 experts
+
+
+def _shard_forward(inp, base, L, **kw):
+    c = inp.cfg
+    P = oracle.make_problem(c.T, c.H, c.I, c.E, c.K, np_store(inp.x), np_store(inp.w13),
+                            expert_base=base, local_experts=L, **kw)
+    sl = slice(base, base + L)
+    return oracle.forward(P, np_store(inp.x), inp.topk_ids.numpy(), inp.topk_weights.numpy(),
+                          np_store(inp.w13[sl]), np_store(inp.w2[sl]))
+
+
+def pin_shards_sum_to_full():
+    """Expert shards partition the experts => their outputs add up to the
+    unsharded output; a token none of whose experts a shard holds gets 0."""
+    inp = rand_problem(40, 64, 32, 8, 2, "bf16", seed=12)
+    full = run_forward(inp)
+    parts = [_shard_forward(inp, b, L) for b, L in SHARDS]
+    assert np.allclose(sum(parts), full, rtol=1e-12, atol=1e-13)
+    ids = inp.topk_ids.numpy()
+    for (b, L), part in zip(SHARDS, parts):
+        none_local = ~((ids >= b) & (ids < b + L)).any(1)
+        assert none_local.any()
+        assert np.all(part[none_local] == 0.0)
+    # a shard holding every expert is the plain forward, bit for bit
+    assert np.array_equal(_shard_forward(inp, 0, 8), full)
+
+
+def pin_shard_vs_torch():
+    """One shard: out[t] = sum over the slots routed into the shard of
+    w * FFN_e(x_t) (torch, fp64), with the shard's weights indexed from 0."""
+    inp = rand_problem(12, 32, 48, 8, 3, "f32", seed=13)
+    base, L = 2, 4
+    out = _shard_forward(inp, base, L)
+    x = inp.x.to(torch.float64)
+    for t in range(inp.cfg.T):
+        ref = torch.zeros(inp.cfg.H, dtype=torch.float64)
+        for k in range(3):
+            e = int(inp.topk_ids[t, k])
+            if base <= e < base + L:
+                ref += float(inp.topk_weights[t, k]) * dense_swiglu(
+                    x[t:t + 1], inp.w13[e].to(torch.float64), inp.w2[e].to(torch.float64))[0]
+        assert np.allclose(out[t], ref.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def pin_align_local_vs_stable_argsort():
+    """A shard's align: numpy's stable sort of the assignments routed into
+    the shard, keyed by local expert; inv_perm = -1 for the others."""
+    for (T, K, E, bm, kind), (base, L) in (((37, 3, 8, 32, "normal"), (3, 4)),
+                                            ((300, 4, 16, 64, "skewed"), (0, 5)),
+                                            ((100, 8, 256, 128, "normal"), (200, 56))):
+        ids = align_ids(T, K, E, kind, seed=3)
+        a = oracle.align(ids, E, bm, expert_base=base, local_experts=L)
+        flat = ids.ravel()
+        na = flat.size
+        local = (flat >= base) & (flat < base + L)
+        counts = np.bincount(flat[local] - base, minlength=L)
+        assert np.array_equal(a["counts"], counts)
+        padded = -(-counts // bm) * bm
+        po = np.concatenate([[0], np.cumsum(padded)])
+        assert np.array_equal(a["padded_offsets"], po)
+        assert np.array_equal(a["offsets"], np.concatenate([[0], np.cumsum(counts)]))
+        cap = oracle.align_capacity(T, K, L, bm)
+        assert len(a["sorted_ids"]) == cap
+        idx = np.nonzero(local)[0]
+        order = idx[np.argsort(flat[idx], kind="stable")]
+        expect = np.full(cap, na, np.int32)
+        pos = 0
+        for e in range(L):
+            seg = order[pos:pos + counts[e]]
+            pos += counts[e]
+            expect[po[e]:po[e] + len(seg)] = seg
+        assert np.array_equal(a["sorted_ids"], expect)
+        inv = np.full(na, -1, np.int64)
+        valid = expect < na
+        inv[expect[valid]] = np.nonzero(valid)[0]
+        assert np.array_equal(a["inv_perm"], inv)
+        nb = int(po[-1] // bm)
+        assert a["num_blocks"] == nb
+        assert np.array_equal(a["block_info"][:nb, 0], np.repeat(np.arange(L), padded // bm))
+
+
+# ------------------------------------------------ clamped SwiGLU (GPT-OSS) pins
+
+def _one_hot_problem(g, u, alpha, limit, w2_identity=True):
+    """T = K = E = 1, x = e_0, gate/up rows with g_j / u_j in column 0 and
+    W2 = identity (H = I), weight 1: out = a exactly as the activation
+    gives it."""
+    I = len(g)
+    H = I
+    x = np.zeros((1, H), np.float32)
+    x[0, 0] = 1.0
+    w13 = np.zeros((1, 2 * I, H), np.float32)
+    w13[0, :I, 0] = g
+    w13[0, I:, 0] = u
+    w2 = np.eye(H, dtype=np.float32)[None] if w2_identity else np.zeros((1, H, I), np.float32)
+    P = oracle.make_problem(1, H, I, 1, 1, x, w13, activation=oracle.ACT_SWIGLU_CLAMP,
+                            swiglu_alpha=alpha, swiglu_limit=limit)
+    out = oracle.forward(P, x, np.zeros((1, 1), np.int32), np.ones((1, 1), np.float32), w13, w2)
+    return out[0], w13[0, :I, 0].astype(np.float64), w13[0, I:, 0].astype(np.float64)
+
+
+def pin_swiglu_clamp_closed_forms():
+    """With alpha = 2 and limit = ln(3)/2, sigmoid(alpha * limit) = 3/4
+    exactly: a gate above the limit gives limit * 3/4 * (u + 1); the linear
+    branch is clamped to [-limit, limit]; a gate of -ln(3)/2 is not clamped
+    and gives g / 4 * (u + 1); a very negative gate gives almost nothing (the
+    gate has no lower clamp)."""
+    lim = math.log(3.0) / 2.0
+    g = [5.0, 5.0, 5.0, -lim, -5.0]
+    u = [0.25, 3.0, -3.0, 0.5, 0.5]
+    a, g32, u32 = _one_hot_problem(g, u, 2.0, lim)
+    expect = [lim * 0.75 * 1.25, lim * 0.75 * (1 + lim), lim * 0.75 * (1 - lim),
+              g32[3] * 0.25 * 1.5]
+    assert np.allclose(a[:4], expect, rtol=2e-7, atol=0), (a, expect)
+    assert abs(a[4]) < 1e-3, a[4]
+
+
+def pin_swiglu_bias_is_a_ones_column():
+    """The w13 bias equals one more input column of ones whose weights are
+    the bias (the extra product is added last, as the bias is)."""
+    inp = rand_problem(9, 32, 16, 4, 2, "f32", seed=14)
+    rng = np.random.default_rng(3)
+    b13 = rng.standard_normal((4, 32)).astype(np.float32)
+    x = np_store(inp.x)
+    w13 = np_store(inp.w13)
+    kw = dict(activation=oracle.ACT_SWIGLU_CLAMP, swiglu_alpha=1.7, swiglu_limit=1.4)
+    P = oracle.make_problem(9, 32, 16, 4, 2, x, w13, w13_bias=b13, **kw)
+    got = oracle.forward(P, x, inp.topk_ids.numpy(), inp.topk_weights.numpy(), w13,
+                         np_store(inp.w2))
+    xa = np.concatenate([x, np.ones((9, 1), np.float32)], 1)
+    w13a = np.concatenate([w13, b13[:, :, None]], 2)
+    w2a = np.concatenate([np_store(inp.w2), np.zeros((4, 1, 16), np.float32)], 1)
+    Pa = oracle.make_problem(9, 33, 16, 4, 2, xa, w13a, **kw)
+    ref = oracle.forward(Pa, xa, inp.topk_ids.numpy(), inp.topk_weights.numpy(), w13a, w2a)
+    assert np.array_equal(got, ref[:, :32])
+
+
+def pin_w2_bias_closed_form():
+    """W2 = 0: out[t] = sum_k w_k * b2[e_k] (numpy)."""
+    inp = rand_problem(11, 16, 16, 5, 3, "f32", seed=15)
+    rng = np.random.default_rng(4)
+    b2 = rng.standard_normal((5, 16)).astype(np.float32)
+    w2 = np.zeros((5, 16, 16), np.float32)
+    x, w13 = np_store(inp.x), np_store(inp.w13)
+    P = oracle.make_problem(11, 16, 16, 5, 3, x, w13, w2_bias=b2)
+    out = oracle.forward(P, x, inp.topk_ids.numpy(), inp.topk_weights.numpy(), w13, w2)
+    ids, w = inp.topk_ids.numpy(), inp.topk_weights.numpy().astype(np.float64)
+    ref = np.einsum("tk,tkc->tc", w, b2[ids].astype(np.float64))
+    assert np.allclose(out, ref, rtol=1e-14, atol=1e-15)
+
+
+def pin_interleaved_gate_up():
+    """w13 (and its bias) with gate/up rows interleaved give exactly the
+    forward of the same rows put back into [gate; up] halves (numpy)."""
+    inp = rand_problem(13, 32, 24, 3, 2, "bf16", seed=16)
+    rng = np.random.default_rng(5)
+    b13 = rng.standard_normal((3, 48)).astype(np.float32)
+    w13 = np_store(inp.w13)  # (E, 2I, H): halves
+    inter = np.empty_like(w13)
+    inter[:, 0::2], inter[:, 1::2] = w13[:, :24], w13[:, 24:]
+    b_inter = np.empty_like(b13)
+    b_inter[:, 0::2], b_inter[:, 1::2] = b13[:, :24], b13[:, 24:]
+    x, w2 = np_store(inp.x), np_store(inp.w2)
+    kw = dict(activation=oracle.ACT_SWIGLU_CLAMP, swiglu_alpha=1.1, swiglu_limit=1.35)
+    args = (x, inp.topk_ids.numpy(), inp.topk_weights.numpy())
+    P1 = oracle.make_problem(13, 32, 24, 3, 2, x, inter, gate_up_interleaved=True,
+                             w13_bias=b_inter, **kw)
+    P2 = oracle.make_problem(13, 32, 24, 3, 2, x, w13, w13_bias=b13, **kw)
+    a = oracle.forward(P1, *args, inter, w2)
+    b = oracle.forward(P2, *args, w13, w2)
+    assert np.array_equal(a, b)
+    assert not np.array_equal(a, oracle.forward(P2, *args, inter, w2))
+
+
+SWIGLU_PINS = [pin_swiglu_clamp_closed_forms, pin_swiglu_bias_is_a_ones_column,
+               pin_w2_bias_closed_form, pin_interleaved_gate_up]
+
+SHARD_PINS = [pin_shards_sum_to_full, pin_shard_vs_torch, pin_align_local_vs_stable_argsort]
+
 FFN_PINS = [
     pin_identical_experts_dense_mlp, pin_top1_unit_weight_per_expert_ffn,
     pin_weighted_sum_over_slots, pin_loop_orders_agree, pin_zero_input, pin_linearity,

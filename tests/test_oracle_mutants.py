@@ -21,7 +21,7 @@ MUTANTS = [
      "double w = (double)topk_w[(size_t)k];"),
     ("down_proj_wrong_expert", "expert_out(p, w2, w2_scale, e, a, y, wrow);\n            for (int c = 0; c < p->H; ++c) o[c]",
      "expert_out(p, w2, w2_scale, 0, a, y, wrow);\n            for (int c = 0; c < p->H; ++c) o[c]"),
-    ("up_row_offset_wrong", "e, p->I + j, wrow);", "e, j + 1 < p->I ? j + 1 : j, wrow);"),
+    ("up_row_offset_wrong", "2 * j + 1 : p->I + j;", "2 * j + 1 : (j + 1 < p->I ? j + 1 : j);"),
     ("bf16_decode_shift", "((uint32_t)b) << 16", "((uint32_t)b) << 15"),
     ("e2m1_exponent_bias", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e)"),
     ("e8m0_bias", "ldexp(1.0, (int)v - 127)", "ldexp(1.0, (int)v - 128)"),
@@ -38,17 +38,31 @@ MUTANTS = [
     ("align_padding_rule", "(counts[e] + bm - 1) / bm * bm", "counts[e] / bm * bm"),
     ("align_sentinel", "sorted_ids[s] = (int32_t)na;", "sorted_ids[s] = -1;"),
     ("align_valid_rows", "bi[3] = left < bm ? left : bm;", "bi[3] = bm;"),
-    ("align_bad_id_accepted", "if (ids[i] < 0 || ids[i] >= E) return -1;\n    for (int e = 0; e < E; ++e) counts[e] = 0;",
-     "for (int e = 0; e < E; ++e) counts[e] = 0;"),
-    ("combine_slot_index", "y[(size_t)inv_perm[(size_t)t * K + k] * H + c]",
-     "y[(size_t)inv_perm[(size_t)t * K] * H + c]"),
+    ("align_bad_id_accepted", "if (ids[i] < 0 || ids[i] >= E) return -1;\n    for (int e = 0; e < L; ++e) counts[e] = 0;",
+     "for (int e = 0; e < L; ++e) counts[e] = 0;"),
+    ("combine_slot_index", "int slot = inv_perm[(size_t)t * K + k];",
+     "int slot = inv_perm[(size_t)t * K];"),
     ("gather_row_index", "load_token_row(p, x, i / p->K, xrow);",
      "load_token_row(p, x, i % p->T, xrow);"),
+    ("swiglu_alpha_dropped", "exp(-p->swiglu_alpha * g)", "exp(-g)"),
+    ("swiglu_plus_one_dropped", "* (u + 1.0);", "* u;"),
+    ("swiglu_gate_clamped_below", "g = fmin(g, p->swiglu_limit);",
+     "g = fmax(fmin(g, p->swiglu_limit), -p->swiglu_limit);"),
+    ("swiglu_linear_not_clamped_below", "u = fmax(fmin(u, p->swiglu_limit), -p->swiglu_limit);",
+     "u = fmin(u, p->swiglu_limit);"),
+    ("swiglu_up_takes_gate_bias", "(b13 ? (double)b13[up_row(p, j)] : 0.0)",
+     "(b13 ? (double)b13[gate_row(p, j)] : 0.0)"),
+    ("interleaved_gate_row_wrong", "return p->gate_up_interleaved ? 2 * j : j;",
+     "return p->gate_up_interleaved ? 2 * j + 1 : j;"),
+    ("w2_bias_dropped", " + (p->w2_bias ? (double)p->w2_bias[(size_t)e * p->H + c] : 0.0)", ""),
+    ("shard_other_slots_keep_slot", "        inv_perm[i] = -1;\n", "        inv_perm[i] = 0;\n"),
+    ("shard_weight_index_global", "e -= p->expert_base; /* index into this shard's weights */",
+     "e = e % shard_size(p);"),
 ]
 
 ALL_PINS = pins.FORMAT_PINS + [pins.pin_align_rejects_bad_id, pins.pin_align_invariants] + [
     (lambda c=c: pins.pin_align_vs_stable_argsort(*c)) for c in pins.ALIGN_CASES[:7]
-] + pins.FFN_PINS
+] + pins.FFN_PINS + pins.SHARD_PINS + pins.SWIGLU_PINS
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])

@@ -26,3 +26,13 @@ def test_align_invariants():
 
 def test_align_rejects_bad_id():
     pins.pin_align_rejects_bad_id()
+
+
+@pytest.mark.parametrize("pin", pins.SHARD_PINS, ids=lambda f: f.__name__)
+def test_shard_pin(pin):
+    pin()
+
+
+@pytest.mark.parametrize("pin", pins.SWIGLU_PINS, ids=lambda f: f.__name__)
+def test_swiglu_pin(pin):
+    pin()
