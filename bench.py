@@ -37,7 +37,7 @@ from mixture_experts_grouped_02_gb300 import inputs as gen  # noqa: E402
 METRIC = "MoE layer tokens/sec and TFLOP/s (prefill); HBM GB/s (decode) vs GB300 peak"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_gate_up_mixtral_prefill.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "mixture_experts_grouped_02_gb300", "csrc", f)
-                  for f in ("gemm_pair.cu", "sched.cuh", "ptx.cuh", "internal.h")]
+                  for f in ("gemm_wpair.cu", "sched.cuh", "ptx.cuh", "internal.h")]
 
 
 def parse():
@@ -332,11 +332,11 @@ def run_ours(args, ws, rank, local):
     if mx:
         stages.append(("quantize_gather_x", lambda: moe.moe_quantize_gather_x_fp8(
             inp.x, _abi.MOE_BF16, cfg.T, cfg.H, cfg.K, inv, xq, xs, st, stream)))
-    elif bm == 256:  # CTA pairs: the gather as its own pass
+    else:  # token rows to their sorted slots
         x_sorted = part(_abi.MOE_WS_XQ, inp.x.dtype)
         stages.append(("gather", lambda: moe.moe_gather_rows(
             inp.x, p.act, cfg.T, cfg.H, cfg.K, inv, x_sorted, st, stream)))
-    a_rows = xq if mx else (x_sorted if bm == 256 else inp.x)
+    a_rows = xq if mx else x_sorted
     stages.append(("gemm_gate_up", lambda: moe.moe_gemm1_silu(
         p, a_rows, xs, w13, s13, sorted_ids, binfo, nblk, h, st, stream)))
     stages.append(("gemm_down", lambda: moe.moe_gemm2_weighted(

@@ -67,22 +67,34 @@ typedef enum {
  *   block_m: rows per alignment block, 0 = automatic: 256 (the GEMMs then
  *            run on CTA pairs) when bf16/fp32 experts receive at least 256
  *            rows on average (T*K >= 256*E), else 128.
- *   h_scale: scale of the e4m3 hidden activation (MX weights only; 0 => 1). */
+ *   h_scale: scale of the e4m3 hidden activation (MX weights only; 0 => 1).
+ *   expert_base, local_experts: expert-parallel shard (local_experts = 0:
+ *            no sharding).  The layer's experts [expert_base,
+ *            expert_base + local_experts) live here; w13/w2 (and their
+ *            scales) hold those experts only, indexed from 0.  Ids still
+ *            range over [0, E); a slot routed to another shard's expert
+ *            contributes nothing, so out is this shard's share of the layer
+ *            output and the shards' outputs sum to the unsharded one.
+ *            Source: "MOE Bmm1 Fused Gather", init_routing_data (a shard
+ *            keeps the histogram of its local experts; experts split into
+ *            equal contiguous ranges by make_expt_dict_uniform). */
 typedef struct {
     int T, H, I, E, K;
     int act;
     int weight;
     int block_m;
     float h_scale;
+    int expert_base;
+    int local_experts;
 } moe_problem_t;
 
 /* Sub-buffers of the moe_forward workspace (byte offsets, see
  * moe_workspace_offsets). */
 typedef enum {
     MOE_WS_STATUS = 0,         /* int32 device status word                  */
-    MOE_WS_COUNTS = 1,         /* int32[E]                                  */
-    MOE_WS_OFFSETS = 2,        /* int32[E+1]                                */
-    MOE_WS_PADDED_OFFSETS = 3, /* int32[E+1]                                */
+    MOE_WS_COUNTS = 1,         /* int32[L]   (L = local experts, E unsharded) */
+    MOE_WS_OFFSETS = 2,        /* int32[L+1]                                */
+    MOE_WS_PADDED_OFFSETS = 3, /* int32[L+1]                                */
     MOE_WS_SORTED_IDS = 4,     /* int32[cap]                                */
     MOE_WS_INV_PERM = 5,       /* int32[T*K]                                */
     MOE_WS_BLOCK_INFO = 6,     /* int32[cap/block_m][4]                     */
@@ -150,6 +162,22 @@ int moe_workspace_offsets(const moe_problem_t* p, size_t offsets[MOE_WS_NUM],
 int moe_align(const int32_t* topk_ids, int T, int K, int E, int block_m, int32_t* counts,
               int32_t* offsets, int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
               int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream);
+
+/* moe_align for one expert-parallel shard holding experts
+ * [expert_base, expert_base + local_experts) of E.  Every per-expert output
+ * (counts, offsets, padded_offsets, the expert field of block_info) covers
+ * the local experts only, indexed e - expert_base; assignments to other
+ * experts are left out of the lists and get inv_perm[i] = -1.  cap =
+ * moe_align_capacity(T, K, local_experts, block_m).  Ids are still checked
+ * against [0, E).  expert_base = 0, local_experts = E is moe_align.
+ * Source: "MOE Bmm1 Fused Gather", init_routing_data (the local experts'
+ * histogram of one shard).  1 <= local_experts <= 1024,
+ * expert_base + local_experts <= E, else MOE_ERR_INVALID_ARG /
+ * MOE_ERR_UNSUPPORTED. */
+int moe_align_local(const int32_t* topk_ids, int T, int K, int E, int expert_base,
+                    int local_experts, int block_m, int32_t* counts, int32_t* offsets,
+                    int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
+                    int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream);
 
 /* ---- mxfp4 weight packing (once, when the model is loaded) -----------------
  * Source: "MOE Bmm1 Fused Gather" -- its matmul takes the e2m1 weights in a

@@ -12,16 +12,17 @@ import torch
 
 from . import _abi
 from ._abi import (MOE_BF16, MOE_E2M1_MX, MOE_E4M3, MOE_F32, MoEError, Problem, moe_abi_version,
-                   moe_align, moe_align_capacity, moe_combine, moe_forward, moe_forward_noalloc,
-                   moe_gather_rows, moe_gemm1_silu, moe_gemm2_default_splits, moe_gemm2_weighted,
-                   moe_get_device_status, moe_mx_packed_bytes, moe_pack_mx_weights,
-                   moe_quantize_gather_x_fp8, moe_quantize_x_fp8, moe_resolve_block_m,
-                   moe_workspace_offsets, moe_workspace_size)
+                   moe_align, moe_align_capacity, moe_align_local, moe_combine, moe_forward,
+                   moe_forward_noalloc, moe_gather_rows, moe_gemm1_silu, moe_gemm2_default_splits,
+                   moe_gemm2_weighted, moe_get_device_status, moe_mx_packed_bytes,
+                   moe_pack_mx_weights, moe_quantize_gather_x_fp8, moe_quantize_x_fp8,
+                   moe_resolve_block_m, moe_workspace_offsets, moe_workspace_size)
 
 __all__ = ["MoEError", "Problem", "make_problem", "dtype_code", "align", "Workspace", "forward",
            "pack_mx", "moe_forward_noalloc", "moe_mx_packed_bytes", "moe_pack_mx_weights",
            "moe_quantize_gather_x_fp8", "moe_gather_rows",
-           "moe_abi_version", "moe_align", "moe_align_capacity", "moe_combine", "moe_forward",
+           "moe_abi_version", "moe_align", "moe_align_capacity", "moe_align_local",
+           "moe_combine", "moe_forward",
            "moe_gemm1_silu", "moe_gemm2_default_splits", "moe_gemm2_weighted",
            "moe_get_device_status", "moe_quantize_x_fp8", "moe_resolve_block_m",
            "moe_workspace_offsets", "moe_workspace_size"]
@@ -37,27 +38,33 @@ def dtype_code(dt) -> int:
     raise ValueError(f"unsupported dtype {dt}")
 
 
-def make_problem(T, H, I, E, K, act="bf16", weight=None, block_m=0, h_scale=1.0) -> Problem:
+def make_problem(T, H, I, E, K, act="bf16", weight=None, block_m=0, h_scale=1.0,
+                 expert_base=0, local_experts=0) -> Problem:
+    """local_experts > 0: an expert-parallel shard holding experts
+    [expert_base, expert_base + local_experts) of E; its weights hold those
+    experts only."""
     a = dtype_code(act)
     w = a if weight is None else dtype_code(weight)
-    return Problem(T, H, I, E, K, a, w, block_m, h_scale)
+    return Problem(T, H, I, E, K, a, w, block_m, h_scale, expert_base, local_experts)
 
 
-def align(topk_ids: torch.Tensor, E: int, block_m: int = 128, dev_status=None, stream=None):
-    """Run moe_align on (T, K) int32 ids; returns the outputs as a dict of
-    device tensors."""
+def align(topk_ids: torch.Tensor, E: int, block_m: int = 128, dev_status=None, stream=None,
+          expert_base: int = 0, local_experts: int = 0):
+    """Run moe_align (moe_align_local for a shard) on (T, K) int32 ids;
+    returns the outputs as a dict of device tensors."""
     T, K = topk_ids.shape
-    cap = moe_align_capacity(T, K, E, block_m)
+    L = local_experts if local_experts > 0 else E
+    cap = moe_align_capacity(T, K, L, block_m)
     dev = topk_ids.device
     i32 = dict(dtype=torch.int32, device=dev)
-    out = dict(counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
-               padded_offsets=torch.empty(E + 1, **i32), sorted_ids=torch.empty(cap, **i32),
+    out = dict(counts=torch.empty(L, **i32), offsets=torch.empty(L + 1, **i32),
+               padded_offsets=torch.empty(L + 1, **i32), sorted_ids=torch.empty(cap, **i32),
                inv_perm=torch.empty(T * K, **i32),
                block_info=torch.empty((cap // block_m, 4), **i32),
                num_blocks=torch.empty(1, **i32))
-    moe_align(topk_ids, T, K, E, block_m, out["counts"], out["offsets"], out["padded_offsets"],
-              out["sorted_ids"], out["inv_perm"], out["block_info"], out["num_blocks"],
-              dev_status, stream)
+    moe_align_local(topk_ids, T, K, E, expert_base, L, block_m, out["counts"], out["offsets"],
+                    out["padded_offsets"], out["sorted_ids"], out["inv_perm"], out["block_info"],
+                    out["num_blocks"], dev_status, stream)
     return out
 
 
@@ -98,12 +105,18 @@ class Workspace:
 
 
 def forward(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=None, out=None,
-            workspace: Workspace | None = None, weight=None, h_scale=1.0, stream=None):
-    """out = MoE expert FFN of x routed by (topk_ids, topk_weights)."""
+            workspace: Workspace | None = None, weight=None, h_scale=1.0, stream=None,
+            num_experts=None, expert_base=0):
+    """out = MoE expert FFN of x routed by (topk_ids, topk_weights).  With
+    num_experts given, w13/w2 hold the experts [expert_base, expert_base +
+    w13.shape[0]) of num_experts (an expert-parallel shard) and out is this
+    shard's share of the layer output."""
     T, H = x.shape
-    E, I = w13.shape[0], w13.shape[1] // 2
+    L, I = w13.shape[0], w13.shape[1] // 2
+    E = L if num_experts is None else num_experts
     K = topk_ids.shape[1]
-    p = make_problem(T, H, I, E, K, x.dtype, weight, 0, h_scale)
+    p = make_problem(T, H, I, E, K, x.dtype, weight, 0, h_scale, expert_base,
+                     0 if num_experts is None else L)
     if workspace is None:
         workspace = Workspace(p, x.device)
     if out is None:

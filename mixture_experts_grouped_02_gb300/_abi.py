@@ -36,7 +36,7 @@ EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_a
            "moe_quantize_x_fp8", "moe_gemm1_silu", "moe_gemm2_weighted", "moe_combine",
            "moe_forward", "moe_forward_noalloc", "moe_get_device_status", "moe_mx_packed_bytes",
            "moe_pack_mx_weights", "moe_quantize_gather_x_fp8", "moe_device_info",
-           "moe_gather_rows")
+           "moe_gather_rows", "moe_align_local")
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -51,7 +51,8 @@ class Problem(ctypes.Structure):
     """moe_problem_t."""
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
                 ("E", ctypes.c_int), ("K", ctypes.c_int), ("act", ctypes.c_int),
-                ("weight", ctypes.c_int), ("block_m", ctypes.c_int), ("h_scale", ctypes.c_float)]
+                ("weight", ctypes.c_int), ("block_m", ctypes.c_int), ("h_scale", ctypes.c_float),
+                ("expert_base", ctypes.c_int), ("local_experts", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -97,6 +98,8 @@ def _declare(L):
     L.moe_workspace_offsets.argtypes = [PP, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     L.moe_align.restype = i32
     L.moe_align.argtypes = [vp, i32, i32, i32, i32] + [vp] * 8 + [vp]
+    L.moe_align_local.restype = i32
+    L.moe_align_local.argtypes = [vp, i32, i32, i32, i32, i32, i32] + [vp] * 8 + [vp]
     L.moe_quantize_x_fp8.restype = i32
     L.moe_quantize_x_fp8.argtypes = [vp, i32, i32, i32, vp, vp, vp]
     L.moe_gather_rows.restype = i32
@@ -191,6 +194,15 @@ def moe_align(topk_ids, T, K, E, block_m, counts, offsets, padded_offsets, sorte
     _check(lib().moe_align(_p(topk_ids), T, K, E, block_m, _p(counts), _p(offsets),
                            _p(padded_offsets), _p(sorted_ids), _p(inv_perm), _p(block_info),
                            _p(num_blocks), _p(dev_status), _stream(stream)), "moe_align")
+
+
+def moe_align_local(topk_ids, T, K, E, expert_base, local_experts, block_m, counts, offsets,
+                    padded_offsets, sorted_ids, inv_perm, block_info, num_blocks, dev_status=None,
+                    stream=None):
+    _check(lib().moe_align_local(_p(topk_ids), T, K, E, expert_base, local_experts, block_m,
+                                 _p(counts), _p(offsets), _p(padded_offsets), _p(sorted_ids),
+                                 _p(inv_perm), _p(block_info), _p(num_blocks), _p(dev_status),
+                                 _stream(stream)), "moe_align_local")
 
 
 def moe_quantize_x_fp8(x, x_dtype, T, H, xq, row_scale, stream=None):

@@ -12,8 +12,9 @@
 // One CTA of 32 warps does the whole job; the work is a few passes over
 // T*K int32 ids.  Warp w owns a contiguous chunk of the flat index range and
 // a private histogram row in shared memory:
-//   1. histogram: per 32-id batch, __match_any_sync groups equal ids and the
-//      group's lowest lane adds the group size to the warp's row;
+//   1. histogram: per 32-id batch, ballots over the bits of the id group
+//      equal ids and the group's lowest lane adds the group size to the
+//      warp's row;
 //   2. per expert, an exclusive scan over the warps' rows gives each warp its
 //      start inside the expert; a block-wide scan over experts gives the CSR
 //      and padded offsets;
@@ -22,6 +23,12 @@
 //      equal ids of lower lanes.  Chunks are in index order, batches in index
 //      order, lanes in index order, so the result is the stable order.
 //   4. padding slots, the tail up to the capacity, and block descriptors.
+// Expert-parallel shard: only the experts [e_base, e_base + e_local) get
+// lists (all per-expert outputs are indexed by e - e_base); an assignment to
+// another expert is left out and its inverse-permutation entry is -1.  The
+// shard of all E experts is the plain align.  Source for the shard: the
+// "MOE Bmm1 Fused Gather" example's init_routing_data, which keeps the
+// histogram of the local experts of one expert shard.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -42,6 +49,19 @@ __device__ __forceinline__ void load_ids(const int* ids, int base, int hi, int l
     const int i = base + 32 * u + lane;
     e[u] = i < hi ? __ldg(ids + i) : -1;
   }
+}
+
+// Lanes of the warp whose `key` equals this lane's, keys in [0, 2^nbits):
+// one ballot per key bit (a warp-level multi-split), the same set
+// __match_any_sync gives, at a cost set by the key width.
+__device__ __forceinline__ unsigned peers_of(int key, int nbits) {
+  unsigned m = 0xffffffffu;
+  for (int b = 0; b < nbits; ++b) {
+    const int bit = (key >> b) & 1;
+    const unsigned bal = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? bal : ~bal;
+  }
+  return m;
 }
 
 // Block-wide exclusive scan of two int values per thread (1024 threads).
@@ -85,10 +105,12 @@ __device__ __forceinline__ void block_exclusive_scan2(int& a, int& b, int* s_tmp
 
 __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs p) {
   extern __shared__ int sm[];
-  const int E = p.E;
-  int* hist = sm;                        // [kAlignWarps][E]
-  int* s_pad = hist + kAlignWarps * E;   // [E + 1] padded offsets
-  int* s_cnt = s_pad + E + 1;            // [E]
+  const int E = p.E;        // ids must lie in [0, E)
+  const int L = p.e_local;  // experts of this shard: [e_base, e_base + L)
+  const int key_bits = 32 - __clz(L);  // keys e + 1 in [0, L], 0 = not counted here
+  int* hist = sm;                        // [kAlignWarps][L]
+  int* s_pad = hist + kAlignWarps * L;   // [L + 1] padded offsets
+  int* s_cnt = s_pad + L + 1;            // [L]
   __shared__ int s_tmp[64];
   __shared__ int s_bad;
   __shared__ int s_carry[2];
@@ -98,14 +120,14 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
   const int bm = p.block_m;
 
   if (tid == 0) s_bad = 0;
-  for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) hist[i] = 0;
+  for (int i = tid; i < kAlignWarps * L; i += kAlignThreads) hist[i] = 0;
   __syncthreads();
 
   // chunk of warp w: [w*chunk, min(na, (w+1)*chunk)), chunk a multiple of 32
   const int chunk = ((na + kAlignWarps - 1) / kAlignWarps + 31) & ~31;
   const int lo = warp * chunk;
   const int hi = min(na, lo + chunk);
-  int* my_hist = hist + warp * E;
+  int* my_hist = hist + warp * L;
 
   // 1. histogram
   for (int base0 = lo; base0 < hi; base0 += 32 * kAlignUnroll) {
@@ -117,8 +139,11 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
       if (base0 + 32 * u + lane < hi && (e < 0 || e >= E)) {
         s_bad = 1;
         e = -1;
+      } else if (e >= 0) {
+        e -= p.e_base;  // local expert; another shard's expert is left out
+        if (e < 0 || e >= L) e = -1;
       }
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const unsigned peers = peers_of(e + 1, key_bits);
       if (e >= 0 && lane == __ffs(peers) - 1) my_hist[e] += __popc(peers);
       __syncwarp();
     }
@@ -133,11 +158,11 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
   }
 
   // 2. per-expert scan over warps, then scans over experts (chunks of 1024)
-  for (int e = tid; e < E; e += kAlignThreads) {
+  for (int e = tid; e < L; e += kAlignThreads) {
     int run = 0;
     for (int w = 0; w < kAlignWarps; ++w) {
-      const int c = hist[w * E + e];
-      hist[w * E + e] = run;
+      const int c = hist[w * L + e];
+      hist[w * L + e] = run;
       run += c;
     }
     s_cnt[e] = run;
@@ -148,9 +173,9 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
     s_carry[1] = 0;
   }
   __syncthreads();
-  for (int e0 = 0; e0 < E; e0 += kAlignThreads) {
+  for (int e0 = 0; e0 < L; e0 += kAlignThreads) {
     const int e = e0 + tid;
-    const int c = e < E ? s_cnt[e] : 0;
+    const int c = e < L ? s_cnt[e] : 0;
     int a = c;
     int b = (c + bm - 1) / bm * bm;
     const int carry_a = s_carry[0], carry_b = s_carry[1];
@@ -158,21 +183,21 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
     block_exclusive_scan2(a, b, s_tmp);
     a += carry_a;
     b += carry_b;
-    if (e < E) {
+    if (e < L) {
       p.offsets[e] = a;
       p.padded_offsets[e] = b;
       s_pad[e] = b;
     }
-    if (e == min(E, e0 + kAlignThreads) - 1) {  // last expert of this chunk
+    if (e == min(L, e0 + kAlignThreads) - 1) {  // last expert of this chunk
       s_carry[0] = a + c;
       s_carry[1] = b + pa;
     }
     __syncthreads();
   }
   if (tid == 0) {
-    p.offsets[E] = s_carry[0];
-    p.padded_offsets[E] = s_carry[1];
-    s_pad[E] = s_carry[1];
+    p.offsets[L] = s_carry[0];
+    p.padded_offsets[L] = s_carry[1];
+    s_pad[L] = s_carry[1];
   }
   __syncthreads();
 
@@ -183,8 +208,12 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
 #pragma unroll
     for (int u = 0; u < kAlignUnroll; ++u) {
       const int i = base0 + 32 * u + lane;
-      const int e = ev[u];
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      int e = ev[u] - p.e_base;
+      if (i >= hi || e < 0 || e >= L) {
+        if (i < hi) p.inv_perm[i] = -1;  // routed to an expert of another shard
+        e = -1;
+      }
+      const unsigned peers = peers_of(e + 1, key_bits);
       if (e >= 0) {
         const unsigned lower = peers & ((1u << lane) - 1u);
         const int slot = s_pad[e] + my_hist[e] + __popc(lower);
@@ -198,12 +227,12 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
   }
 
   // 4a. padding slots of each expert, and the tail [padded_offsets[E], cap)
-  for (int e = tid; e < E; e += kAlignThreads)
+  for (int e = tid; e < L; e += kAlignThreads)
     for (int s = s_pad[e] + s_cnt[e]; s < s_pad[e + 1]; ++s) p.sorted_ids[s] = na;
-  for (long long s = s_pad[E] + tid; s < p.cap; s += kAlignThreads) p.sorted_ids[s] = na;
+  for (long long s = s_pad[L] + tid; s < p.cap; s += kAlignThreads) p.sorted_ids[s] = na;
 
   // 4b. block descriptors {expert, m, first slot, valid rows}
-  const int nb = s_pad[E] / bm;
+  const int nb = s_pad[L] / bm;
   const long long max_blocks = p.cap / bm;
   int4* bi = reinterpret_cast<int4*>(p.block_info);
   for (long long b = tid; b < max_blocks; b += kAlignThreads) {
@@ -212,7 +241,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
       const int row = static_cast<int>(b) * bm;
       // the expert whose padded range holds `row`: last e with s_pad[e] <= row
       // among experts with a non-empty range
-      int l = 0, h = E;  // find smallest e with s_pad[e + 1] > row
+      int l = 0, h = L;  // find smallest e with s_pad[e + 1] > row
       while (l < h) {
         const int mid = (l + h) >> 1;
         if (s_pad[mid + 1] > row)
@@ -230,12 +259,12 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
 
 }  // namespace
 
-size_t align_smem_bytes(int E) {
-  return sizeof(int) * (static_cast<size_t>(kAlignWarps) * E + (E + 1) + E);
+size_t align_smem_bytes(int L) {
+  return sizeof(int) * (static_cast<size_t>(kAlignWarps) * L + (L + 1) + L);
 }
 
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s) {
-  const size_t smem = align_smem_bytes(a.E);
+  const size_t smem = align_smem_bytes(a.e_local);
   cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;

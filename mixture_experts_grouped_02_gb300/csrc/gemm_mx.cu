@@ -9,10 +9,12 @@
 // with the e8m0 code 127 (unit scales; here the per-row fp8 scale of x is
 // applied in the epilogue instead); the weights arrive pre-arranged for the
 // kernel (its MX4 value and scale layouts); pack_e4m3x2 (fp32 -> e4m3, round
-// to nearest even, saturating) for the hidden activation.  The SiLU*up and
-// routing-weight epilogues are those of gemm.cu.
+// to nearest even, saturating) for the hidden activation.  The epilogues form
+// SiLU(g)*u per row (gate/up) and multiply the routing weight (down), as the
+// bf16 GEMMs do.
 //
-// Layout per CTA (one per SM, persistent, bands of N tiles as in gemm.cu):
+// Layout per CTA (one per SM, persistent, tiles walked in bands of N tiles
+// so that co-resident CTAs share weight tiles in L2):
 //  * tile = 128 sorted rows x 192 weight rows, as two MMAs of N = 96:
 //    gate/up: 96 gate rows and the matching 96 up rows of w13[e];
 //    down: 192 rows of w2[e];
@@ -34,7 +36,9 @@
 //  * tensor memory: two 192-column fp32 accumulators, 4 columns of unit A
 //    scales, 4 columns of B scales per stage and MMA half.
 //
-// All waits are bounded as in gemm.cu.
+// Every mbarrier wait is bounded (MxArgs::timeout_ns of wall clock); a thread
+// that gives up raises the CTA's abort flag, which every other wait polls,
+// and the kernel records MOE_ERR_TIMEOUT, drains and frees its TMEM.
 #include <cuda_bf16.h>
 
 #include "internal.h"

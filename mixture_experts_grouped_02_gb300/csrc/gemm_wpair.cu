@@ -1,0 +1,471 @@
+// gemm_wpair.cu -- the two bf16/fp32 grouped GEMMs of the expert FFN:
+//   gate/up: h[s, j] = SiLU(w13[e, j, :] . x_s) * (w13[e, I + j, :] . x_s)
+//   down:    y[q, s, c] = w_s * sum_{j in split q} w2[e, c, j] * h[s, j]
+// for every valid slot s of an align block of expert e (x_s: the token row
+// of slot s, in sorted order as moe_gather_rows writes it; w_s its routing
+// weight).  Sources: "factor_moe_fused_gemm.cu", fused_silu_gate_kernel
+// (gate = first half of the w13 rows, SiLU(g) = g / (1 + e^-g)); "moe triton
+// kernel use tma", the review comment on TOKEN_INPUT_USE_TMA /
+// MUL_ROUTED_WEIGHT (token rows contiguous in sorted order, routing weight
+// in the down projection's epilogue); "MOE Bmm1 Fused Gather" (weights as
+// the MMA's A operand, the gathered tokens as B, two-CTA mode).
+//
+// Tile.  One tcgen05.mma.cta_group::2 covers 256 weight rows (128 per CTA of
+// a cluster of two) and N tokens of one align block, N = the block's valid
+// row count rounded up to 16 (at most 256).  A block of an expert that
+// received 5 tokens runs N = 16 instead of a full 128- or 256-row tile, so
+// padding costs next to no tensor-core time and a sparsely used expert's
+// tiles are pure weight streaming.  Per CTA and 64-wide K step (one stage):
+// 128 weight rows (16 KB) and N/2 token rows, loaded as a 16-row box when
+// N <= 32 (decode) and as a 128-row box otherwise; six 32 KB stages.
+//  * gate/up: a CTA's 128 weight rows are 64 gate rows and the 64 up rows
+//    with the same indices j, so TMEM lanes 0-63 hold gate and 64-127 up of
+//    the same j for every token column.  The epilogue warp of lanes
+//    32q..32q+31 (q < 2) and the one of lanes 64+32q.. exchange half of each
+//    32-column chunk through shared memory and each forms SiLU(g)*u for 16
+//    tokens; the 32 lanes of a warp store 32 consecutive h values of a row;
+//  * down: TMEM lane = output column, so the 32 lanes of a warp store 32
+//    consecutive fp32 of one y row (128 bytes) per token.
+//
+// Pair protocol.  One producer thread per CTA issues its TMA copies with the
+// .cta_group::2 form, which completes them on the LEADER's full barrier; the
+// leader alone declares both CTAs' bytes there, so no follower thread signals
+// the leader per stage (a cluster-scope release would wait for all of the
+// releasing thread's earlier memory operations).  The leader's MMA thread
+// issues the pair MMAs (A and B read from the same shared-memory offsets in
+// both CTAs; each CTA's TMEM receives its 128 rows of D) and commits with a
+// multicast to both CTAs' empty and accumulator-full barriers.  The
+// follower's epilogue threads arrive on a barrier of their own CTA and one
+// idle lane relays each accumulator release to the leader.  Both CTAs
+// allocate TMEM as a pair and meet at a cluster barrier before freeing it.
+//
+// Schedule.  Persistent: one cluster per SM pair, tiles (block, weight tile,
+// K split) walked in bands of weight tiles so that co-resident pairs share
+// weight and token tiles in L2; two TMEM accumulators, so the epilogue of one
+// tile overlaps the MMAs of the next.
+//
+// Every mbarrier wait is bounded (GemmArgs::timeout_ns of wall clock): a
+// thread that gives up raises the CTA's abort flag, which every other wait
+// polls, lets issued copies and MMAs drain, and the kernel records
+// MOE_ERR_TIMEOUT in the status word and frees its TMEM.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace moe {
+namespace {
+
+enum Kind { kGateUp = 0, kDown = 1 };
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr uint32_t kFmt = 1;
+};
+template <>
+struct Elem<float> {
+  static constexpr uint32_t kFmt = 2;
+};
+
+template <int KIND, typename T>
+struct WCfg {
+  static constexpr int kWRows = 128;          // weight rows per CTA (MMA M = 256 per pair)
+  static constexpr int kNMax = 256;           // tokens per tile at most
+  static constexpr int kRowBytes = 128;
+  static constexpr int kBK = kRowBytes / sizeof(T);
+  static constexpr int kUmmaK = 32 / sizeof(T);
+  static constexpr int kStages = 6;
+  static constexpr int kABytes = kWRows * kRowBytes;            // 16 KB of weights
+  static constexpr int kBigRows = kNMax / 2;                    // token box rows
+  static constexpr int kSmallRows = 16;
+  static constexpr int kBBytes = kBigRows * kRowBytes;          // 16 KB slot
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kAccCols = kNMax;
+  static constexpr int kTmemCols = 2 * kAccCols;
+  static constexpr int kProducerWarp = 0;
+  static constexpr int kMmaWarp = 1;
+  static constexpr int kThreads = (2 + 4) * 32;
+  // gate/up exchange: 2 warp pairs x 2 directions x 16 columns x 32 lanes
+  static constexpr int kXchgBytes = KIND == kGateUp ? 2 * 2 * 16 * 32 * 4 : 0;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kXchgBytes + 1024;
+};
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return g / (1.0f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ void settle(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) {
+  }
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier `id` over `threads` threads that also ANDs `pred` across them.
+__device__ __forceinline__ int named_bar_and(int id, int threads, int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "r"(id), "r"(threads)
+      : "memory");
+  return r;
+}
+
+// Tokens the MMA of a block with `valid` rows covers: a multiple of 16.
+__device__ __forceinline__ int tile_n(int valid) {
+  return min(256, max(16, (valid + 15) & ~15));
+}
+
+template <typename T>
+__device__ __forceinline__ void store_h(T* p, float v);
+template <>
+__device__ __forceinline__ void store_h<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16_rn(v);
+}
+template <>
+__device__ __forceinline__ void store_h<float>(float* p, float v) {
+  *p = v;
+}
+
+template <int KIND, typename T>
+__global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
+    wpair_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmTok,
+                      const __grid_constant__ CUtensorMap tmTokS,
+                      const __grid_constant__ CUtensorMap tmW) {
+  using C = WCfg<KIND, T>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[C::kStages];
+  __shared__ __align__(8) uint64_t empty_bar[C::kStages];
+  __shared__ __align__(8) uint64_t accf_bar[2];
+  __shared__ __align__(8) uint64_t acce_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t relay_acce[2];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_skip;
+  __shared__ int s_skip_pair;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t smemA = smem_base;
+  const uint32_t smemB = smem_base + C::kStages * C::kABytes;
+  float* xchg = reinterpret_cast<float*>(smem_raw + (smem_base - smem_u32(smem_raw)) +
+                                         C::kStages * C::kStageBytes);
+
+  if (threadIdx.x == 0) {
+    s_skip = (a.status != nullptr && *reinterpret_cast<volatile int32_t*>(a.status) != 0);
+    s_abort = 0;
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&accf_bar[i]), 1);
+      mbar_init(smem_u32(&acce_bar[i]), 128 + 1);
+      mbar_init(smem_u32(&relay_acce[i]), 128);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  cluster_sync();
+  if (threadIdx.x == 0)
+    s_skip_pair = leader ? s_skip
+                         : static_cast<int>(ld_shared_cluster_u32(mapa_shared(smem_u32(&s_skip), 0)));
+  __syncthreads();
+  const bool skip = s_skip_pair != 0;
+  if (!skip && warp == C::kMmaWarp) tmem_alloc_pair(smem_u32(&s_tmem_base), C::kTmemCols);
+  if (warp == C::kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmTok);
+    tma_prefetch_desc(&tmTokS);
+    tma_prefetch_desc(&tmW);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = s_tmem_base;
+
+  const int num_blocks = skip ? 0 : *a.num_blocks;
+  const int total = num_blocks * a.n_tiles * a.splits;
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const uint64_t to = a.timeout_ns;
+
+  if (warp == C::kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < total && ok; tile += nclusters) {
+        const Tile t = decode_tile(tile, num_blocks, a);
+        const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
+        const int e = bi.x;
+        const int n = tile_n(bi.w);
+        const int half = n >> 1;
+        const bool small = half <= C::kSmallRows;
+        const int tok_row = bi.z + static_cast<int>(rank) * half;
+        const uint32_t tx =
+            2u * static_cast<uint32_t>(C::kABytes + (small ? C::kSmallRows : C::kBigRows) *
+                                                        C::kRowBytes);
+        // this CTA's weight rows: 64 gate rows j and the 64 up rows j, or
+        // 128 rows of w2
+        const int wrow = KIND == kGateUp
+                             ? e * 2 * a.I + t.nt * 128 + static_cast<int>(rank) * 64
+                             : e * a.H + t.nt * 256 + static_cast<int>(rank) * 128;
+        int kb, ke;
+        split_range(a, t.split, kb, ke);
+        for (int kt = kb; kt < ke; ++kt) {
+          if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, to)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + stage * 8u;
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), tx);
+          const uint32_t sa = smemA + stage * C::kABytes;
+          if constexpr (KIND == kGateUp) {
+            tma_load_2d_pair(sa, &tmW, fb, kt * C::kBK, wrow);
+            tma_load_2d_pair(sa + C::kABytes / 2, &tmW, fb, kt * C::kBK, wrow + a.I);
+          } else {
+            tma_load_2d_pair(sa, &tmW, fb, kt * C::kBK, wrow);
+          }
+          tma_load_2d_pair(smemB + stage * C::kBBytes, small ? &tmTokS : &tmTok, fb, kt * C::kBK,
+                           tok_row);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) settle(to / 8);
+    }
+    __syncwarp();
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (leader && lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < total && ok; tile += nclusters) {
+        const Tile t = decode_tile(tile, num_blocks, a);
+        const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
+        const uint32_t idesc = make_idesc(Elem<T>::kFmt, 256, tile_n(bi.w));
+        int kb, ke;
+        split_range(a, t.split, kb, ke);
+        if (!mbar_wait_bounded_cluster(smem_u32(&acce_bar[acc]), acc_phase ^ 1, &s_abort, to)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * C::kAccCols;
+        for (int kt = kb; kt < ke; ++kt) {
+          if (!mbar_wait_bounded_cluster(smem_u32(&full_bar[stage]), phase, &s_abort, to)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_base = smemA + stage * C::kABytes;
+          const uint32_t b_base = smemB + stage * C::kBBytes;
+#pragma unroll
+          for (int k = 0; k < C::kBK / C::kUmmaK; ++k) {
+            const uint64_t ad = sw128_kmajor_desc(a_base + k * 32);
+            const uint64_t bd = sw128_kmajor_desc(b_base + k * 32);
+            const uint32_t accum = (kt > kb || k > 0) ? 1u : 0u;
+            if constexpr (Elem<T>::kFmt == 1)
+              umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+            else
+              umma_tf32_pair(d_tmem, ad, bd, idesc, accum);
+          }
+          umma_commit_pair(smem_u32(&empty_bar[stage]), 0x3);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(smem_u32(&accf_bar[acc]), 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (!ok) {
+        umma_commit_pair(smem_u32(&drain_bar), 0x1);
+        drain_wait(smem_u32(&drain_bar), 0, to / 4);
+      }
+    } else if (!leader && lane == 1) {
+      const uint32_t acce0 = mapa_shared(smem_u32(&acce_bar[0]), 0);
+      uint32_t acc = 0, acc_phase = 0;
+      for (int tile = cluster; tile < total; tile += nclusters) {
+        if (!mbar_wait_bounded(smem_u32(&relay_acce[acc]), acc_phase, &s_abort, to)) break;
+        mbar_arrive_cluster(acce0 + acc * 8u);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = cluster; tile < total; tile += nclusters) {
+      const Tile t = decode_tile(tile, num_blocks, a);
+      const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
+      const int valid = bi.w;
+      const int n = tile_n(valid);
+      int good = 1;
+      if (lane == 0) good = mbar_wait_bounded(smem_u32(&accf_bar[acc]), acc_phase, &s_abort, to);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      // the two warps of an exchange pair leave together or not at all
+      if constexpr (KIND == kGateUp) good = named_bar_and(1 + (q & 1), 64, good);
+      if (!good) break;
+      tc_fence_after_sync();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::kAccCols;
+      if constexpr (KIND == kGateUp) {
+        const bool gate_warp = q < 2;
+        const int pq = q & 1;
+        const int j = t.nt * 128 + static_cast<int>(rank) * 64 + pq * 32 + lane;
+        float* x_g = xchg + (pq * 2 + 0) * 16 * 32;  // gate, columns 16..31 of a chunk
+        float* x_u = xchg + (pq * 2 + 1) * 16 * 32;  // up, columns 0..15
+        T* hcol = reinterpret_cast<T*>(a.out) + j;
+        for (int c0 = 0; c0 < n; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c0, v);
+          tmem_wait_ld();
+          if (gate_warp) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x_g[i * 32 + lane] = __uint_as_float(v[16 + i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x_u[i * 32 + lane] = __uint_as_float(v[i]);
+          }
+          named_bar_sync(1 + pq, 64);
+          // gate warp: tokens c0..c0+15; up warp: tokens c0+16..c0+31
+          const int nb = gate_warp ? c0 : c0 + 16;
+          if (j < a.I) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g = gate_warp ? __uint_as_float(v[i]) : x_g[i * 32 + lane];
+              const float u = gate_warp ? x_u[i * 32 + lane] : __uint_as_float(v[16 + i]);
+              if (nb + i < valid)
+                store_h<T>(hcol + static_cast<long long>(bi.z + nb + i) * a.I, silu_mul(g, u));
+            }
+          }
+          named_bar_sync(1 + pq, 64);  // the exchange slots are free again
+        }
+      } else {
+        const int c = t.nt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
+        float* ycol = reinterpret_cast<float*>(a.out) +
+                      static_cast<long long>(t.split) * a.cap * a.H + c;
+        for (int c0 = 0; c0 < n; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c0, v);
+          // routing weight of token c0 + lane, broadcast below
+          const int my = c0 + lane;
+          const float w_l = my < valid ? a.topk_weights[a.sorted_ids[bi.z + my]] : 0.0f;
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float w = __shfl_sync(0xffffffffu, w_l, i);
+            if (c0 + i < valid && c < a.H)
+              ycol[static_cast<long long>(bi.z + c0 + i) * a.H] = w * __uint_as_float(v[i]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(leader ? smem_u32(&acce_bar[acc]) : smem_u32(&relay_acce[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  if (threadIdx.x == 0 && s_abort) report_error(a.status, MOE_ERR_TIMEOUT);
+  if (!skip && warp == C::kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int KIND, typename T>
+cudaLaunchConfig_t wpair_config(int grid, cudaStream_t s, cudaLaunchAttribute* attr) {
+  using C = WCfg<KIND, T>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int KIND, typename T>
+int max_pairs() {
+  using C = WCfg<KIND, T>;
+  auto kern = wpair_gemm_kernel<KIND, T>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = wpair_config<KIND, T>(2, nullptr, attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int KIND, typename T>
+cudaError_t launch(const GemmArgs& a, const CUtensorMap& tmTok, const CUtensorMap& tmTokS,
+                   const CUtensorMap& tmW, int grid, cudaStream_t s) {
+  using C = WCfg<KIND, T>;
+  auto kern = wpair_gemm_kernel<KIND, T>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = wpair_config<KIND, T>(grid, s, attr);
+  return cudaLaunchKernelEx(&cfg, kern, a, tmTok, tmTokS, tmW);
+}
+
+}  // namespace
+
+int wpair_max_active(int kind, int dtype) {
+  if (kind == 0)
+    return dtype == MOE_BF16 ? max_pairs<kGateUp, __nv_bfloat16>() : max_pairs<kGateUp, float>();
+  return dtype == MOE_BF16 ? max_pairs<kDown, __nv_bfloat16>() : max_pairs<kDown, float>();
+}
+
+cudaError_t launch_wpair_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
+                                 const CUtensorMap& tmTokS, const CUtensorMap& tmW, int grid,
+                                 cudaStream_t s) {
+  if (dtype == MOE_BF16) return launch<kGateUp, __nv_bfloat16>(a, tmTok, tmTokS, tmW, grid, s);
+  return launch<kGateUp, float>(a, tmTok, tmTokS, tmW, grid, s);
+}
+
+cudaError_t launch_wpair_down(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
+                              const CUtensorMap& tmTokS, const CUtensorMap& tmW, int grid,
+                              cudaStream_t s) {
+  if (dtype == MOE_BF16) return launch<kDown, __nv_bfloat16>(a, tmTok, tmTokS, tmW, grid, s);
+  return launch<kDown, float>(a, tmTok, tmTokS, tmW, grid, s);
+}
+
+}  // namespace moe

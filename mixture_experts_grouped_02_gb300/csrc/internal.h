@@ -13,14 +13,16 @@ namespace moe {
 // Default wall-clock limit of any single pipeline wait inside a kernel.
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
-// The grouped GEMMs tile 128 sorted rows (tokens) per block: the align
-// block size equals the GEMM's M tile.
+// Align blocks of the block-scaled GEMMs (their M tile), and the smaller of
+// the two automatic block sizes of the bf16/fp32 GEMMs.
 constexpr int kBlockM = 128;
 
 struct AlignArgs {
   const int32_t* ids;
   int n_assign;  // T*K
-  int E;
+  int E;         // ids lie in [0, E)
+  int e_base;    // first expert of this shard
+  int e_local;   // experts of this shard (E when unsharded)
   int block_m;
   long long cap;
   int32_t* counts;
@@ -41,7 +43,7 @@ struct GemmArgs {
   int splits;    // reduction splits (down projection); 1 for gate/up
   int band;      // N tiles per raster band
   long long cap; // rows of the padded sorted list
-  const void* x;               // gate/up: token rows (T, H), gathered by cp.async
+  const void* x;               // gate/up: token rows in sorted order (cap, H)
   const int32_t* sorted_ids;
   const int32_t* block_info;
   const int32_t* num_blocks;
@@ -101,21 +103,18 @@ cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, i
                                      const int32_t* inv_perm, uint8_t* xq_sorted,
                                      float* row_scale, const int32_t* status, cudaStream_t s);
 
-// dtype: MOE_BF16 or MOE_F32.  tmA: down -> h (box 128 rows; unused by
-// gate/up, which gathers x itself).  tmB: w13 (box 128 rows) / w2 (box 256 rows).
-cudaError_t launch_gemm_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmA,
-                                const CUtensorMap& tmB, int grid, cudaStream_t s);
-cudaError_t launch_gemm_down(int dtype, const GemmArgs& a, const CUtensorMap& tmA,
-                             const CUtensorMap& tmB, int grid, cudaStream_t s);
-
-// CTA-pair variants for 256-row align blocks (grid = 2 x clusters).
+// Align blocks of 256 rows: the largest token tile of the bf16/fp32 GEMMs.
 constexpr int kPairBlockM = 256;
-// CTA pairs the device holds at once for the gate/up (kind 0) or down (1)
-// pair kernel, 0 if it cannot be determined.
-int pair_max_active(int kind, int dtype);
-cudaError_t launch_pair_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmA,
-                                const CUtensorMap& tmB, int grid, cudaStream_t s);
-cudaError_t launch_pair_down(int dtype, const GemmArgs& a, const CUtensorMap& tmA,
-                             const CUtensorMap& tmB, int grid, cudaStream_t s);
+
+// The bf16/fp32 grouped GEMMs on CTA pairs with the weights on the MMA's M
+// side (gemm_wpair.cu); grid = 2 x clusters.  tmTok / tmTokS: token rows in sorted order (x for gate/up, h for down),
+// boxes of 128 and 16 rows; tmW: w13 (box 64 rows) or w2 (box 128 rows).
+int wpair_max_active(int kind, int dtype);
+cudaError_t launch_wpair_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
+                                 const CUtensorMap& tmTokS, const CUtensorMap& tmW, int grid,
+                                 cudaStream_t s);
+cudaError_t launch_wpair_down(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
+                              const CUtensorMap& tmTokS, const CUtensorMap& tmW, int grid,
+                              cudaStream_t s);
 
 }  // namespace moe

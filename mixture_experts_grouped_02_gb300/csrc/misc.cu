@@ -9,7 +9,8 @@ namespace moe {
 namespace {
 
 // out[t, :] = sum_k sum_q y[q, inv_perm[t*K + k], :], fp32 in k order, then
-// one rounding to the output type.  Source: the index_add of the "Current
+// one rounding to the output type.  A negative slot (an assignment to an
+// expert another shard holds) adds nothing.  Source: the index_add of the "Current
 // PyTorch path" in "factor_moe_fused_gemm.cu" and its
 // weighted_scatter_add_kernel, made deterministic: each token owns its row,
 // so no atomics and a fixed summation order.  CTA (x, y) handles token rows
@@ -35,12 +36,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         float4 v[kCombineBatch];
 #pragma unroll
         for (int k = 0; k < kCombineBatch; ++k)
-          if (k < K)
+          if (k < K && slots[k] >= 0)
             v[k] = __ldg(reinterpret_cast<const float4*>(y + static_cast<long long>(slots[k]) * H) +
                          c);
 #pragma unroll
         for (int k = 0; k < kCombineBatch; ++k)
-          if (k < K) {
+          if (k < K && slots[k] >= 0) {
             acc.x += v[k].x;
             acc.y += v[k].y;
             acc.z += v[k].z;
@@ -49,6 +50,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       } else {
         for (int k = 0; k < K; ++k) {
           const long long row = slots[k];
+          if (row < 0) continue;
           for (int q = 0; q < splits; ++q) {
             const float4 v = __ldg(reinterpret_cast<const float4*>(
                                        y + (static_cast<long long>(q) * cap + row) * H) +
@@ -113,7 +115,8 @@ __global__ void __launch_bounds__(256) quantize_x_kernel(const void* __restrict_
 // The same quantisation, with each token's codes written to every slot of the
 // expert-sorted list the token occupies (xq_sorted[inv_perm[t*K + k]]), so that
 // the block-scaled gate/up GEMM reads contiguous rows: the token gather is
-// fused into this pass, which reads every row of x anyway.
+// fused into this pass, which reads every row of x anyway.  Negative slots
+// (another shard's experts) are skipped.
 __global__ void __launch_bounds__(256) quantize_gather_x_kernel(
     const void* __restrict__ x, int bf16, int T, int H, int K, const int32_t* __restrict__ inv_perm,
     uint8_t* __restrict__ xq_sorted, float* __restrict__ row_scale, const int32_t* status) {
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(256) quantize_gather_x_kernel(
       asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pk) : "f"(v1), "f"(v0));
       for (int k = 0; k < K; ++k) {
         const long long slot = inv_perm[static_cast<long long>(t) * K + k];
-        *reinterpret_cast<uint16_t*>(xq_sorted + slot * H + c) = pk;
+        if (slot >= 0) *reinterpret_cast<uint16_t*>(xq_sorted + slot * H + c) = pk;
       }
     }
     __syncthreads();
@@ -148,7 +151,8 @@ __global__ void __launch_bounds__(256) quantize_gather_x_kernel(
 // Token rows to sorted slots: xs[inv_perm[t*K + k], :] = x[t, :] for every
 // choice k of token t (rows of padding slots untouched).  The gather of the
 // gate/up GEMM done as its own pass, for the CTA-pair GEMMs whose A operand
-// then arrives by plain TMA tiles.  16-byte copies; a CTA per token row.
+// then arrives by plain TMA tiles.  16-byte copies; a CTA per token row;
+// negative slots (another shard's experts) are skipped.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
                                                           int T, int row_vec, int K,
                                                           const int32_t* __restrict__ inv_perm,
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
       const uint4 v = __ldg(src + c);
       for (int k = 0; k < K; ++k) {
         const long long slot = inv_perm[static_cast<long long>(t) * K + k];
-        xs[slot * row_vec + c] = v;
+        if (slot >= 0) xs[slot * row_vec + c] = v;
       }
     }
   }

@@ -20,7 +20,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr size_t kWsAlign = 1024;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxDevices = 64;
@@ -34,6 +34,11 @@ bool valid_dtype_pair(int act, int weight) {
   return weight == MOE_E2M1_MX && act == MOE_BF16;
 }
 
+// Experts held by this call: the shard's, or all E.
+int local_experts(const moe_problem_t* p) {
+  return p->local_experts > 0 ? p->local_experts : p->E;
+}
+
 int check_problem(const moe_problem_t* p) {
   if (p == nullptr) return MOE_ERR_INVALID_ARG;
   if (p->T < 0 || p->H <= 0 || p->I <= 0 || p->E <= 0 || p->K <= 0) return MOE_ERR_INVALID_ARG;
@@ -41,33 +46,38 @@ int check_problem(const moe_problem_t* p) {
   if (p->block_m != 0 && p->block_m != 16 && p->block_m != 32 && p->block_m != 64 &&
       p->block_m != 128 && p->block_m != 256)
     return MOE_ERR_INVALID_ARG;
-  if (p->E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (p->expert_base < 0 || p->local_experts < 0 ||
+      static_cast<long long>(p->expert_base) + p->local_experts > p->E ||
+      (p->local_experts == 0 && p->expert_base != 0))
+    return MOE_ERR_INVALID_ARG;
+  if (local_experts(p) > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   const long long na = static_cast<long long>(p->T) * p->K;
   if (na >= (1ll << 30)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
-// Rows per align block.  The bf16/fp32 GEMMs run on CTA pairs (256-row
-// blocks) when experts receive many tokens on average -- padding each expert
-// to 256 instead of 128 rows then costs little -- and on single CTAs
-// (128-row blocks) otherwise.
+// Rows per align block.  The bf16/fp32 GEMMs take a block's tokens as the
+// MMA's N (up to 256, rounded up to 16 from the block's valid rows), so the
+// block size bounds the tile and costs no MMA work on padding: 256-row
+// blocks once experts receive 256 rows on average (larger tiles move fewer
+// bytes into the SMs per MMA), 128 otherwise (a smaller padded workspace).
+// The block-scaled GEMMs tile 128 rows.
 int block_m_of(const moe_problem_t* p) {
   if (p->block_m != 0) return p->block_m;
   if (p->weight == MOE_E2M1_MX) return kBlockM;
   const long long na = static_cast<long long>(p->T) * p->K;
-  return na >= 768ll * p->E ? kPairBlockM : kBlockM;
+  return na >= 256ll * p->E ? kPairBlockM : kBlockM;
 }
 
 bool is_mx(const moe_problem_t* p) { return p->weight == MOE_E2M1_MX; }
 
-// The bf16/fp32 GEMMs read 128-byte k-tiles (64 bf16 / 32 fp32) and write
-// 32-column output chunks; the block-scaled GEMMs need whole 32-element scale
-// blocks along K (the end of K inside a 128-element tile is zero-filled).
-// The GEMM tile is 128 sorted rows.
+// The bf16/fp32 GEMMs read 128-byte k-tiles (64 bf16 / 32 fp32); any align
+// block of at most 256 rows is one tile.  The block-scaled GEMMs need 128-row
+// blocks and whole 32-element scale blocks along K (the end of K inside a
+// 128-element tile is zero-filled).
 int check_gemm_shapes(const moe_problem_t* p) {
   const int bm = block_m_of(p);
-  if (bm != kBlockM && !(bm == kPairBlockM && p->weight != MOE_E2M1_MX))
-    return MOE_ERR_UNSUPPORTED;
+  if (is_mx(p) && bm != kBlockM) return MOE_ERR_UNSUPPORTED;
   if (is_mx(p)) {
     if (p->H % 32 != 0 || p->I % 32 != 0) return MOE_ERR_UNSUPPORTED;
     if (!(p->h_scale >= 0.0f) || p->h_scale > 3.0e38f) return MOE_ERR_INVALID_ARG;
@@ -115,22 +125,40 @@ long long capacity(long long T, long long K, long long E, long long bm) {
   return na + std::min(E, na) * (bm - 1);
 }
 
+int pairs_held(int kind, int dtype);
+
+// K splits of the down projection.  Only batches too small to give every
+// worker (CTA pair, or SM for the block-scaled GEMM) several tiles split: the
+// count makes the number of (tile, split) units fill whole waves of
+// workers as closely as possible, each split keeping at least 4 k-tiles.
+// The block count is estimated on the host (at most one partly filled block
+// per active expert).
 int default_splits(const moe_problem_t* p) {
   const int bm = block_m_of(p);
   const long long na = static_cast<long long>(p->T) * p->K;
   if (na == 0) return 1;
-  const long long cap = capacity(p->T, p->K, p->E, bm);
+  const long long L = local_experts(p);
+  const long long cap = capacity(p->T, p->K, L, bm);
   const long long est_blocks =
-      std::min(cap / bm, (na + bm - 1) / bm + std::min<long long>(p->E, na));
+      std::max(1ll, std::min({cap / bm, na, (na + bm - 1) / bm + std::min(L, na) - 1}));
   const long long n_tiles = (p->H + down_tile_n(p) - 1) / down_tile_n(p);
   const long long k_tiles = std::max(1, (p->I + down_tile_k(p) - 1) / down_tile_k(p));
-  const long long work = std::max(1ll, est_blocks * n_tiles);
-  const long long target = 2ll * sm_count();
-  if (work >= target) return 1;
-  long long s = (target + work - 1) / work;
-  s = std::min(s, std::max(1ll, k_tiles / 4));
-  s = std::min(s, 32ll);
-  return static_cast<int>(std::max(1ll, s));
+  const long long units = std::max(1ll, est_blocks * n_tiles);
+  const long long workers = is_mx(p) ? sm_count() : pairs_held(1, p->act);
+  if (units >= 4 * workers) return 1;
+  const long long s_max = std::min(32ll, std::max(1ll, k_tiles / 4));
+  long long best = 1;
+  double best_eff = 0.0;
+  for (long long sp = 1; sp <= s_max; ++sp) {
+    const long long u = units * sp;
+    const long long waves = (u + workers - 1) / workers;
+    const double eff = static_cast<double>(u) / static_cast<double>(waves * workers);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = sp;
+    }
+  }
+  return static_cast<int>(best);
 }
 
 struct Layout {
@@ -142,21 +170,20 @@ struct Layout {
 void layout_of(const moe_problem_t* p, Layout* L) {
   const int bm = block_m_of(p);
   const long long na = static_cast<long long>(p->T) * p->K;
-  const long long cap = capacity(p->T, p->K, p->E, bm);
+  const long long cap = capacity(p->T, p->K, local_experts(p), bm);
   const bool mx = p->weight == MOE_E2M1_MX;
   const int splits = default_splits(p);
   size_t sz[MOE_WS_NUM] = {};
   sz[MOE_WS_STATUS] = 256;
-  sz[MOE_WS_COUNTS] = 4ull * p->E;
-  sz[MOE_WS_OFFSETS] = 4ull * (p->E + 1);
-  sz[MOE_WS_PADDED_OFFSETS] = 4ull * (p->E + 1);
+  sz[MOE_WS_COUNTS] = 4ull * local_experts(p);
+  sz[MOE_WS_OFFSETS] = 4ull * (local_experts(p) + 1);
+  sz[MOE_WS_PADDED_OFFSETS] = 4ull * (local_experts(p) + 1);
   sz[MOE_WS_SORTED_IDS] = 4ull * cap;
   sz[MOE_WS_INV_PERM] = 4ull * na;
   sz[MOE_WS_BLOCK_INFO] = 16ull * (cap / bm);
   sz[MOE_WS_NUM_BLOCKS] = 4;
   // A rows in sorted order: e4m3 codes (MX), activation rows (CTA pairs)
-  sz[MOE_WS_XQ] = mx ? static_cast<size_t>(cap) * p->H
-                     : (bm == kPairBlockM ? static_cast<size_t>(cap) * p->H * act_bytes(p->act) : 0);
+  sz[MOE_WS_XQ] = static_cast<size_t>(cap) * p->H * (mx ? 1 : act_bytes(p->act));
   sz[MOE_WS_X_SCALE] = mx ? 4ull * p->T : 0;
   sz[MOE_WS_H] = static_cast<size_t>(cap) * p->I * (mx ? 1 : act_bytes(p->act));
   sz[MOE_WS_Y] = 4ull * splits * static_cast<size_t>(cap) * p->H;
@@ -227,15 +254,18 @@ int make_map(CUtensorMap* tm, int dtype, const void* base, long long inner, long
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-int run_align(const int32_t* ids, int T, int K, int E, int bm, int32_t* counts, int32_t* offsets,
-              int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
-              int32_t* block_info, int32_t* num_blocks, int32_t* status, cudaStream_t s) {
+int run_align(const int32_t* ids, int T, int K, int E, int e_base, int e_local, int bm,
+              int32_t* counts, int32_t* offsets, int32_t* padded_offsets, int32_t* sorted_ids,
+              int32_t* inv_perm, int32_t* block_info, int32_t* num_blocks, int32_t* status,
+              cudaStream_t s) {
   AlignArgs a;
   a.ids = ids;
   a.n_assign = T * K;
   a.E = E;
+  a.e_base = e_base;
+  a.e_local = e_local;
   a.block_m = bm;
-  a.cap = capacity(T, K, E, bm);
+  a.cap = capacity(T, K, e_local, bm);
   a.counts = counts;
   a.offsets = offsets;
   a.padded_offsets = padded_offsets;
@@ -255,36 +285,40 @@ GemmArgs base_args(const moe_problem_t* p) {
   a.I = p->I;
   a.E = p->E;
   a.K = p->K;
-  a.cap = capacity(p->T, p->K, p->E, block_m_of(p));
+  a.cap = capacity(p->T, p->K, local_experts(p), block_m_of(p));
   a.timeout_ns = kWaitTimeoutNs;
   return a;
 }
 
-// Persistent grid: one CTA per SM, no more CTAs than tiles.  CTA pairs: no
-// more pairs than the device holds at once (cluster placement can leave SMs
-// without a partner), so that every pair is resident from the start.
+// Persistent grid of CTA pairs: no more pairs than the device holds at once
+// (cluster placement can leave SMs without a partner), so that every pair
+// is resident from the start, and no more than there are tiles.
 int pair_limit(int kind, int dtype) {
   static std::mutex mu;
   static int cache[2][2] = {{-1, -1}, {-1, -1}};
   std::lock_guard<std::mutex> lk(mu);
   int& v = cache[kind][dtype == MOE_BF16 ? 1 : 0];
-  if (v < 0) v = pair_max_active(kind, dtype);
+  if (v < 0) v = wpair_max_active(kind, dtype);
   return v;
 }
 
-int grid_for(long long tiles, bool pairs, int kind = 0, int dtype = MOE_BF16) {
-  const long long sms = sm_count();
-  if (!pairs) return static_cast<int>(std::max(1ll, std::min(sms, tiles)));
-  long long limit = sms / 2;
+int pairs_held(int kind, int dtype) {
+  long long limit = sm_count() / 2;
   const int held = pair_limit(kind, dtype);
   if (held > 0) limit = std::min<long long>(limit, held);
-  const long long clusters = std::max(1ll, std::min(limit, tiles));
+  return static_cast<int>(std::max(1ll, limit));
+}
+
+int pair_grid(long long tiles, int kind, int dtype) {
+  const long long clusters = std::max(1ll, std::min<long long>(pairs_held(kind, dtype), tiles));
   return static_cast<int>(2 * clusters);
 }
 
-int run_gemm1(const moe_problem_t* p, const void* x, const void* w13, const int32_t* sorted_ids,
-              const int32_t* block_info, const int32_t* num_blocks, void* h, int32_t* status,
-              cudaStream_t s) {
+// Gate/up: token rows of x in sorted order (moe_gather_rows) x w13, on CTA
+// pairs with 256 weight rows (128 gate + 128 up indices j) per tile.
+int run_gemm1(const moe_problem_t* p, const void* x_sorted, const void* w13,
+              const int32_t* sorted_ids, const int32_t* block_info, const int32_t* num_blocks,
+              void* h, int32_t* status, cudaStream_t s) {
   GemmArgs a = base_args(p);
   const int bk = p->act == MOE_BF16 ? 64 : 32;
   a.n_tiles = (p->I + 127) / 128;
@@ -296,25 +330,18 @@ int run_gemm1(const moe_problem_t* p, const void* x, const void* w13, const int3
   a.num_blocks = num_blocks;
   a.out = h;
   a.status = status;
-  a.x = x;
-  if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) return MOE_ERR_INVALID_ARG;
-  CUtensorMap tmB;
-  int rc = make_map(&tmB, p->act, w13, p->H, 2ll * p->I * p->E, bk, 128);
+  a.x = x_sorted;
+  CUtensorMap tmTok, tmTokS, tmW;
+  int rc = make_map(&tmW, p->act, w13, p->H, 2ll * p->I * local_experts(p), bk, 64);
+  if (rc == MOE_OK) rc = make_map(&tmTok, p->act, x_sorted, p->H, a.cap, bk, 128);
+  if (rc == MOE_OK) rc = make_map(&tmTokS, p->act, x_sorted, p->H, a.cap, bk, 16);
   if (rc != MOE_OK) return rc;
-  const int bm = block_m_of(p);
-  const long long max_tiles = (a.cap / bm) * a.n_tiles;
-  if (bm == kPairBlockM) {
-    // CTA pairs read x in sorted order (cap rows) as plain TMA tiles
-    CUtensorMap tmA;
-    rc = make_map(&tmA, p->act, x, p->H, a.cap, bk, 128);
-    if (rc != MOE_OK) return rc;
-    return cuda_status(
-        launch_pair_gate_up(p->act, a, tmA, tmB, grid_for(max_tiles, true, 0, p->act), s));
-  }
-  const CUtensorMap& tmA = tmB;  // the single-CTA kernel gathers x without a tensor map
-  return cuda_status(launch_gemm_gate_up(p->act, a, tmA, tmB, grid_for(max_tiles, false), s));
+  const long long max_tiles = (a.cap / block_m_of(p)) * a.n_tiles;
+  return cuda_status(launch_wpair_gate_up(p->act, a, tmTok, tmTokS, tmW,
+                                          pair_grid(max_tiles, 0, p->act), s));
 }
 
+// Down: h rows x w2 x routing weight, on CTA pairs with 256 w2 rows per tile.
 int run_gemm2(const moe_problem_t* p, const void* h, const void* w2, const float* topk_weights,
               const int32_t* sorted_ids, const int32_t* block_info, const int32_t* num_blocks,
               float* y, int splits, int32_t* status, cudaStream_t s) {
@@ -330,19 +357,14 @@ int run_gemm2(const moe_problem_t* p, const void* h, const void* w2, const float
   a.topk_weights = topk_weights;
   a.out = y;
   a.status = status;
-  CUtensorMap tmA, tmB;
-  int rc = make_map(&tmA, p->act, h, p->I, a.cap, bk, 128);
+  CUtensorMap tmTok, tmTokS, tmW;
+  int rc = make_map(&tmW, p->act, w2, p->I, 1ll * p->H * local_experts(p), bk, 128);
+  if (rc == MOE_OK) rc = make_map(&tmTok, p->act, h, p->I, a.cap, bk, 128);
+  if (rc == MOE_OK) rc = make_map(&tmTokS, p->act, h, p->I, a.cap, bk, 16);
   if (rc != MOE_OK) return rc;
-  const int bm = block_m_of(p);
-  const bool pairs = bm == kPairBlockM;
-  // single CTA: one 256-row box of w2; pairs: each CTA loads 128 of the 256 rows
-  rc = make_map(&tmB, p->act, w2, p->I, 1ll * p->H * p->E, bk, pairs ? 128 : 256);
-  if (rc != MOE_OK) return rc;
-  const long long max_tiles = (a.cap / bm) * a.n_tiles * splits;
-  if (pairs)
-    return cuda_status(
-        launch_pair_down(p->act, a, tmA, tmB, grid_for(max_tiles, true, 1, p->act), s));
-  return cuda_status(launch_gemm_down(p->act, a, tmA, tmB, grid_for(max_tiles, false), s));
+  const long long max_tiles = (a.cap / block_m_of(p)) * a.n_tiles * splits;
+  return cuda_status(launch_wpair_down(p->act, a, tmTok, tmTokS, tmW,
+                                       pair_grid(max_tiles, 1, p->act), s));
 }
 
 MxArgs mx_args(const moe_problem_t* p) {
@@ -353,7 +375,7 @@ MxArgs mx_args(const moe_problem_t* p) {
   a.I = p->I;
   a.E = p->E;
   a.K = p->K;
-  a.cap = capacity(p->T, p->K, p->E, kBlockM);
+  a.cap = capacity(p->T, p->K, local_experts(p), kBlockM);
   a.h_scale = h_scale_of(p);
   a.timeout_ns = kWaitTimeoutNs;
   return a;
@@ -382,7 +404,7 @@ int run_gemm1_mx(const moe_problem_t* p, const void* xq, const float* x_row_scal
   CUtensorMap tmA, tmW;
   int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, p->H, a.cap, p->H, 128, 128);
   if (rc != MOE_OK) return rc;
-  rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, Hp, 2ll * p->I * p->E,
+  rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, Hp, 2ll * p->I * local_experts(p),
                       Hp / 2, 128, 96);
   if (rc != MOE_OK) return rc;
   a.sorted_ids = sorted_ids;
@@ -416,7 +438,7 @@ int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const u
   CUtensorMap tmA, tmW;
   int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq, p->I, a.cap, p->I, 128, 128);
   if (rc != MOE_OK) return rc;
-  rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, Ip, 1ll * p->H * p->E,
+  rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, Ip, 1ll * p->H * local_experts(p),
                       Ip / 2, 128, 192);
   if (rc != MOE_OK) return rc;
   a.sorted_ids = sorted_ids;
@@ -488,18 +510,29 @@ int moe_workspace_offsets(const moe_problem_t* p, size_t offsets[MOE_WS_NUM],
 int moe_align(const int32_t* topk_ids, int T, int K, int E, int block_m, int32_t* counts,
               int32_t* offsets, int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
               int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream) {
+  return moe_align_local(topk_ids, T, K, E, 0, E, block_m, counts, offsets, padded_offsets,
+                         sorted_ids, inv_perm, block_info, num_blocks, dev_status, stream);
+}
+
+int moe_align_local(const int32_t* topk_ids, int T, int K, int E, int expert_base,
+                    int local_experts, int block_m, int32_t* counts, int32_t* offsets,
+                    int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
+                    int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream) {
   if (T < 0 || K <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
   if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128 && block_m != 256)
     return MOE_ERR_INVALID_ARG;
-  if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (expert_base < 0 || local_experts <= 0 ||
+      static_cast<long long>(expert_base) + local_experts > E)
+    return MOE_ERR_INVALID_ARG;
+  if (local_experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(T) * K >= (1ll << 30)) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!topk_ids || !counts || !offsets || !padded_offsets || !sorted_ids || !inv_perm ||
       !block_info || !num_blocks)
     return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(block_info) & 15u) != 0) return MOE_ERR_INVALID_ARG;
-  return run_align(topk_ids, T, K, E, block_m, counts, offsets, padded_offsets, sorted_ids,
-                   inv_perm, block_info, num_blocks, dev_status,
+  return run_align(topk_ids, T, K, E, expert_base, local_experts, block_m, counts, offsets,
+                   padded_offsets, sorted_ids, inv_perm, block_info, num_blocks, dev_status,
                    static_cast<cudaStream_t>(stream));
 }
 
@@ -622,7 +655,8 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
   const int bm = block_m_of(p);
 
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
-  rc = run_align(topk_ids, p->T, p->K, p->E, bm, reinterpret_cast<int32_t*>(part(MOE_WS_COUNTS)),
+  rc = run_align(topk_ids, p->T, p->K, p->E, p->expert_base, local_experts(p), bm,
+                 reinterpret_cast<int32_t*>(part(MOE_WS_COUNTS)),
                  reinterpret_cast<int32_t*>(part(MOE_WS_OFFSETS)),
                  reinterpret_cast<int32_t*>(part(MOE_WS_PADDED_OFFSETS)), sorted_ids, inv_perm,
                  block_info, num_blocks, status, s);
@@ -639,22 +673,18 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                       splits, status, s);
     if (rc != MOE_OK) return rc;
   } else {
-    const void* a_rows = x;
-    if (bm == kPairBlockM) {  // CTA pairs: the gather as its own pass
-      void* xs = part(MOE_WS_XQ);
-      if (launch_gather_rows(x, p->T, static_cast<int>(p->H * act_bytes(p->act)), p->K,
-                             inv_perm, xs, status, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      a_rows = xs;
-    }
-    rc = run_gemm1(p, a_rows, w13, sorted_ids, block_info, num_blocks, h, status, s);
+    void* xs = part(MOE_WS_XQ);  // token rows in sorted order
+    if (launch_gather_rows(x, p->T, static_cast<int>(p->H * act_bytes(p->act)), p->K, inv_perm,
+                           xs, status, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    rc = run_gemm1(p, xs, w13, sorted_ids, block_info, num_blocks, h, status, s);
     if (rc != MOE_OK) return rc;
     rc = run_gemm2(p, h, w2, topk_weights, sorted_ids, block_info, num_blocks, y, splits, status,
                    s);
     if (rc != MOE_OK) return rc;
   }
-  return cuda_status(launch_combine(y, splits, capacity(p->T, p->K, p->E, bm), inv_perm, p->T,
-                                    p->K, p->H, p->act, out, status, s));
+  return cuda_status(launch_combine(y, splits, capacity(p->T, p->K, local_experts(p), bm),
+                                    inv_perm, p->T, p->K, p->H, p->act, out, status, s));
 }
 
 size_t moe_mx_packed_bytes(int E, int R, int K, int sections, size_t* value_bytes,
@@ -681,7 +711,7 @@ int moe_pack_mx_weights(const uint8_t* w, const uint8_t* w_scale, int E, int R, 
 
 int moe_device_info(int* sm_count_out, int* pair_clusters_out) {
   if (sm_count_out) *sm_count_out = sm_count();
-  if (pair_clusters_out) *pair_clusters_out = pair_limit(0, MOE_BF16);
+  if (pair_clusters_out) *pair_clusters_out = pairs_held(0, MOE_BF16);
   return MOE_OK;
 }
 

@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
     L = _abi.lib()
     for name in declared_functions():
         assert hasattr(L, name), name
-    assert _abi.moe_abi_version() == 1
+    assert _abi.moe_abi_version() == 2
 
 
 def test_status_strings():
@@ -104,9 +104,9 @@ def test_entry_points_reject_bad_arguments_before_launch():
     p = make_problem(16, 100, 256, 8, 2, "bf16")  # H not a multiple of 64
     assert L.moe_gemm1_silu(ctypes.byref(p), *([fake] * 8), None, None) == \
         _abi.MOE_ERR_UNSUPPORTED
-    p = make_problem(16, 128, 256, 8, 2, "bf16", block_m=64)
+    p = make_problem(16, 128, 256, 8, 2, "bf16", "mxfp4", block_m=64)
     assert L.moe_gemm1_silu(ctypes.byref(p), *([fake] * 8), None, None) == \
-        _abi.MOE_ERR_UNSUPPORTED
+        _abi.MOE_ERR_UNSUPPORTED  # the block-scaled GEMMs tile 128 rows
     p = make_problem(16, 128, 256, 8, 2, "bf16")
     assert L.moe_gemm2_weighted(ctypes.byref(p), *([fake] * 7), fake, 0, None, None) == \
         _abi.MOE_ERR_INVALID_ARG  # k_splits = 0
@@ -125,6 +125,13 @@ def test_entry_points_reject_bad_arguments_before_launch():
     assert L.moe_quantize_x_fp8(fake, _abi.MOE_BF16, 4, 7, fake, fake, None) == \
         _abi.MOE_ERR_INVALID_ARG
     assert L.moe_get_device_status(None, None) == _abi.MOE_ERR_INVALID_ARG
+    # expert shards: the range must lie inside [0, E)
+    for base, local in ((-1, 2), (7, 2), (0, 0), (0, 9)):
+        assert L.moe_align_local(fake, 4, 2, 8, base, local, 128, *([fake] * 7), None, None) == \
+            _abi.MOE_ERR_INVALID_ARG
+    for base, local in ((1, 0), (-1, 3), (6, 3)):
+        bad = make_problem(16, 128, 256, 8, 2, "bf16", expert_base=base, local_experts=local)
+        assert _abi.moe_workspace_size(bad) == 0
 
 
 def test_product_package_does_not_import_oracle():

@@ -70,6 +70,24 @@ def test_align_bad_id_sets_status():
     assert int(got["num_blocks"].item()) == 0
 
 
+@pytest.mark.parametrize("case,shard", [((300, 4, 16, 64, "skewed"), (0, 5)),
+                                        ((37, 3, 8, 32, "normal"), (3, 4)),
+                                        ((2000, 8, 256, 128, "normal"), (224, 32)),
+                                        ((64, 2, 8, 256, "normal"), (7, 1))])
+def test_align_local_bit_exact(case, shard):
+    T, K, E, bm, kind = case
+    base, L = shard
+    ids = pins.align_ids(T, K, E, kind)
+    ref = oracle.align(ids, E, bm, expert_base=base, local_experts=L)
+    st = _status()
+    got = moe.align(torch.from_numpy(ids).cuda(), E, bm, dev_status=st, expert_base=base,
+                    local_experts=L)
+    assert moe.moe_get_device_status(st) == 0
+    for k in ("counts", "offsets", "padded_offsets", "sorted_ids", "inv_perm", "block_info"):
+        assert np.array_equal(got[k].cpu().numpy(), ref[k]), k
+    assert int(got["num_blocks"].item()) == ref["num_blocks"]
+
+
 # ------------------------------------------------------------------ stages
 
 STAGE_CASES = [
@@ -90,7 +108,7 @@ def _expert_of_rows(al, rows, ids_flat):
     return ids_flat[al["sorted_ids"][rows]].astype(np.int32)
 
 
-@pytest.mark.parametrize("bm", [128, 256], ids=["cta", "pair"])
+@pytest.mark.parametrize("bm", [32, 128, 256])
 @pytest.mark.parametrize("case", STAGE_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s" % c)
 def test_gemm1_silu_stage(case, bm):
     T, H, I, E, K, dt = case
@@ -103,12 +121,11 @@ def test_gemm1_silu_stage(case, bm):
     cap = moe.moe_align_capacity(T, K, E, bm)
     h = torch.full((cap, I), float("nan"), dtype=d.x.dtype, device="cuda")
     st = _status()
-    x_in = d.x
-    if bm == 256:  # CTA pairs read the token rows at their sorted slots
-        xs = np.zeros((cap, H), np.float32)
-        valid = al_ref["sorted_ids"] < T * K
-        xs[valid] = inp.x.float().numpy()[al_ref["sorted_ids"][valid] // K]
-        x_in = torch.from_numpy(xs).to(d.x.dtype).cuda()
+    # the GEMM reads the token rows at their sorted slots (moe_gather_rows)
+    xs = np.zeros((cap, H), np.float32)
+    valid = al_ref["sorted_ids"] < T * K
+    xs[valid] = inp.x.float().numpy()[al_ref["sorted_ids"][valid] // K]
+    x_in = torch.from_numpy(xs).to(d.x.dtype).cuda()
     moe.moe_gemm1_silu(p, x_in, None, d.w13, None, al["sorted_ids"], al["block_info"],
                        al["num_blocks"], h, st)
     assert moe.moe_get_device_status(st) == 0
@@ -129,7 +146,7 @@ def test_gemm1_silu_stage(case, bm):
         assert torch.isnan(h[torch.from_numpy(pad).long().cuda()].float()).all()
 
 
-@pytest.mark.parametrize("bm", [128, 256], ids=["cta", "pair"])
+@pytest.mark.parametrize("bm", [32, 128, 256])
 @pytest.mark.parametrize("splits", [1, 2, 3])
 @pytest.mark.parametrize("case", STAGE_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s" % c)
 def test_gemm2_weighted_stage(case, splits, bm):
@@ -201,7 +218,7 @@ def _run_forward(d, cfg, poison=True, block_m=0):
     return out, ws
 
 
-@pytest.mark.parametrize("bm", [0, 256], ids=["auto", "pair"])
+@pytest.mark.parametrize("bm", [0, 16, 256])
 @pytest.mark.parametrize("case", FORWARD_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s_%s" % c)
 def test_forward_small(case, bm):
     cfg = gen.MoEConfig("fwd", *case)
@@ -228,7 +245,7 @@ def test_forward_tiny_config():
     assert_close(out, ref, what="tiny")
 
 
-@pytest.mark.parametrize("bm", [128, 256], ids=["cta", "pair"])
+@pytest.mark.parametrize("bm", [128, 256])
 def test_forward_deterministic_and_padding_untouched(bm):
     cfg = gen.MoEConfig("fwd", 300, 256, 320, 3, 2, "bf16", "normal")
     d = gen.generate(cfg, seed=32).to("cuda")
@@ -507,3 +524,60 @@ def test_forward_lowp_full_size_sampled():
     out = _run_forward_mx(inp, cfg)
     assert torch.isfinite(out.float()).all()
     _check_mx(out, inp, sample_tokens(cfg.T, 8, seed=2))
+
+
+# ------------------------------------------------------------------ expert shards
+
+def _oracle_shard(inp, base, L, tokens, mode=oracle.EXACT, **kw):
+    c = inp.cfg
+    P = oracle.make_problem(c.T, c.H, c.I, c.E, c.K, np_store(inp.x[:1]), np_store(inp.w13[:1]),
+                            expert_base=base, local_experts=L, **kw)
+    sl = slice(base, base + L)
+    sc = lambda t: None if t is None else np_store(t[sl].cpu())
+    return oracle.forward(P, np_store(inp.x.cpu()), inp.topk_ids.cpu().numpy(),
+                          inp.topk_weights.cpu().numpy(), np_store(inp.w13[sl].cpu()),
+                          np_store(inp.w2[sl].cpu()), sc(inp.w13_scale), sc(inp.w2_scale),
+                          mode=mode, tokens=tokens)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_forward_expert_shards(dtype):
+    """Each shard's output against the oracle's shard; the shards' outputs
+    sum to the unsharded forward."""
+    cfg = gen.MoEConfig("shard", 200, 256, 320, 8, 2, dtype, "normal")
+    inp = gen.generate(cfg, seed=41)
+    d = inp.to("cuda")
+    total = torch.zeros((cfg.T, cfg.H), dtype=torch.float64, device="cuda")
+    for base, L in ((0, 3), (3, 4), (7, 1)):
+        out = moe.forward(d.x, d.topk_ids, d.topk_weights, d.w13[base:base + L].contiguous(),
+                          d.w2[base:base + L].contiguous(), num_experts=cfg.E, expert_base=base)
+        ref = _oracle_shard(inp, base, L, np.arange(cfg.T))
+        assert_close(out, ref, what=f"shard {base}+{L}")
+        # tokens none of whose experts live here get an exact zero row
+        ids = inp.topk_ids.numpy()
+        none = ~((ids >= base) & (ids < base + L)).any(1)
+        assert torch.all(out[torch.from_numpy(none).cuda()] == 0)
+        total += out.double()
+    full, _ = _run_forward(d, cfg)
+    # each shard's output is rounded once to the activation type
+    assert_close(total, full.double().cpu().numpy(), max_abs=4e-2, what="sum of shards")
+
+
+def test_forward_expert_shard_mx():
+    cfg = gen.MoEConfig("shard_mx", 96, 256, 320, 16, 4, "mxfp4", "uniform")
+    inp = gen.generate(cfg, seed=42)
+    d = inp.to("cuda")
+    base, L = 4, 8
+    sl = slice(base, base + L)
+    w13p, s13p = moe.pack_mx(d.w13[sl].contiguous(), d.w13_scale[sl].contiguous(), 2)
+    w2p, s2p = moe.pack_mx(d.w2[sl].contiguous(), d.w2_scale[sl].contiguous(), 1)
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "bf16", "mxfp4", expert_base=base,
+                         local_experts=L)
+    ws = moe.Workspace(p)
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, w13p, s13p, w2p, s2p, out, ws.buffer,
+                    ws.nbytes)
+    assert moe.moe_get_device_status(ws.status) == 0
+    emu = _oracle_shard(inp, base, L, np.arange(cfg.T), mode=oracle.EMULATE, quantize_x=True,
+                        h_e4m3=True)
+    assert_close(out, emu, max_abs=MX_MAX_ABS, rel_l2=MX_REL_EMU, what="mx shard vs emulate")
