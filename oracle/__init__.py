@@ -90,6 +90,8 @@ def _declare(L):
     L.orc_align_local.restype = ci
     L.orc_align_local.argtypes = [i32p, ci, ci, ci, ci, ci, ci, i32p, i32p, i32p, i32p, i32p, i32p,
                                   i32p]
+    L.orc_route.restype = ci
+    L.orc_route.argtypes = [vp, ci, ci, ci, ci, i32p, f64p]
     L.orc_align_capacity.restype = ctypes.c_long
     L.orc_align_capacity.argtypes = [ci, ci, ci, ci]
     L.orc_moe_forward.restype = ci
@@ -165,6 +167,21 @@ def make_problem(T, H, I, E, K, x, w13, quantize_x=False, h_e4m3=False, h_scale=
                 None if b13 is None else b13.ctypes.data, None if b2 is None else b2.ctypes.data)
     P._keep = (b13, b2)  # the arrays the pointers refer to live as long as P
     return P
+
+
+def route(logits, K):
+    """Top-K experts (descending logit, ties to the lower id) and their
+    softmax weights renormalised over the K chosen, for (T, E) logits stored
+    as fp32 or bf16 bits."""
+    logits = _storage(logits)
+    T, E = logits.shape
+    ids = np.zeros((T, K), np.int32)
+    w = np.zeros((T, K), np.float64)
+    rc = lib().orc_route(_vptr(logits), _dtype_code(logits), T, E, K, _ptr(ids, ctypes.c_int32),
+                         _ptr(w, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("K outside [1, E]")
+    return ids, w
 
 
 def align_capacity(T, K, E, bm):

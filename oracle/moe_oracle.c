@@ -438,6 +438,53 @@ void orc_combine(const float* y, const int32_t* inv_perm, int T, int K, int H, d
 }
 
 /* ------------------------------------------------------------------ */
+/* Router                                                              */
+/* ------------------------------------------------------------------ */
+
+/* Top-K routing of T tokens over E experts from their router logits
+ * (logit_dtype ORC_F32 or ORC_BF16, (T, E) row-major): ids[t, 0..K-1] are
+ * the experts of the K largest logits in descending order, an equal logit
+ * going to the lower expert id; weights[t, k] is the softmax over the
+ * experts, renormalised over the K chosen ones, which equals the softmax
+ * over the K chosen logits alone:
+ *   w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0).
+ * Source: "MOE Bmm1 Fused Gather", init_routing_data (topk with
+ * apply_softmax over the router logits, whose histogram feeds the ragged
+ * metadata).  The softmax is monotone, so ranking the logits ranks the
+ * probabilities; ranking the logits keeps the choice exact.  Computed in
+ * fp64.  Returns 0, or -1 when K is outside [1, E]. */
+int orc_route(const void* logits, int logit_dtype, int T, int E, int K, int32_t* ids,
+              double* weights) {
+    if (K < 1 || K > E) return -1;
+    char* taken = (char*)malloc((size_t)E);
+    double* v = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int t = 0; t < T; ++t) {
+        memset(taken, 0, (size_t)E);
+        for (int k = 0; k < K; ++k) {
+            int best = -1;
+            double bv = 0.0;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                double l = load_act(logits, logit_dtype, (size_t)t * E + e);
+                if (best < 0 || l > bv) { /* strictly larger: ties keep the lower id */
+                    best = e;
+                    bv = l;
+                }
+            }
+            taken[best] = 1;
+            ids[(size_t)t * K + k] = best;
+            v[k] = bv;
+        }
+        double sum = 0.0;
+        for (int k = 0; k < K; ++k) sum += exp(v[k] - v[0]);
+        for (int k = 0; k < K; ++k) weights[(size_t)t * K + k] = exp(v[k] - v[0]) / sum;
+    }
+    free(taken);
+    free(v);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* Align                                                               */
 /* ------------------------------------------------------------------ */
 

@@ -619,6 +619,53 @@ def pin_interleaved_gate_up():
     assert not np.array_equal(a, oracle.forward(P2, *args, inter, w2))
 
 
+# ---------------------------------------------------------------- router pins
+
+def pin_route_vs_library():
+    """ids: numpy's stable argsort of the negated logits, first K (ties to
+    the lower id); weights: scipy's softmax over all E experts, taken at the
+    chosen ids and renormalised (a different computation from the oracle's
+    softmax over the K chosen logits)."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(8)
+    for T, E, K in ((37, 8, 2), (20, 256, 8), (5, 3, 3), (9, 1, 1)):
+        logits = rng.standard_normal((T, E)).astype(np.float32)
+        ids, w = oracle.route(logits, K)
+        ref_ids = np.argsort(-logits, axis=1, kind="stable")[:, :K]
+        assert np.array_equal(ids, ref_ids)
+        p = softmax(logits.astype(np.float64), axis=1)
+        pk = np.take_along_axis(p, ref_ids, 1)
+        assert np.allclose(w, pk / pk.sum(1, keepdims=True), rtol=1e-12, atol=0)
+
+
+def pin_route_ties_and_bf16():
+    """Equal logits go to the lower expert id; bf16 logits are ranked at
+    their stored values (two logits that round to the same bf16 tie)."""
+    logits = np.array([[0.5, 2.0, 2.0, -1.0, 2.0],
+                       [1.0, 1.0, 1.0, 1.0, 1.0]], np.float32)
+    ids, w = oracle.route(logits, 3)
+    assert ids.tolist() == [[1, 2, 4], [0, 1, 2]]
+    assert np.allclose(w, 1.0 / 3.0, rtol=1e-15)
+    b = torch.tensor([[1.0, 1.001, 0.5]], dtype=torch.float32).to(torch.bfloat16)
+    assert float(b[0, 0]) == float(b[0, 1])  # 1.001 rounds to 1.0 in bf16
+    ids, w = oracle.route(np_store(b), 2)
+    assert ids.tolist() == [[0, 1]] and np.allclose(w, 0.5, rtol=1e-15)
+
+
+def pin_route_matches_input_generator():
+    """Without ties, the generator's route (softmax over all experts in
+    fp32, stable top-k on the probabilities, renormalise) picks the same
+    experts and, within fp32 rounding, the same weights."""
+    cfg = gen.MoEConfig("route", 64, 8, 8, 32, 4, "f32", "zipf")
+    logits = gen.router_logits(cfg, 3)
+    ids, w = oracle.route(logits.numpy(), cfg.K)
+    gi, gw = gen.route(logits, cfg.K)
+    assert np.array_equal(ids, gi.numpy())
+    assert np.allclose(w, gw.numpy(), rtol=2e-6, atol=0)
+
+
+ROUTE_PINS = [pin_route_vs_library, pin_route_ties_and_bf16, pin_route_matches_input_generator]
+
 SWIGLU_PINS = [pin_swiglu_clamp_closed_forms, pin_swiglu_bias_is_a_ones_column,
                pin_w2_bias_closed_form, pin_interleaved_gate_up]
 

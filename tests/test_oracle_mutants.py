@@ -55,6 +55,10 @@ MUTANTS = [
     ("interleaved_gate_row_wrong", "return p->gate_up_interleaved ? 2 * j : j;",
      "return p->gate_up_interleaved ? 2 * j + 1 : j;"),
     ("w2_bias_dropped", " + (p->w2_bias ? (double)p->w2_bias[(size_t)e * p->H + c] : 0.0)", ""),
+    ("route_ties_to_higher_id", "if (best < 0 || l > bv) {", "if (best < 0 || l >= bv) {"),
+    ("route_softmax_over_first_only", "for (int k = 0; k < K; ++k) sum += exp(v[k] - v[0]);",
+     "for (int k = 0; k < K; ++k) sum += exp(v[0] - v[0]);"),
+    ("route_keeps_taken", "if (taken[e]) continue;", "if (0) continue;"),
     ("shard_other_slots_keep_slot", "        inv_perm[i] = -1;\n", "        inv_perm[i] = 0;\n"),
     ("shard_weight_index_global", "e -= p->expert_base; /* index into this shard's weights */",
      "e = e % shard_size(p);"),
@@ -62,7 +66,7 @@ MUTANTS = [
 
 ALL_PINS = pins.FORMAT_PINS + [pins.pin_align_rejects_bad_id, pins.pin_align_invariants] + [
     (lambda c=c: pins.pin_align_vs_stable_argsort(*c)) for c in pins.ALIGN_CASES[:7]
-] + pins.FFN_PINS + pins.SHARD_PINS + pins.SWIGLU_PINS
+] + pins.FFN_PINS + pins.SHARD_PINS + pins.SWIGLU_PINS + pins.ROUTE_PINS
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])

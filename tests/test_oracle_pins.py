@@ -36,3 +36,8 @@ def test_shard_pin(pin):
 @pytest.mark.parametrize("pin", pins.SWIGLU_PINS, ids=lambda f: f.__name__)
 def test_swiglu_pin(pin):
     pin()
+
+
+@pytest.mark.parametrize("pin", pins.ROUTE_PINS, ids=lambda f: f.__name__)
+def test_route_pin(pin):
+    pin()
