@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import dataclasses
 import hashlib
 import io
 import json
@@ -51,6 +52,15 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--block-m", type=int, default=0,
                     help="align block (token tile) of the GEMMs; 0 picks it from the problem")
+    ap.add_argument("--shrink", type=int, default=1,
+                    help="divide the workload's tokens and experts by this factor (same tokens "
+                         "per expert; for profiling captures that must stay small)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the 48-point batch sweep of one expert shard of the GPT-OSS-shaped "
+                         "layer (lowp_oai), one JSON line with a 'sweep' list")
+    ap.add_argument("--ep-shards", type=int, default=8,
+                    help="expert shards of the layer in the sweep (one is timed)")
+    ap.add_argument("--ep-rank", type=int, default=0, help="the shard the sweep times")
     return ap.parse_args()
 
 
@@ -236,8 +246,14 @@ def cpu_oracle_rate(cfg, inp_cpu, seconds):
     threads = len(os.sched_getaffinity(0))
     oracle.lib()
     mx = cfg.dtype == "mxfp4"
+    act = {}
+    if cfg.activation == "swiglu_oai":
+        act = dict(activation=oracle.ACT_SWIGLU_CLAMP, swiglu_alpha=inp_cpu.swiglu_alpha,
+                   swiglu_limit=inp_cpu.swiglu_limit, gate_up_interleaved=True,
+                   w13_bias=inp_cpu.w13_bias.numpy(), w2_bias=inp_cpu.w2_bias.numpy())
     P = oracle.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, gen.to_numpy_storage(inp_cpu.x[:1]),
-                            gen.to_numpy_storage(inp_cpu.w13[:1]), quantize_x=mx, h_e4m3=mx)
+                            gen.to_numpy_storage(inp_cpu.w13[:1]), quantize_x=mx, h_e4m3=mx,
+                            h_scale=inp_cpu.h_scale, **act)
     args = (gen.to_numpy_storage(inp_cpu.x), inp_cpu.topk_ids.numpy(),
             inp_cpu.topk_weights.numpy(), gen.to_numpy_storage(inp_cpu.w13),
             gen.to_numpy_storage(inp_cpu.w2))
@@ -284,23 +300,20 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, ws, rank, local):
-    import mixture_experts_grouped_02_gb300 as moe
-    from mixture_experts_grouped_02_gb300 import _abi
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    moe._abi.lib()
-    cfg = gen.config(args.config)
-    # weights are the same model on every rank; each rank routes its own batch
-    inp = gen.generate(cfg, seed=0, device=dev)
-    if rank > 0:
-        seed = rank_batch_seed(rank)
-        inp.x = gen.draw_x(cfg, seed=seed, device=dev)
-        inp.topk_ids, inp.topk_weights = gen.route(gen.router_logits(cfg, seed, dev), cfg.K)
+def build_stages(moe, _abi, cfg, inp, dev, block_m=0, shard=None):
+    """Problem, workspace, packed weights and the exact launches moe_forward
+    makes, one C-ABI call per stage.  shard = (expert_base, local_experts):
+    inp's weights hold those experts only."""
     mx = cfg.dtype == "mxfp4"
+    act = {}
+    if cfg.activation == "swiglu_oai":  # GPT-OSS expert FFN
+        act = dict(activation=moe.MOE_ACT_SWIGLU_CLAMP, swiglu_alpha=inp.swiglu_alpha,
+                   swiglu_limit=inp.swiglu_limit, gate_up_interleaved=True,
+                   w13_bias=inp.w13_bias, w2_bias=inp.w2_bias)
+    base, L = shard if shard is not None else (0, 0)
     p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "bf16" if mx else cfg.dtype,
-                         "mxfp4" if mx else None, block_m=args.block_m)
+                         "mxfp4" if mx else None, block_m=block_m, h_scale=inp.h_scale,
+                         expert_base=base, local_experts=L, **act)
     wsp = moe.Workspace(p, dev)
     part = lambda i, dt=torch.int32: wsp.part(i, dt)
     st = wsp.status
@@ -315,20 +328,20 @@ def run_ours(args, ws, rank, local):
     # model weights as the kernels read them (mxfp4: packed once, at load time)
     w13, s13, w2, s2 = inp.w13, None, inp.w2, None
     if mx:
-        w13, s13 = moe.pack_mx(inp.w13, inp.w13_scale, 2)
+        w13, s13 = moe.pack_mx(inp.w13, inp.w13_scale, 2, interleaved=inp.interleaved)
         w2, s2 = moe.pack_mx(inp.w2, inp.w2_scale, 1)
     splits = moe.moe_gemm2_default_splits(p)
     bm = moe.moe_resolve_block_m(p)  # the align block the GEMMs of this problem tile by
-    cap = moe.moe_align_capacity(cfg.T, cfg.K, cfg.E, bm)
+    cap = moe.moe_align_capacity(cfg.T, cfg.K, L if L else cfg.E, bm)
     out = torch.empty((cfg.T, cfg.H), dtype=inp.x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
     st.zero_()
 
     # exactly the launches moe_forward makes, one C-ABI call per stage
     stages = []
-    stages.append(("align", lambda: moe.moe_align(
-        inp.topk_ids, cfg.T, cfg.K, cfg.E, bm, counts, offs, poffs, sorted_ids, inv, binfo, nblk,
-        st, stream)))
+    stages.append(("align", lambda: moe.moe_align_local(
+        inp.topk_ids, cfg.T, cfg.K, cfg.E, base, L if L else cfg.E, bm, counts, offs, poffs,
+        sorted_ids, inv, binfo, nblk, st, stream)))
     if mx:
         stages.append(("quantize_gather_x", lambda: moe.moe_quantize_gather_x_fp8(
             inp.x, _abi.MOE_BF16, cfg.T, cfg.H, cfg.K, inv, xq, xs, st, stream)))
@@ -343,6 +356,31 @@ def run_ours(args, ws, rank, local):
         p, h, w2, s2, inp.topk_weights, sorted_ids, binfo, nblk, y, splits, st, stream)))
     stages.append(("combine", lambda: moe.moe_combine(
         y, splits, cap, inv, cfg.T, cfg.K, cfg.H, p.act, out, st, stream)))
+    return stages, p, wsp, (w13, s13, w2, s2), out, bm, stream
+
+
+def run_ours(args, ws, rank, local):
+    import mixture_experts_grouped_02_gb300 as moe
+    from mixture_experts_grouped_02_gb300 import _abi
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe._abi.lib()
+    cfg = gen.config(args.config)
+    if args.shrink > 1:
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}/{args.shrink}",
+                                  T=max(1, cfg.T // args.shrink), E=max(1, cfg.E // args.shrink))
+    # weights are the same model on every rank; each rank routes its own batch
+    inp = gen.generate(cfg, seed=0, device=dev)
+    if rank > 0:
+        seed = rank_batch_seed(rank)
+        inp.x = gen.draw_x(cfg, seed=seed, device=dev)
+        inp.topk_ids, inp.topk_weights = gen.route(gen.router_logits(cfg, seed, dev), cfg.K)
+    stages, p, wsp, (w13, s13, w2, s2), out, bm, stream = build_stages(
+        moe, _abi, cfg, inp, dev, args.block_m)
+    st = wsp.status
+    mx = cfg.dtype == "mxfp4"
+    splits = moe.moe_gemm2_default_splits(p)
     names = [n for n, _ in stages]
 
     def step(ev=None):
@@ -475,9 +513,92 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def sweep_batch_sizes(E: int, K: int):
+    """The batch sizes of the "MOE Bmm1 Fused Gather" benchmark
+    (get_batch_sizes): 48 rows-per-expert counts from 4 to 992 in steps that
+    widen with the size, times E / K."""
+    bpe = [b for k in range(8) for b in range(2 ** (2 + k), 2 ** (3 + k), min(2 ** k, 32))]
+    return [b * E // K for b in bpe]
+
+
+def run_sweep(args, rank, local):
+    """One expert shard (E / ep_shards local experts) of the GPT-OSS-shaped
+    layer over the 48 batch sizes: the whole path per batch (tokens routed
+    to other shards are skipped), timed like the main benchmark."""
+    import mixture_experts_grouped_02_gb300 as moe
+    from mixture_experts_grouped_02_gb300 import _abi
+
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe._abi.lib()
+    cfg0 = gen.config("lowp_oai")
+    L = cfg0.E // args.ep_shards
+    base = args.ep_rank * L
+    experts = range(base, base + L)
+    w13, w2, s13, s2 = gen.draw_weights(cfg0, seed=0, device=dev, experts=experts)
+    full = gen.MoEInputs(cfg0, None, None, None, None, None)  # biases and scalars only
+    gen.draw_swiglu_oai(full, seed=0, device=dev)
+    hbm_gbs, _, peak_kind = peaks()
+    points = []
+    for T in sweep_batch_sizes(cfg0.E, cfg0.K):
+        cfg = cfg0.with_tokens(T)
+        ids, w = gen.route(gen.router_logits(cfg, 0, dev), cfg.K)
+        inp = gen.MoEInputs(cfg, gen.draw_x(cfg, 0, dev), w13, w2, ids, w, s13, s2,
+                            full.w13_bias[base:base + L].contiguous(),
+                            full.w2_bias[base:base + L].contiguous(), full.swiglu_alpha,
+                            full.swiglu_limit, full.h_scale)
+        stages, p, wsp, _, _, bm, stream = build_stages(moe, _abi, cfg, inp, dev, 0, (base, L))
+        steps = max(5, min(args.steps, 50))
+        for _ in range(3):
+            for _, f in stages:
+                f()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+              for _ in range(steps)]
+        torch.cuda.synchronize(dev)
+        for i in range(steps):
+            ev[i][0].record(stream)
+            for j, (_, f) in enumerate(stages):
+                f()
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        if moe.moe_get_device_status(wsp.status, stream) != 0:
+            raise RuntimeError(f"device status at T={T}")
+        names = [n for n, _ in stages]
+        ms = {n: statistics.median(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
+              for j, n in enumerate(names)}
+        total = sum(ms.values())
+        flat = ids.flatten().long()
+        local_n = int(((flat >= base) & (flat < base + L)).sum())
+        active = int((torch.bincount(flat[(flat >= base) & (flat < base + L)] - base,
+                                     minlength=L) > 0).sum())
+        w13_bytes = active * (inp.w13[0].numel() + inp.w13_scale[0].numel())
+        g1 = ms["gemm_gate_up"] * 1e-3
+        points.append({"T": T, "local_assignments": local_n, "active_local_experts": active,
+                       "ms_per_step": total, "tokens_per_s": T / (total * 1e-3),
+                       "gemm_gate_up_ms": ms["gemm_gate_up"],
+                       "gemm_gate_up_tflops": 4 * local_n * cfg.H * cfg.I / g1 / 1e12,
+                       "gemm_gate_up_weight_gbs": w13_bytes / g1 / 1e9,
+                       "gemm_gate_up_weight_hbm_frac": w13_bytes / g1 / 1e9 / hbm_gbs,
+                       "stage_ms": ms})
+        del stages, p, wsp, inp
+        torch.cuda.empty_cache()
+    line = {"metric": METRIC, "unit": "tokens/s", "impl": "ours", "n_gpus": 1,
+            "data": "synthetic", "dtype": "e4m3 x mxfp4 (fp32 acc)",
+            "config": {"workload": "lowp_oai batch sweep", "H": cfg0.H, "I": cfg0.I,
+                       "E": cfg0.E, "top_k": cfg0.K, "ep_shards": args.ep_shards,
+                       "local_experts": [base, base + L], "peak": f"{peak_kind} HBM copy"},
+            "sweep": points}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
+    if args.sweep:
+        run_sweep(args, rank, local)
+        return
     if args.impl == "reference":
         run_reference(args, ws, rank)  # rank 0 alone; no process group needed
     else:

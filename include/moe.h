@@ -58,15 +58,20 @@ typedef enum {
                      /* nibble, plus one e8m0 scale byte per 32 K elements     */
 } moe_dtype_t;
 
+/* Activation of the first GEMM's epilogue (moe_problem_t.activation). */
+typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SWIGLU_CLAMP = 1 } moe_activation_t;
+
 /* One MoE layer.  T tokens of width H, E experts with intermediate size I,
  * top-K routing.
  *   act    : dtype of x and out: MOE_F32 or MOE_BF16.
  *   weight : dtype of w13/w2: equal to act, or MOE_E2M1_MX (then act must
  *            be MOE_BF16; x is cast to e4m3 with one fp32 scale per row and
  *            the hidden activation is stored as e4m3(a / h_scale)).
- *   block_m: rows per alignment block, 0 = automatic: 256 (the GEMMs then
- *            run on CTA pairs) when bf16/fp32 experts receive at least 256
- *            rows on average (T*K >= 256*E), else 128.
+ *   block_m: rows per alignment block (16, 32, 64, 128 or 256; MX weights:
+ *            128), 0 = automatic: 256 when bf16/fp32 experts receive at
+ *            least 256 rows on average (T*K >= 256*E), else 128.  The
+ *            bf16/fp32 GEMMs take one block as the N side of a tile and
+ *            spend MMA work only on its valid rows (rounded up to 16).
  *   h_scale: scale of the e4m3 hidden activation (MX weights only; 0 => 1).
  *   expert_base, local_experts: expert-parallel shard (local_experts = 0:
  *            no sharding).  The layer's experts [expert_base,
@@ -77,7 +82,21 @@ typedef enum {
  *            output and the shards' outputs sum to the unsharded one.
  *            Source: "MOE Bmm1 Fused Gather", init_routing_data (a shard
  *            keeps the histogram of its local experts; experts split into
- *            equal contiguous ranges by make_expt_dict_uniform). */
+ *            equal contiguous ranges by make_expt_dict_uniform).
+ *   activation, swiglu_alpha, swiglu_limit, gate_up_interleaved, w13_bias,
+ *   w2_bias: the expert FFN's activation and biases (L = experts held).
+ *            MOE_ACT_SILU: a = SiLU(g) * u, the plain SwiGLU of
+ *            "factor_moe_fused_gemm.cu".  MOE_ACT_SWIGLU_CLAMP: GPT-OSS's
+ *            variant from "MOE Bmm1 Fused Gather" (_swiglu_step1/2): g =
+ *            min(g, limit), u = clamp(u, -limit, limit),
+ *            a = g * sigmoid(alpha * g) * (u + 1).  g and u are the
+ *            accumulators plus w13_bias (per expert and w13 row, that page's
+ *            apply_bias_and_scale); y = W2 a + w2_bias before the routing
+ *            weight.  Either bias may be NULL (zero) and goes with either
+ *            activation.  gate_up_interleaved: w13 (and w13_bias) hold gate
+ *            and up in alternating rows, that page's layout, instead of the
+ *            two halves; for MX weights pass the same flag to
+ *            moe_pack_mx_weights, whose packed form is always in halves. */
 typedef struct {
     int T, H, I, E, K;
     int act;
@@ -86,6 +105,12 @@ typedef struct {
     float h_scale;
     int expert_base;
     int local_experts;
+    int activation;           /* moe_activation_t                          */
+    float swiglu_alpha;       /* MOE_ACT_SWIGLU_CLAMP: sigmoid slope       */
+    float swiglu_limit;       /* MOE_ACT_SWIGLU_CLAMP: clamp, > 0          */
+    int gate_up_interleaved;  /* w13 rows 2j = gate j, 2j+1 = up j         */
+    const float* w13_bias;    /* device (L, 2I) fp32 in w13's row order    */
+    const float* w2_bias;     /* device (L, H) fp32                        */
 } moe_problem_t;
 
 /* Sub-buffers of the moe_forward workspace (byte offsets, see
@@ -100,7 +125,7 @@ typedef enum {
     MOE_WS_BLOCK_INFO = 6,     /* int32[cap/block_m][4]                     */
     MOE_WS_NUM_BLOCKS = 7,     /* int32[1]                                  */
     MOE_WS_XQ = 8,             /* A rows in sorted order [cap][H]: e4m3     */
-                               /* (MX weights) or act (256-row blocks)      */
+                               /* (MX weights) or act rows                  */
     MOE_WS_X_SCALE = 9,        /* fp32[T]      (MX weights only)            */
     MOE_WS_H = 10,             /* act or e4m3 [cap][I]                      */
     MOE_WS_Y = 11,             /* fp32[splits][cap][H]                      */
@@ -179,6 +204,27 @@ int moe_align_local(const int32_t* topk_ids, int T, int K, int E, int expert_bas
                     int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
                     int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream);
 
+/* ---- routing + align ------------------------------------------------------
+ * The router step before the path, folded into align.  Source: "MOE Bmm1
+ * Fused Gather", init_routing_data: topk(logits, k, apply_softmax) over the
+ * router logits, whose expert histogram feeds the ragged metadata.
+ *   logits        (T, E) logit_dtype (MOE_F32 or MOE_BF16), row-major
+ *   topk_ids      (T, K) int32 out: the experts of the K largest logits of
+ *                 each token in descending order, an equal logit going to
+ *                 the lower expert id (compared at the logits' own values)
+ *   topk_weights  (T, K) fp32 out: softmax over the E experts renormalised
+ *                 over the K chosen = softmax over the K chosen logits
+ * then moe_align_local over those ids (all other outputs as there).  Up to
+ * 1024 tokens the align kernel routes the batch itself (one launch); larger
+ * batches are routed by a kernel of a warp per token first.  K <= 32,
+ * E <= 1024.  A token whose logits are NaN where a choice is made records
+ * MOE_ERR_DEVICE_BAD_ID. */
+int moe_route_align(const void* logits, int logit_dtype, int T, int E, int K, int expert_base,
+                    int local_experts, int block_m, int32_t* topk_ids, float* topk_weights,
+                    int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                    int32_t* sorted_ids, int32_t* inv_perm, int32_t* block_info,
+                    int32_t* num_blocks, int32_t* dev_status, void* stream);
+
 /* ---- mxfp4 weight packing (once, when the model is loaded) -----------------
  * Source: "MOE Bmm1 Fused Gather" -- its matmul takes the e2m1 weights in a
  * pre-shuffled value layout and the e8m0 scales in a swizzled scale layout,
@@ -199,11 +245,15 @@ int moe_align_local(const int32_t* topk_ids, int T, int K, int E, int expert_bas
  * moe_mx_packed_bytes returns the total bytes (0 on bad arguments) and the
  * two parts; K must be a multiple of 32.  moe_pack_mx_weights writes the
  * packed form on `stream` (all pointers device memory; the packed values
- * must be 32-byte and the images 16-byte aligned to be used). */
+ * must be 32-byte and the images 16-byte aligned to be used).  interleaved
+ * = 1 (sections = 2 only): the natural rows hold the two sections
+ * alternately (row 2j of section 0, row 2j+1 of section 1, GPT-OSS's gate /
+ * linear layout); the packed form is the same as for the halves. */
 size_t moe_mx_packed_bytes(int E, int R, int K, int sections, size_t* value_bytes,
                            size_t* scale_bytes);
 int moe_pack_mx_weights(const uint8_t* w, const uint8_t* w_scale, int E, int R, int K,
-                        int sections, uint8_t* w_packed, uint8_t* scale_packed, void* stream);
+                        int sections, int interleaved, uint8_t* w_packed, uint8_t* scale_packed,
+                        void* stream);
 
 /* ---- fp8 activation step ------------------------------------------------
  * Source: "MOE Bmm1 Fused Gather" (Triton Gluon example), pack_e4m3x2
@@ -224,12 +274,15 @@ int moe_quantize_gather_x_fp8(const void* x, int x_dtype, int T, int H, int K,
                               const int32_t* inv_perm, uint8_t* xq_sorted, float* row_scale,
                               int32_t* dev_status, void* stream);
 
-/* ---- gather step (256-row blocks) -------------------------------------------
+/* ---- gather step (bf16/fp32 weights) ---------------------------------------
+ * Source: "MOE Bmm1 Fused Gather", load_activations (token rows gathered by
+ * index), done as its own pass.
  * Token rows to sorted slots: x_sorted[inv_perm[t*K + k], :] = x[t, :] for
- * every choice of every token (rows of padding slots are not written); x
- * (T, H) in dtype (MOE_BF16 / MOE_F32), x_sorted (cap, H), inv_perm from
- * moe_align.  The gate/up GEMM on CTA pairs (block_m 256) reads its token rows
- * in this sorted form.  Skipped when *dev_status != 0. */
+ * every choice of every token (rows of padding slots are not written; a
+ * negative inv_perm entry, another shard's slot, is skipped); x (T, H) in
+ * dtype (MOE_BF16 / MOE_F32), x_sorted (cap, H), inv_perm from moe_align.
+ * The bf16/fp32 gate/up GEMM reads its token rows in this sorted form.
+ * Skipped when *dev_status != 0. */
 int moe_gather_rows(const void* x, int dtype, int T, int H, int K, const int32_t* inv_perm,
                     void* x_sorted, int32_t* dev_status, void* stream);
 
@@ -242,9 +295,8 @@ int moe_gather_rows(const void* x, int dtype, int T, int H, int K, const int32_t
  * For every slot s of a block b < *num_blocks with i = sorted_ids[s] < N_a
  * and e = block_info[b].expert:
  *   h[s, j] = SiLU(W13[e, j, :] . x[i / K, :]) * (W13[e, I + j, :] . x[i / K, :])
- * x    (T, H) act, gathered by the kernel; with 256-row blocks (CTA pairs)
- *      the rows in sorted order (cap, H) as written by moe_gather_rows; for
- *      MX weights, the e4m3 codes in sorted order (cap, H) as written by
+ * x    the token rows in sorted order (cap, H): act rows as written by
+ *      moe_gather_rows, or for MX weights the e4m3 codes as written by
  *      moe_quantize_gather_x_fp8, with x_row_scale (T) fp32
  * w13  (E, 2I, H) weight dtype (MX: packed values + scale images of
  *      moe_pack_mx_weights with R = 2I, K = H, sections = 2)
@@ -252,8 +304,7 @@ int moe_gather_rows(const void* x, int dtype, int T, int H, int K, const int32_t
  *      are not written.  H and I must be multiples of 64 (32 for MOE_F32 and
  *      for MX weights).
  * sorted_ids/block_info/num_blocks as written by moe_align with the same
- * block_m (128, or 256 for the CTA-pair GEMMs of bf16/fp32 weights).
- * dev_status may be NULL. */
+ * block_m (MX weights: 128).  dev_status may be NULL. */
 int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_scale,
                    const void* w13, const uint8_t* w13_scale, const int32_t* sorted_ids,
                    const int32_t* block_info, const int32_t* num_blocks, void* h,
@@ -283,14 +334,15 @@ int moe_gemm2_weighted(const moe_problem_t* p, const void* h, const void* w2,
  * weighted_scatter_add_kernel of "factor_moe_fused_gemm.cu", done here as a
  * deterministic per-token reduction instead of atomics:
  *   out[t, c] = sum_{k < K} sum_{q < k_splits} y[q, inv_perm[t*K + k], c]
- * summed in fp32 in k order, rounded once to out_dtype (MOE_F32/MOE_BF16).
+ * summed in fp32 in k order, rounded once to out_dtype (MOE_F32/MOE_BF16);
+ * a negative inv_perm entry (another shard's slot) adds nothing.
  * y (k_splits, cap, H) fp32; inv_perm (T*K); out (T, H). */
 int moe_combine(const float* y, int k_splits, size_t cap, const int32_t* inv_perm, int T, int K,
                 int H, int out_dtype, void* out, int32_t* dev_status, void* stream);
 
 /* ---- the whole forward -----------------------------------------------------
- * Runs align -> [fp8 step with the gather (MX) | gather (256-row blocks)]
- * -> GEMM1 -> GEMM2 -> combine on
+ * Runs align -> [fp8 step with the gather (MX) | gather] -> GEMM1 -> GEMM2
+ * -> combine on
  * `stream`, with every intermediate in `workspace` (device memory of at
  * least moe_workspace_size(p) bytes, 256-byte aligned, owned by the caller,
  * reusable across calls but not shared by calls in flight at once).

@@ -11,17 +11,20 @@ from __future__ import annotations
 import torch
 
 from . import _abi
-from ._abi import (MOE_BF16, MOE_E2M1_MX, MOE_E4M3, MOE_F32, MoEError, Problem, moe_abi_version,
+from ._abi import (MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP, MOE_BF16, MOE_E2M1_MX, MOE_E4M3, MOE_F32,
+                   MoEError, Problem, moe_abi_version,
                    moe_align, moe_align_capacity, moe_align_local, moe_combine, moe_forward,
+                   moe_route_align,
                    moe_forward_noalloc, moe_gather_rows, moe_gemm1_silu, moe_gemm2_default_splits,
                    moe_gemm2_weighted, moe_get_device_status, moe_mx_packed_bytes,
                    moe_pack_mx_weights, moe_quantize_gather_x_fp8, moe_quantize_x_fp8,
                    moe_resolve_block_m, moe_workspace_offsets, moe_workspace_size)
 
-__all__ = ["MoEError", "Problem", "make_problem", "dtype_code", "align", "Workspace", "forward",
+__all__ = ["MOE_ACT_SILU", "MOE_ACT_SWIGLU_CLAMP", "MoEError", "Problem", "make_problem", "dtype_code", "align", "Workspace", "forward",
            "pack_mx", "moe_forward_noalloc", "moe_mx_packed_bytes", "moe_pack_mx_weights",
            "moe_quantize_gather_x_fp8", "moe_gather_rows",
            "moe_abi_version", "moe_align", "moe_align_capacity", "moe_align_local",
+           "moe_route_align", "route_align",
            "moe_combine", "moe_forward",
            "moe_gemm1_silu", "moe_gemm2_default_splits", "moe_gemm2_weighted",
            "moe_get_device_status", "moe_quantize_x_fp8", "moe_resolve_block_m",
@@ -39,13 +42,27 @@ def dtype_code(dt) -> int:
 
 
 def make_problem(T, H, I, E, K, act="bf16", weight=None, block_m=0, h_scale=1.0,
-                 expert_base=0, local_experts=0) -> Problem:
+                 expert_base=0, local_experts=0, activation=MOE_ACT_SILU, swiglu_alpha=1.0,
+                 swiglu_limit=float("inf"), gate_up_interleaved=False, w13_bias=None,
+                 w2_bias=None) -> Problem:
     """local_experts > 0: an expert-parallel shard holding experts
     [expert_base, expert_base + local_experts) of E; its weights hold those
-    experts only."""
+    experts only.  activation MOE_ACT_SWIGLU_CLAMP selects the clamped
+    SwiGLU (swiglu_alpha, swiglu_limit); gate_up_interleaved: w13 rows
+    alternate gate and up; w13_bias (experts, 2I) / w2_bias (experts, H):
+    fp32 device tensors, kept alive by the returned problem."""
     a = dtype_code(act)
     w = a if weight is None else dtype_code(weight)
-    return Problem(T, H, I, E, K, a, w, block_m, h_scale, expert_base, local_experts)
+    for b in (w13_bias, w2_bias):
+        if b is not None and (b.dtype != torch.float32 or not b.is_contiguous()):
+            raise ValueError("biases are contiguous fp32 device tensors")
+    lim = swiglu_limit if activation == MOE_ACT_SWIGLU_CLAMP else 0.0
+    P = Problem(T, H, I, E, K, a, w, block_m, h_scale, expert_base, local_experts, activation,
+                swiglu_alpha, lim, int(gate_up_interleaved),
+                None if w13_bias is None else w13_bias.data_ptr(),
+                None if w2_bias is None else w2_bias.data_ptr())
+    P._keep = (w13_bias, w2_bias)
+    return P
 
 
 def align(topk_ids: torch.Tensor, E: int, block_m: int = 128, dev_status=None, stream=None,
@@ -68,7 +85,32 @@ def align(topk_ids: torch.Tensor, E: int, block_m: int = 128, dev_status=None, s
     return out
 
 
-def pack_mx(w: torch.Tensor, w_scale: torch.Tensor, sections: int, stream=None):
+def route_align(logits: torch.Tensor, K: int, block_m: int = 128, dev_status=None, stream=None,
+                expert_base: int = 0, local_experts: int = 0):
+    """moe_route_align on (T, E) router logits (fp32 or bf16): returns the
+    top-K ids and weights and the align outputs as a dict of device
+    tensors."""
+    T, E = logits.shape
+    L = local_experts if local_experts > 0 else E
+    cap = moe_align_capacity(T, K, L, block_m)
+    dev = logits.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = dict(topk_ids=torch.empty((T, K), **i32),
+               topk_weights=torch.empty((T, K), dtype=torch.float32, device=dev),
+               counts=torch.empty(L, **i32), offsets=torch.empty(L + 1, **i32),
+               padded_offsets=torch.empty(L + 1, **i32), sorted_ids=torch.empty(cap, **i32),
+               inv_perm=torch.empty(T * K, **i32),
+               block_info=torch.empty((cap // block_m, 4), **i32),
+               num_blocks=torch.empty(1, **i32))
+    moe_route_align(logits.contiguous(), dtype_code(logits.dtype), T, E, K, expert_base, L,
+                    block_m, out["topk_ids"], out["topk_weights"], out["counts"], out["offsets"],
+                    out["padded_offsets"], out["sorted_ids"], out["inv_perm"],
+                    out["block_info"], out["num_blocks"], dev_status, stream)
+    return out
+
+
+def pack_mx(w: torch.Tensor, w_scale: torch.Tensor, sections: int, stream=None,
+            interleaved: bool = False):
     """Packed (values, scale images) of an mxfp4 weight tensor in natural form
     (E, R, K/2) + (E, R, K/32), as the block-scaled GEMMs read it; done once
     when the model is loaded."""
@@ -79,8 +121,8 @@ def pack_mx(w: torch.Tensor, w_scale: torch.Tensor, sections: int, stream=None):
     vals = torch.empty((E, R, Kp // 2), dtype=torch.uint8, device=w.device)
     imgs = torch.empty(sb, dtype=torch.uint8, device=w.device)
     assert vals.numel() == vb
-    moe_pack_mx_weights(w.contiguous(), w_scale.contiguous(), E, R, K, sections, vals, imgs,
-                        stream)
+    moe_pack_mx_weights(w.contiguous(), w_scale.contiguous(), E, R, K, sections, int(interleaved),
+                        vals, imgs, stream)
     return vals, imgs
 
 
@@ -106,17 +148,19 @@ class Workspace:
 
 def forward(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=None, out=None,
             workspace: Workspace | None = None, weight=None, h_scale=1.0, stream=None,
-            num_experts=None, expert_base=0):
+            num_experts=None, expert_base=0, **activation):
     """out = MoE expert FFN of x routed by (topk_ids, topk_weights).  With
     num_experts given, w13/w2 hold the experts [expert_base, expert_base +
     w13.shape[0]) of num_experts (an expert-parallel shard) and out is this
-    shard's share of the layer output."""
+    shard's share of the layer output.  `activation`: make_problem's
+    activation, swiglu_alpha, swiglu_limit, gate_up_interleaved, w13_bias,
+    w2_bias.  MX weights (weight="mxfp4") come packed by pack_mx."""
     T, H = x.shape
     L, I = w13.shape[0], w13.shape[1] // 2
     E = L if num_experts is None else num_experts
     K = topk_ids.shape[1]
     p = make_problem(T, H, I, E, K, x.dtype, weight, 0, h_scale, expert_base,
-                     0 if num_experts is None else L)
+                     0 if num_experts is None else L, **activation)
     if workspace is None:
         workspace = Workspace(p, x.device)
     if out is None:

@@ -36,9 +36,10 @@ EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_a
            "moe_quantize_x_fp8", "moe_gemm1_silu", "moe_gemm2_weighted", "moe_combine",
            "moe_forward", "moe_forward_noalloc", "moe_get_device_status", "moe_mx_packed_bytes",
            "moe_pack_mx_weights", "moe_quantize_gather_x_fp8", "moe_device_info",
-           "moe_gather_rows", "moe_align_local")
+           "moe_gather_rows", "moe_align_local", "moe_route_align")
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
+MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP = 0, 1
 
 
 class MoEError(RuntimeError):
@@ -52,7 +53,10 @@ class Problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
                 ("E", ctypes.c_int), ("K", ctypes.c_int), ("act", ctypes.c_int),
                 ("weight", ctypes.c_int), ("block_m", ctypes.c_int), ("h_scale", ctypes.c_float),
-                ("expert_base", ctypes.c_int), ("local_experts", ctypes.c_int)]
+                ("expert_base", ctypes.c_int), ("local_experts", ctypes.c_int),
+                ("activation", ctypes.c_int), ("swiglu_alpha", ctypes.c_float),
+                ("swiglu_limit", ctypes.c_float), ("gate_up_interleaved", ctypes.c_int),
+                ("w13_bias", ctypes.c_void_p), ("w2_bias", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -98,6 +102,8 @@ def _declare(L):
     L.moe_workspace_offsets.argtypes = [PP, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     L.moe_align.restype = i32
     L.moe_align.argtypes = [vp, i32, i32, i32, i32] + [vp] * 8 + [vp]
+    L.moe_route_align.restype = i32
+    L.moe_route_align.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32] + [vp] * 9 + [vp, vp]
     L.moe_align_local.restype = i32
     L.moe_align_local.argtypes = [vp, i32, i32, i32, i32, i32, i32] + [vp] * 8 + [vp]
     L.moe_quantize_x_fp8.restype = i32
@@ -123,7 +129,7 @@ def _declare(L):
     L.moe_mx_packed_bytes.restype = sz
     L.moe_mx_packed_bytes.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     L.moe_pack_mx_weights.restype = i32
-    L.moe_pack_mx_weights.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
+    L.moe_pack_mx_weights.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
 
 
 def status_string(status: int) -> str:
@@ -205,6 +211,16 @@ def moe_align_local(topk_ids, T, K, E, expert_base, local_experts, block_m, coun
                                  _stream(stream)), "moe_align_local")
 
 
+def moe_route_align(logits, logit_dtype, T, E, K, expert_base, local_experts, block_m, topk_ids,
+                    topk_weights, counts, offsets, padded_offsets, sorted_ids, inv_perm,
+                    block_info, num_blocks, dev_status=None, stream=None):
+    _check(lib().moe_route_align(_p(logits), logit_dtype, T, E, K, expert_base, local_experts,
+                                 block_m, _p(topk_ids), _p(topk_weights), _p(counts), _p(offsets),
+                                 _p(padded_offsets), _p(sorted_ids), _p(inv_perm),
+                                 _p(block_info), _p(num_blocks), _p(dev_status),
+                                 _stream(stream)), "moe_route_align")
+
+
 def moe_quantize_x_fp8(x, x_dtype, T, H, xq, row_scale, stream=None):
     _check(lib().moe_quantize_x_fp8(_p(x), x_dtype, T, H, _p(xq), _p(row_scale),
                                     _stream(stream)), "moe_quantize_x_fp8")
@@ -270,8 +286,10 @@ def moe_mx_packed_bytes(E, R, K, sections):
     return vb.value, sb.value
 
 
-def moe_pack_mx_weights(w, w_scale, E, R, K, sections, w_packed, scale_packed, stream=None):
-    _check(lib().moe_pack_mx_weights(_p(w), _p(w_scale), E, R, K, sections, _p(w_packed),
+def moe_pack_mx_weights(w, w_scale, E, R, K, sections, interleaved, w_packed, scale_packed,
+                        stream=None):
+    _check(lib().moe_pack_mx_weights(_p(w), _p(w_scale), E, R, K, sections, interleaved,
+                                     _p(w_packed),
                                      _p(scale_packed), _stream(stream)), "moe_pack_mx_weights")
 
 

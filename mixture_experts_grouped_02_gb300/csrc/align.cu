@@ -29,6 +29,10 @@
 // shard of all E experts is the plain align.  Source for the shard: the
 // "MOE Bmm1 Fused Gather" example's init_routing_data, which keeps the
 // histogram of the local experts of one expert shard.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -41,14 +45,86 @@ constexpr int kAlignThreads = kAlignWarps * 32;
 // order: keeps several loads in flight instead of one round trip per batch.
 constexpr int kAlignUnroll = 8;
 
-// ids [base + 32u + lane] for u < kAlignUnroll, -1 at or past `hi`.
+// ids [base + 32u + lane] for u < kAlignUnroll, -1 at or past `hi`.  Plain
+// loads: the ids may have been written by this kernel's routing step.
 __device__ __forceinline__ void load_ids(const int* ids, int base, int hi, int lane,
                                          int (&e)[kAlignUnroll]) {
 #pragma unroll
   for (int u = 0; u < kAlignUnroll; ++u) {
     const int i = base + 32 * u + lane;
-    e[u] = i < hi ? __ldg(ids + i) : -1;
+    e[u] = i < hi ? ids[i] : -1;
   }
+}
+
+// ---------------------------------------------------------------- routing
+// Top-K routing of one token by one warp, from its E router logits: the
+// experts of the K largest logits in descending order (an equal logit goes
+// to the lower expert id) and the softmax over the experts renormalised
+// over the K chosen, which is the softmax over the chosen logits alone.
+// Source: "MOE Bmm1 Fused Gather", init_routing_data (topk with
+// apply_softmax feeding the expert histogram).  Lane l owns experts
+// l, l + 32, ... (E <= 1024); each of the K rounds takes every lane's best
+// untaken expert and a warp arg-max.  A token whose remaining logits all
+// compare false (NaN) records MOE_ERR_DEVICE_BAD_ID.
+__device__ __forceinline__ float logit_at(const RouteArgs& r, long long idx) {
+  if (r.bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(r.logits)[idx]);
+  return reinterpret_cast<const float*>(r.logits)[idx];
+}
+
+__device__ __forceinline__ void route_token(const RouteArgs& r, int t, int lane) {
+  const long long row = static_cast<long long>(t) * r.E;
+  unsigned taken = 0;  // bit i: expert lane + 32 i chosen
+  float my_v = 0.0f;   // lane k keeps the k-th choice
+  int my_id = 0;
+  for (int k = 0; k < r.K; ++k) {
+    float bv = -INFINITY;
+    int bid = 0x7fffffff;
+    for (int i = 0, e = lane; e < r.E; ++i, e += 32) {
+      if ((taken >> i) & 1u) continue;
+      const float l = logit_at(r, row + e);
+      if (bid == 0x7fffffff || l > bv) {  // ids ascend per lane: ties keep the lower
+        if (!(l != l)) {
+          bv = l;
+          bid = e;
+        }
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+      const int oid = __shfl_xor_sync(0xffffffffu, bid, d);
+      if (ov > bv || (ov == bv && oid < bid)) {
+        bv = ov;
+        bid = oid;
+      }
+    }
+    if (bid == 0x7fffffff) {  // nothing left that compares
+      if (lane == 0) report_error(r.status, MOE_ERR_DEVICE_BAD_ID);
+      bid = 0;
+    } else if ((bid & 31) == lane) {
+      taken |= 1u << (bid >> 5);
+    }
+    if (lane == k) {
+      my_v = bv;
+      my_id = bid;
+    }
+  }
+  const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = lane < r.K ? expf(my_v - v0) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+  if (lane < r.K) {
+    r.ids[static_cast<long long>(t) * r.K + lane] = my_id;
+    r.weights[static_cast<long long>(t) * r.K + lane] = ex / sum;
+  }
+}
+
+__global__ void __launch_bounds__(256) route_kernel(const RouteArgs r) {
+  const int lane = threadIdx.x & 31;
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int t = w; t < r.T; t += nw) route_token(r, t, lane);
 }
 
 // Lanes of the warp whose `key` equals this lane's, keys in [0, 2^nbits):
@@ -121,6 +197,10 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
 
   if (tid == 0) s_bad = 0;
   for (int i = tid; i < kAlignWarps * L; i += kAlignThreads) hist[i] = 0;
+  // 0. routing of small batches, in this CTA: a warp per token; the ids it
+  //    writes are read back below after the barrier
+  if (p.route.logits != nullptr)
+    for (int t = warp; t < p.route.T; t += kAlignWarps) route_token(p.route, t, lane);
   __syncthreads();
 
   // chunk of warp w: [w*chunk, min(na, (w+1)*chunk)), chunk a multiple of 32
@@ -261,6 +341,12 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
 
 size_t align_smem_bytes(int L) {
   return sizeof(int) * (static_cast<size_t>(kAlignWarps) * L + (L + 1) + L);
+}
+
+cudaError_t launch_route(const RouteArgs& r, cudaStream_t s) {
+  const int blocks = static_cast<int>(std::min<long long>((r.T + 7) / 8, 152ll * 8));
+  route_kernel<<<blocks, 256, 0, s>>>(r);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s) {

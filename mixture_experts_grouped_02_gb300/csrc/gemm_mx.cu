@@ -92,7 +92,28 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) {
+// Barrier over the 128 epilogue threads (named barrier 1) that also ANDs
+// `pred` across them.
+__device__ __forceinline__ int epilogue_bar_and(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred)
+      : "memory");
+  return r;
+}
+
+// The activation: SiLU(g) * u, or GPT-OSS's clamped SwiGLU ("MOE Bmm1 Fused
+// Gather", _swiglu_step1/2): gate clamped from above at `limit`, linear
+// branch to [-limit, limit], g * sigmoid(alpha g) * (u + 1).
+__device__ __forceinline__ float activate(const Epilogue& ep, float g, float u) {
+  if (ep.act == MOE_ACT_SWIGLU_CLAMP) {
+    g = fminf(g, ep.limit);
+    u = fmaxf(fminf(u, ep.limit), -ep.limit);
+    return g / (1.0f + __expf(-ep.alpha * g)) * (u + 1.0f);
+  }
   return g / (1.0f + __expf(-g)) * u;
 }
 
@@ -118,6 +139,9 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_skip;
   __shared__ volatile int s_abort;
+  // biases of the tile's 192 weight rows (gate/up: 96 gate then 96 up;
+  // down: 192 columns of the w2 bias), one set per accumulator
+  __shared__ float s_bias[2][C::kBN];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -289,26 +313,50 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const int et = threadIdx.x - (C::kMmaWarp + 1) * 32;  // 0..127 over the epilogue warps
+    const bool has_bias = KIND == kMxGateUp ? a.ep.b13 != nullptr : a.ep.b2 != nullptr;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode_tile(tile, num_blocks, a);
       const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
       const int r0 = bi.z, valid = bi.w;
+      if (has_bias) {
+        // this tile's biases, read once; the slot of this accumulator was
+        // last read two tiles ago, before the barrier of the previous tile
+        for (int i = et; i < C::kBN; i += 128) {
+          float b = 0.0f;
+          if constexpr (KIND == kMxGateUp) {
+            const int j = t.nt * C::kHalf + (i % C::kHalf);
+            if (j < a.I)
+              b = a.ep.b13[i < C::kHalf ? gate_bias_index(a.ep, a.I, bi.x, j)
+                                        : up_bias_index(a.ep, a.I, bi.x, j)];
+          } else {
+            const int c = t.nt * C::kBN + i;
+            if (c < a.H && t.split == 0) b = a.ep.b2[static_cast<long long>(bi.x) * a.H + c];
+          }
+          s_bias[acc][i] = b;
+        }
+      }
       const bool row_ok = r < valid;
-      float rs = 0.0f;
+      float rs = 0.0f, wt = 0.0f;
       if (row_ok) {
         const int i = a.sorted_ids[r0 + r];
-        if constexpr (KIND == kMxGateUp)
+        if constexpr (KIND == kMxGateUp) {
           rs = a.x_row_scale[i / a.K];
-        else
-          rs = a.topk_weights[i] * a.h_scale;
+        } else {
+          wt = a.topk_weights[i];
+          rs = wt * a.h_scale;
+        }
       }
       int good = 1;
       if (lane == 0) good = mbar_wait_bounded(smem_u32(&accf_bar[acc]), acc_phase, &s_abort, to);
       good = __shfl_sync(0xffffffffu, good, 0);
+      // the four epilogue warps agree on going on (and see the biases)
+      good = epilogue_bar_and(good);
       if (!good) break;
       tc_fence_after_sync();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::kAccCols;
+      const float* sb = s_bias[acc];
       if constexpr (KIND == kMxGateUp) {
         uint8_t* hq = static_cast<uint8_t*>(a.out) + static_cast<long long>(r0 + r) * a.I;
 #pragma unroll 1
@@ -325,9 +373,13 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
               float o[4];
 #pragma unroll
               for (int w = 0; w < 4; ++w) {
-                const float gg = rs * __uint_as_float(g[4 * v + w]);
-                const float uu = rs * __uint_as_float(u[4 * v + w]);
-                o[w] = __fdiv_rn(silu_mul(gg, uu), a.h_scale);
+                float gg = rs * __uint_as_float(g[4 * v + w]);
+                float uu = rs * __uint_as_float(u[4 * v + w]);
+                if (has_bias) {
+                  gg += sb[c * 32 + 4 * v + w];
+                  uu += sb[C::kHalf + c * 32 + 4 * v + w];
+                }
+                o[w] = __fdiv_rn(activate(a.ep, gg, uu), a.h_scale);
               }
               pk[v] = e4m3x4(o[0], o[1], o[2], o[3]);
             }
@@ -347,10 +399,16 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
           const int col0 = t.nt * C::kBN + c * 32;
           if (row_ok && col0 < a.H) {
             float4* dst = reinterpret_cast<float4*>(y + col0);
+            // the w2 bias (zero past the first K split) times the weight
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(rs * __uint_as_float(v[4 * i + 0]), rs * __uint_as_float(v[4 * i + 1]),
-                                   rs * __uint_as_float(v[4 * i + 2]), rs * __uint_as_float(v[4 * i + 3]));
+            for (int i = 0; i < 8; ++i) {
+              float o[4];
+#pragma unroll
+              for (int w = 0; w < 4; ++w)
+                o[w] = rs * __uint_as_float(v[4 * i + w]) +
+                       (has_bias ? wt * sb[c * 32 + 4 * i + w] : 0.0f);
+              dst[i] = make_float4(o[0], o[1], o[2], o[3]);
+            }
           }
         }
       }
@@ -384,15 +442,28 @@ cudaError_t launch(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& t
 
 // ------------------------------------------------------------------ packing
 
-// Packed values: rows of Kp = round_up(K, 128) e2m1 elements, zero beyond K.
-__global__ void pack_values_kernel(const uint8_t* __restrict__ w, long long rows, int K, int Kp,
-                                   uint8_t* __restrict__ out) {
+// Row of the natural (E, R, K) tensor that lands at packed row `row` (of
+// expert e = row / R): the same row, or with two interleaved sections
+// (rows 2j, 2j+1 = section 0 and 1 of index j) the row that section layout
+// puts there.
+__device__ __forceinline__ long long natural_row(long long row, int R, int interleaved) {
+  if (!interleaved) return row;
+  const long long e = row / R;
+  const int r = static_cast<int>(row - e * R);
+  const int half = R / 2;
+  return e * R + (r < half ? 2 * r : 2 * (r - half) + 1);
+}
+
+// Packed values: rows of Kp = round_up(K, 128) e2m1 elements, zero beyond K;
+// interleaved gate/up rows are put in halves.
+__global__ void pack_values_kernel(const uint8_t* __restrict__ w, long long rows, int R, int K,
+                                   int Kp, int interleaved, uint8_t* __restrict__ out) {
   const long long out_pitch = Kp / 2, in_pitch = K / 2;
   const long long n = rows * out_pitch;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long row = i / out_pitch, col = i - row * out_pitch;
-    out[i] = col < in_pitch ? w[row * in_pitch + col] : 0;
+    out[i] = col < in_pitch ? w[natural_row(row, R, interleaved) * in_pitch + col] : 0;
   }
 }
 
@@ -401,7 +472,7 @@ __global__ void pack_values_kernel(const uint8_t* __restrict__ w, long long rows
 // Groups come in pairs (a 192-row tile reads two), so rows past the section's
 // end exist as unit scales.
 __global__ void pack_scales_kernel(const uint8_t* __restrict__ sc, int E, int R, int K,
-                                   int sections, int groups, int kp_tiles,
+                                   int sections, int groups, int kp_tiles, int interleaved,
                                    uint8_t* __restrict__ out) {
   const int nblk = K / 32;
   const int rows_per_sec = R / sections;
@@ -421,7 +492,8 @@ __global__ void pack_scales_kernel(const uint8_t* __restrict__ sc, int E, int R,
     const int blk = 4 * kt + b;
     uint8_t v = 127;
     if (c < 3 && srow < rows_per_sec && blk < nblk) {
-      const long long row = static_cast<long long>(e) * R + sec * rows_per_sec + srow;
+      const long long row = natural_row(static_cast<long long>(e) * R + sec * rows_per_sec + srow,
+                                        R, interleaved);
       v = sc[row * nblk + blk];
     }
     out[i] = v;
@@ -441,13 +513,16 @@ cudaError_t launch_mx_down(const MxArgs& a, const CUtensorMap& tmA, const CUtens
 }
 
 cudaError_t launch_pack_mx(const uint8_t* w, const uint8_t* w_scale, int E, int R, int K,
-                           int sections, uint8_t* w_packed, uint8_t* s_packed, cudaStream_t s) {
+                           int sections, int interleaved, uint8_t* w_packed, uint8_t* s_packed,
+                           cudaStream_t s) {
   const int Kp = (K + 127) / 128 * 128;
   const int groups = mx_scale_groups(R / sections);
-  pack_values_kernel<<<1184, 256, 0, s>>>(w, static_cast<long long>(E) * R, K, Kp, w_packed);
+  pack_values_kernel<<<1184, 256, 0, s>>>(w, static_cast<long long>(E) * R, R, K, Kp, interleaved,
+                                          w_packed);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  pack_scales_kernel<<<1184, 256, 0, s>>>(w_scale, E, R, K, sections, groups, Kp / 128, s_packed);
+  pack_scales_kernel<<<1184, 256, 0, s>>>(w_scale, E, R, K, sections, groups, Kp / 128,
+                                          interleaved, s_packed);
   return cudaGetLastError();
 }
 

@@ -93,7 +93,16 @@ struct WCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + kXchgBytes + 1024;
 };
 
-__device__ __forceinline__ float silu_mul(float g, float u) {
+// The activation of the first GEMM: SiLU(g) * u, or the clamped SwiGLU of
+// GPT-OSS ("MOE Bmm1 Fused Gather", _swiglu_step1/2): the gate clamped from
+// above at `limit`, the linear branch to [-limit, limit], then
+// g * sigmoid(alpha g) * (u + 1).
+__device__ __forceinline__ float activate(const Epilogue& ep, float g, float u) {
+  if (ep.act == MOE_ACT_SWIGLU_CLAMP) {
+    g = fminf(g, ep.limit);
+    u = fmaxf(fminf(u, ep.limit), -ep.limit);
+    return g / (1.0f + __expf(-ep.alpha * g)) * (u + 1.0f);
+  }
   return g / (1.0f + __expf(-g)) * u;
 }
 
@@ -139,7 +148,8 @@ template <int KIND, typename T>
 __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
     wpair_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmTok,
                       const __grid_constant__ CUtensorMap tmTokS,
-                      const __grid_constant__ CUtensorMap tmW) {
+                      const __grid_constant__ CUtensorMap tmW,
+                      const __grid_constant__ CUtensorMap tmWu) {
   using C = WCfg<KIND, T>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::kStages];
@@ -190,6 +200,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
     tma_prefetch_desc(&tmTok);
     tma_prefetch_desc(&tmTokS);
     tma_prefetch_desc(&tmW);
+    if (KIND == kGateUp) tma_prefetch_desc(&tmWu);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -219,10 +230,11 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
         const uint32_t tx =
             2u * static_cast<uint32_t>(C::kABytes + (small ? C::kSmallRows : C::kBigRows) *
                                                         C::kRowBytes);
-        // this CTA's weight rows: 64 gate rows j and the 64 up rows j, or
-        // 128 rows of w2
+        // this CTA's weight rows: 64 gate rows j and the 64 up rows j (at
+        // the same row of the up map, shifted by up_row_offset), or 128 rows
+        // of w2
         const int wrow = KIND == kGateUp
-                             ? e * 2 * a.I + t.nt * 128 + static_cast<int>(rank) * 64
+                             ? e * a.w_rows_per_expert + t.nt * 128 + static_cast<int>(rank) * 64
                              : e * a.H + t.nt * 256 + static_cast<int>(rank) * 128;
         int kb, ke;
         split_range(a, t.split, kb, ke);
@@ -236,7 +248,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
           const uint32_t sa = smemA + stage * C::kABytes;
           if constexpr (KIND == kGateUp) {
             tma_load_2d_pair(sa, &tmW, fb, kt * C::kBK, wrow);
-            tma_load_2d_pair(sa + C::kABytes / 2, &tmW, fb, kt * C::kBK, wrow + a.I);
+            tma_load_2d_pair(sa + C::kABytes / 2, &tmWu, fb, kt * C::kBK, wrow + a.up_row_offset);
           } else {
             tma_load_2d_pair(sa, &tmW, fb, kt * C::kBK, wrow);
           }
@@ -336,16 +348,21 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
         float* x_g = xchg + (pq * 2 + 0) * 16 * 32;  // gate, columns 16..31 of a chunk
         float* x_u = xchg + (pq * 2 + 1) * 16 * 32;  // up, columns 0..15
         T* hcol = reinterpret_cast<T*>(a.out) + j;
+        // this lane's bias: of gate j (lanes 0-63) or of up j (64-127)
+        float bias = 0.0f;
+        if (a.ep.b13 != nullptr && j < a.I)
+          bias = a.ep.b13[gate_warp ? gate_bias_index(a.ep, a.I, bi.x, j)
+                                    : up_bias_index(a.ep, a.I, bi.x, j)];
         for (int c0 = 0; c0 < n; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(taddr + c0, v);
           tmem_wait_ld();
           if (gate_warp) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x_g[i * 32 + lane] = __uint_as_float(v[16 + i]);
+            for (int i = 0; i < 16; ++i) x_g[i * 32 + lane] = __uint_as_float(v[16 + i]) + bias;
           } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x_u[i * 32 + lane] = __uint_as_float(v[i]);
+            for (int i = 0; i < 16; ++i) x_u[i * 32 + lane] = __uint_as_float(v[i]) + bias;
           }
           named_bar_sync(1 + pq, 64);
           // gate warp: tokens c0..c0+15; up warp: tokens c0+16..c0+31
@@ -353,10 +370,10 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
           if (j < a.I) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float g = gate_warp ? __uint_as_float(v[i]) : x_g[i * 32 + lane];
-              const float u = gate_warp ? x_u[i * 32 + lane] : __uint_as_float(v[16 + i]);
+              const float g = gate_warp ? __uint_as_float(v[i]) + bias : x_g[i * 32 + lane];
+              const float u = gate_warp ? x_u[i * 32 + lane] : __uint_as_float(v[16 + i]) + bias;
               if (nb + i < valid)
-                store_h<T>(hcol + static_cast<long long>(bi.z + nb + i) * a.I, silu_mul(g, u));
+                store_h<T>(hcol + static_cast<long long>(bi.z + nb + i) * a.I, activate(a.ep, g, u));
             }
           }
           named_bar_sync(1 + pq, 64);  // the exchange slots are free again
@@ -365,6 +382,10 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
         const int c = t.nt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
         float* ycol = reinterpret_cast<float*>(a.out) +
                       static_cast<long long>(t.split) * a.cap * a.H + c;
+        // the w2 bias joins once, in the first K split
+        const float bias = (a.ep.b2 != nullptr && t.split == 0 && c < a.H)
+                               ? a.ep.b2[static_cast<long long>(bi.x) * a.H + c]
+                               : 0.0f;
         for (int c0 = 0; c0 < n; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(taddr + c0, v);
@@ -376,7 +397,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
           for (int i = 0; i < 32; ++i) {
             const float w = __shfl_sync(0xffffffffu, w_l, i);
             if (c0 + i < valid && c < a.H)
-              ycol[static_cast<long long>(bi.z + c0 + i) * a.H] = w * __uint_as_float(v[i]);
+              ycol[static_cast<long long>(bi.z + c0 + i) * a.H] = w * (__uint_as_float(v[i]) + bias);
           }
         }
       }
@@ -435,7 +456,7 @@ int max_pairs() {
 
 template <int KIND, typename T>
 cudaError_t launch(const GemmArgs& a, const CUtensorMap& tmTok, const CUtensorMap& tmTokS,
-                   const CUtensorMap& tmW, int grid, cudaStream_t s) {
+                   const CUtensorMap& tmW, const CUtensorMap& tmWu, int grid, cudaStream_t s) {
   using C = WCfg<KIND, T>;
   auto kern = wpair_gemm_kernel<KIND, T>;
   cudaError_t err =
@@ -443,7 +464,7 @@ cudaError_t launch(const GemmArgs& a, const CUtensorMap& tmTok, const CUtensorMa
   if (err != cudaSuccess) return err;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = wpair_config<KIND, T>(grid, s, attr);
-  return cudaLaunchKernelEx(&cfg, kern, a, tmTok, tmTokS, tmW);
+  return cudaLaunchKernelEx(&cfg, kern, a, tmTok, tmTokS, tmW, tmWu);
 }
 
 }  // namespace
@@ -455,17 +476,18 @@ int wpair_max_active(int kind, int dtype) {
 }
 
 cudaError_t launch_wpair_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
-                                 const CUtensorMap& tmTokS, const CUtensorMap& tmW, int grid,
-                                 cudaStream_t s) {
-  if (dtype == MOE_BF16) return launch<kGateUp, __nv_bfloat16>(a, tmTok, tmTokS, tmW, grid, s);
-  return launch<kGateUp, float>(a, tmTok, tmTokS, tmW, grid, s);
+                                 const CUtensorMap& tmTokS, const CUtensorMap& tmW,
+                                 const CUtensorMap& tmWu, int grid, cudaStream_t s) {
+  if (dtype == MOE_BF16)
+    return launch<kGateUp, __nv_bfloat16>(a, tmTok, tmTokS, tmW, tmWu, grid, s);
+  return launch<kGateUp, float>(a, tmTok, tmTokS, tmW, tmWu, grid, s);
 }
 
 cudaError_t launch_wpair_down(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
                               const CUtensorMap& tmTokS, const CUtensorMap& tmW, int grid,
                               cudaStream_t s) {
-  if (dtype == MOE_BF16) return launch<kDown, __nv_bfloat16>(a, tmTok, tmTokS, tmW, grid, s);
-  return launch<kDown, float>(a, tmTok, tmTokS, tmW, grid, s);
+  if (dtype == MOE_BF16) return launch<kDown, __nv_bfloat16>(a, tmTok, tmTokS, tmW, tmW, grid, s);
+  return launch<kDown, float>(a, tmTok, tmTokS, tmW, tmW, grid, s);
 }
 
 }  // namespace moe

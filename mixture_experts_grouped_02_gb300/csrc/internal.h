@@ -17,7 +17,35 @@ constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 // the two automatic block sizes of the bf16/fp32 GEMMs.
 constexpr int kBlockM = 128;
 
+// Activation and biases of the expert FFN (moe_problem_t).
+struct Epilogue {
+  int act;             // MOE_ACT_SILU / MOE_ACT_SWIGLU_CLAMP
+  float alpha, limit;  // MOE_ACT_SWIGLU_CLAMP
+  int interleaved;     // w13 rows and w13_bias entries: gate 2j, up 2j+1
+  const float* b13;    // (L, 2I) or null
+  const float* b2;     // (L, H) or null
+};
+
+// Row of gate j / up j of expert e in w13_bias.
+__host__ __device__ inline long long gate_bias_index(const Epilogue& ep, int I, int e, int j) {
+  return static_cast<long long>(e) * 2 * I + (ep.interleaved ? 2 * j : j);
+}
+__host__ __device__ inline long long up_bias_index(const Epilogue& ep, int I, int e, int j) {
+  return static_cast<long long>(e) * 2 * I + (ep.interleaved ? 2 * j + 1 : I + j);
+}
+
+// Router logits of the routing step folded into align (moe_route_align).
+struct RouteArgs {
+  const void* logits;  // (T, E) fp32 or bf16, or null: the ids are given
+  int bf16;            // logits are bf16
+  int T, E, K;
+  int32_t* ids;        // (T, K) out
+  float* weights;      // (T, K) out
+  int32_t* status;
+};
+
 struct AlignArgs {
+  RouteArgs route;     // route.logits != null: route first, into `ids`
   const int32_t* ids;
   int n_assign;  // T*K
   int E;         // ids lie in [0, E)
@@ -51,6 +79,9 @@ struct GemmArgs {
   void* out;                  // gate/up: h (cap, I); down: y (splits, cap, H) fp32
   int32_t* status;
   unsigned long long timeout_ns;
+  Epilogue ep;
+  int w_rows_per_expert;      // gate/up: rows of one expert in the gate weight map
+  int up_row_offset;          // gate/up: up row j = gate row j + this (in the up map)
 };
 
 // Arguments of one block-scaled (fp8 activations x mxfp4 weights) grouped
@@ -74,6 +105,7 @@ struct MxArgs {
   float h_scale;               // hq = e4m3(a / h_scale)
   int32_t* status;
   unsigned long long timeout_ns;
+  Epilogue ep;
 };
 
 // tmW: packed e2m1 values of w13 / w2, (E*R rows) x (Kp elements), box
@@ -85,13 +117,18 @@ cudaError_t launch_mx_gate_up(const MxArgs& a, const CUtensorMap& tmA, const CUt
 cudaError_t launch_mx_down(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW,
                            int grid, cudaStream_t s);
 cudaError_t launch_pack_mx(const uint8_t* w, const uint8_t* w_scale, int E, int R, int K,
-                           int sections, uint8_t* w_packed, uint8_t* s_packed, cudaStream_t s);
+                           int sections, int interleaved, uint8_t* w_packed, uint8_t* s_packed,
+                           cudaStream_t s);
 
 // 96-row scale groups per section of `rows` weight rows (an even number).
 inline int mx_scale_groups(int rows) { return 2 * ((rows + 191) / 192); }
 inline int mx_padded_k(int K) { return (K + 127) / 128 * 128; }
 
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
+// The routing step alone, a warp per token over many CTAs (large batches).
+cudaError_t launch_route(const RouteArgs& r, cudaStream_t s);
+// Largest batch whose routing the single-CTA align kernel does itself.
+constexpr int kRouteInAlignMaxTokens = 1024;
 cudaError_t launch_combine(const float* y, int splits, long long cap, const int32_t* inv_perm,
                            int T, int K, int H, int out_dtype, void* out, int32_t* status,
                            cudaStream_t s);
@@ -110,9 +147,11 @@ constexpr int kPairBlockM = 256;
 // side (gemm_wpair.cu); grid = 2 x clusters.  tmTok / tmTokS: token rows in sorted order (x for gate/up, h for down),
 // boxes of 128 and 16 rows; tmW: w13 (box 64 rows) or w2 (box 128 rows).
 int wpair_max_active(int kind, int dtype);
+// tmWu: the map of the up rows (gate/up; the same map as tmW when w13 is in
+// halves); unused by down.
 cudaError_t launch_wpair_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
-                                 const CUtensorMap& tmTokS, const CUtensorMap& tmW, int grid,
-                                 cudaStream_t s);
+                                 const CUtensorMap& tmTokS, const CUtensorMap& tmW,
+                                 const CUtensorMap& tmWu, int grid, cudaStream_t s);
 cudaError_t launch_wpair_down(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
                               const CUtensorMap& tmTokS, const CUtensorMap& tmW, int grid,
                               cudaStream_t s);

@@ -51,6 +51,13 @@ int check_problem(const moe_problem_t* p) {
       (p->local_experts == 0 && p->expert_base != 0))
     return MOE_ERR_INVALID_ARG;
   if (local_experts(p) > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (p->activation != MOE_ACT_SILU && p->activation != MOE_ACT_SWIGLU_CLAMP)
+    return MOE_ERR_INVALID_ARG;
+  if (p->activation == MOE_ACT_SWIGLU_CLAMP &&
+      !(p->swiglu_limit > 0.0f && p->swiglu_limit < 3.0e38f && p->swiglu_alpha > -3.0e38f &&
+        p->swiglu_alpha < 3.0e38f))
+    return MOE_ERR_INVALID_ARG;
+  if (p->gate_up_interleaved != 0 && p->gate_up_interleaved != 1) return MOE_ERR_INVALID_ARG;
   const long long na = static_cast<long long>(p->T) * p->K;
   if (na >= (1ll << 30)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -257,8 +264,10 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA
 int run_align(const int32_t* ids, int T, int K, int E, int e_base, int e_local, int bm,
               int32_t* counts, int32_t* offsets, int32_t* padded_offsets, int32_t* sorted_ids,
               int32_t* inv_perm, int32_t* block_info, int32_t* num_blocks, int32_t* status,
-              cudaStream_t s) {
+              cudaStream_t s, const RouteArgs* route = nullptr) {
   AlignArgs a;
+  std::memset(&a.route, 0, sizeof(a.route));
+  if (route != nullptr) a.route = *route;
   a.ids = ids;
   a.n_assign = T * K;
   a.E = E;
@@ -277,6 +286,17 @@ int run_align(const int32_t* ids, int T, int K, int E, int e_base, int e_local, 
   return cuda_status(launch_align(a, s));
 }
 
+Epilogue epilogue_of(const moe_problem_t* p) {
+  Epilogue ep;
+  ep.act = p->activation;
+  ep.alpha = p->swiglu_alpha;
+  ep.limit = p->swiglu_limit;
+  ep.interleaved = p->gate_up_interleaved;
+  ep.b13 = p->w13_bias;
+  ep.b2 = p->w2_bias;
+  return ep;
+}
+
 GemmArgs base_args(const moe_problem_t* p) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -287,6 +307,7 @@ GemmArgs base_args(const moe_problem_t* p) {
   a.K = p->K;
   a.cap = capacity(p->T, p->K, local_experts(p), block_m_of(p));
   a.timeout_ns = kWaitTimeoutNs;
+  a.ep = epilogue_of(p);
   return a;
 }
 
@@ -331,13 +352,32 @@ int run_gemm1(const moe_problem_t* p, const void* x_sorted, const void* w13,
   a.out = h;
   a.status = status;
   a.x = x_sorted;
-  CUtensorMap tmTok, tmTokS, tmW;
-  int rc = make_map(&tmW, p->act, w13, p->H, 2ll * p->I * local_experts(p), bk, 64);
+  CUtensorMap tmTok, tmTokS, tmW, tmWu;
+  int rc;
+  if (p->gate_up_interleaved) {
+    // gate rows 2j and up rows 2j+1: two maps of I rows per expert, each row
+    // two w13 rows apart
+    const CUtensorMapDataType dt =
+        p->act == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const long long row_bytes = 2ll * p->H * act_bytes(p->act);
+    const long long rows = 1ll * p->I * local_experts(p);
+    rc = make_map_typed(&tmW, dt, w13, p->H, rows, row_bytes, bk, 64);
+    if (rc == MOE_OK)
+      rc = make_map_typed(&tmWu, dt, static_cast<const char*>(w13) + p->H * act_bytes(p->act),
+                          p->H, rows, row_bytes, bk, 64);
+    a.w_rows_per_expert = p->I;
+    a.up_row_offset = 0;
+  } else {
+    rc = make_map(&tmW, p->act, w13, p->H, 2ll * p->I * local_experts(p), bk, 64);
+    tmWu = tmW;
+    a.w_rows_per_expert = 2 * p->I;
+    a.up_row_offset = p->I;
+  }
   if (rc == MOE_OK) rc = make_map(&tmTok, p->act, x_sorted, p->H, a.cap, bk, 128);
   if (rc == MOE_OK) rc = make_map(&tmTokS, p->act, x_sorted, p->H, a.cap, bk, 16);
   if (rc != MOE_OK) return rc;
   const long long max_tiles = (a.cap / block_m_of(p)) * a.n_tiles;
-  return cuda_status(launch_wpair_gate_up(p->act, a, tmTok, tmTokS, tmW,
+  return cuda_status(launch_wpair_gate_up(p->act, a, tmTok, tmTokS, tmW, tmWu,
                                           pair_grid(max_tiles, 0, p->act), s));
 }
 
@@ -378,6 +418,7 @@ MxArgs mx_args(const moe_problem_t* p) {
   a.cap = capacity(p->T, p->K, local_experts(p), kBlockM);
   a.h_scale = h_scale_of(p);
   a.timeout_ns = kWaitTimeoutNs;
+  a.ep = epilogue_of(p);
   return a;
 }
 
@@ -534,6 +575,43 @@ int moe_align_local(const int32_t* topk_ids, int T, int K, int E, int expert_bas
   return run_align(topk_ids, T, K, E, expert_base, local_experts, block_m, counts, offsets,
                    padded_offsets, sorted_ids, inv_perm, block_info, num_blocks, dev_status,
                    static_cast<cudaStream_t>(stream));
+}
+
+int moe_route_align(const void* logits, int logit_dtype, int T, int E, int K, int expert_base,
+                    int local_experts, int block_m, int32_t* topk_ids, float* topk_weights,
+                    int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                    int32_t* sorted_ids, int32_t* inv_perm, int32_t* block_info,
+                    int32_t* num_blocks, int32_t* dev_status, void* stream) {
+  if (T < 0 || E <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (logit_dtype != MOE_BF16 && logit_dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (K > E) return MOE_ERR_INVALID_ARG;
+  if (K > 32 || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128 && block_m != 256)
+    return MOE_ERR_INVALID_ARG;
+  if (expert_base < 0 || local_experts <= 0 ||
+      static_cast<long long>(expert_base) + local_experts > E)
+    return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * K >= (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_weights || !counts || !offsets || !padded_offsets ||
+      !sorted_ids || !inv_perm || !block_info || !num_blocks)
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(block_info) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  RouteArgs r;
+  r.logits = logits;
+  r.bf16 = logit_dtype == MOE_BF16;
+  r.T = T;
+  r.E = E;
+  r.K = K;
+  r.ids = topk_ids;
+  r.weights = topk_weights;
+  r.status = dev_status;
+  const bool in_align = T <= kRouteInAlignMaxTokens;
+  if (!in_align && launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return run_align(topk_ids, T, K, E, expert_base, local_experts, block_m, counts, offsets,
+                   padded_offsets, sorted_ids, inv_perm, block_info, num_blocks, dev_status, s,
+                   in_align ? &r : nullptr);
 }
 
 int moe_quantize_x_fp8(const void* x, int x_dtype, int T, int H, uint8_t* xq, float* row_scale,
@@ -702,11 +780,13 @@ size_t moe_mx_packed_bytes(int E, int R, int K, int sections, size_t* value_byte
 }
 
 int moe_pack_mx_weights(const uint8_t* w, const uint8_t* w_scale, int E, int R, int K,
-                        int sections, uint8_t* w_packed, uint8_t* scale_packed, void* stream) {
+                        int sections, int interleaved, uint8_t* w_packed, uint8_t* scale_packed,
+                        void* stream) {
   if (moe_mx_packed_bytes(E, R, K, sections, nullptr, nullptr) == 0) return MOE_ERR_INVALID_ARG;
+  if (interleaved != 0 && (interleaved != 1 || sections != 2)) return MOE_ERR_INVALID_ARG;
   if (!w || !w_scale || !w_packed || !scale_packed) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_pack_mx(w, w_scale, E, R, K, sections, w_packed, scale_packed,
-                                    static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_pack_mx(w, w_scale, E, R, K, sections, interleaved, w_packed,
+                                    scale_packed, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_device_info(int* sm_count_out, int* pair_clusters_out) {

@@ -16,7 +16,15 @@ dsv3_prefill       8192    7168   2048   256  8   bf16    N(0,1)+Zipf bias
 mixtral_decode_T*  1..128  4096   14336  8    2   bf16    N(0,1)
 dsv3_decode_T*     1..128  7168   2048   256  8   bf16    N(0,1)+Zipf bias
 lowp               2048    2880   2880   128  4   mxfp4   U(0,1)
+lowp_oai           2048    2880   2880   128  4   mxfp4   U(0,1)
 =================  ======  =====  =====  ===  ==  ======  ================
+
+``lowp_oai`` is the same layer with GPT-OSS's expert FFN as the "MOE Bmm1
+Fused Gather" example benchmarks it: the clamped SwiGLU with alpha =
+U(0,1)/5 + 1 and limit = U(0,1)/5 + 1.3, gate and linear rows of w13
+interleaved, a per-expert fp32 w13 bias ~ N(0,1), fp8 hidden activation
+with out-scale U(0,1) + 3.5 (the example's y_scale).  The w2 bias ~ N(0,1)
+is this workload's reading (the example benchmarks the first GEMM only).
 
 Values: x ~ N(0,1); w13 ~ N(0, 1/sqrt(H)), w2 ~ N(0, 1/sqrt(I)) (standard
 deviation 1/sqrt(fan_in)), drawn in fp32 and rounded to nearest-even into
@@ -57,6 +65,7 @@ class MoEConfig:
     K: int
     dtype: str  # "f32" | "bf16" | "mxfp4"
     routing: str  # "normal" | "zipf" | "uniform"
+    activation: str = "silu"  # "silu" | "swiglu_oai" (clamped, biases, interleaved w13)
 
     @property
     def n_assign(self) -> int:
@@ -76,6 +85,8 @@ _BASE = {
     "mixtral_prefill": MoEConfig("mixtral_prefill", 4096, 4096, 14336, 8, 2, "bf16", "normal"),
     "dsv3_prefill": MoEConfig("dsv3_prefill", 8192, 7168, 2048, 256, 8, "bf16", "zipf"),
     "lowp": MoEConfig("lowp", 2048, 2880, 2880, 128, 4, "mxfp4", "uniform"),
+    "lowp_oai": MoEConfig("lowp_oai", 2048, 2880, 2880, 128, 4, "mxfp4", "uniform",
+                          "swiglu_oai"),
 }
 DECODE_T = (1, 8, 32, 128)
 for _t in DECODE_T:
@@ -91,7 +102,7 @@ def config(name: str) -> MoEConfig:
 
 
 # tensor ids for sub-seeding
-_X, _W13, _W2, _LOGITS, _ZIPF = 1, 2, 3, 4, 5
+_X, _W13, _W2, _LOGITS, _ZIPF, _B13, _B2, _OAI = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 def _generator(seed: int, tensor_id: int, part: int, device) -> torch.Generator:
@@ -111,11 +122,24 @@ class MoEInputs:
     topk_weights: torch.Tensor  # (T, K) fp32
     w13_scale: torch.Tensor | None = None  # (E, 2I, H/32) uint8 e8m0
     w2_scale: torch.Tensor | None = None  # (E, H, I/32) uint8 e8m0
+    # activation "swiglu_oai" only: rows of w13 (and w13_bias) alternate
+    # gate / linear; scalars of the clamped SwiGLU and the fp8 out-scale
+    w13_bias: torch.Tensor | None = None  # (E, 2I) fp32, w13's row order
+    w2_bias: torch.Tensor | None = None  # (E, H) fp32
+    swiglu_alpha: float = 1.0
+    swiglu_limit: float = float("inf")
+    h_scale: float = 1.0
+
+    @property
+    def interleaved(self) -> bool:
+        return self.cfg.activation == "swiglu_oai"
 
     def to(self, device) -> "MoEInputs":
         mv = lambda t: None if t is None else t.to(device)
-        return MoEInputs(self.cfg, mv(self.x), mv(self.w13), mv(self.w2), mv(self.topk_ids),
-                         mv(self.topk_weights), mv(self.w13_scale), mv(self.w2_scale))
+        return dataclasses.replace(
+            self, x=mv(self.x), w13=mv(self.w13), w2=mv(self.w2), topk_ids=mv(self.topk_ids),
+            topk_weights=mv(self.topk_weights), w13_scale=mv(self.w13_scale),
+            w2_scale=mv(self.w2_scale), w13_bias=mv(self.w13_bias), w2_bias=mv(self.w2_bias))
 
 
 def _storage_dtype(cfg: MoEConfig):
@@ -231,7 +255,24 @@ def generate(cfg: MoEConfig | str, seed: int = 0, device="cpu") -> MoEInputs:
     x = draw_x(cfg, seed, device)
     w13, w2, s13, s2 = draw_weights(cfg, seed, device)
     ids, w = route(router_logits(cfg, seed, device), cfg.K)
-    return MoEInputs(cfg, x.contiguous(), w13.contiguous(), w2.contiguous(), ids, w, s13, s2)
+    inp = MoEInputs(cfg, x.contiguous(), w13.contiguous(), w2.contiguous(), ids, w, s13, s2)
+    if cfg.activation == "swiglu_oai":
+        draw_swiglu_oai(inp, seed, device)
+    return inp
+
+
+def draw_swiglu_oai(inp: MoEInputs, seed: int = 0, device="cpu") -> None:
+    """Biases and scalars of the GPT-OSS expert FFN (see the module doc)."""
+    cfg = inp.cfg
+    inp.w13_bias = torch.randn((cfg.E, 2 * cfg.I), generator=_generator(seed, _B13, 0, device),
+                               device=device, dtype=torch.float32)
+    inp.w2_bias = torch.randn((cfg.E, cfg.H), generator=_generator(seed, _B2, 0, device),
+                              device=device, dtype=torch.float32)
+    u = torch.rand(3, generator=_generator(seed, _OAI, 0, "cpu"), dtype=torch.float32)
+    # held as fp32 values, the precision the GPU path takes them in
+    inp.swiglu_alpha = float(np.float32(float(u[0]) / 5.0 + 1.0))
+    inp.swiglu_limit = float(np.float32(float(u[1]) / 5.0 + 1.3))
+    inp.h_scale = float(np.float32(float(u[2]) + 3.5))
 
 
 def to_numpy_storage(t: torch.Tensor | None):

@@ -23,12 +23,35 @@ def generate(cfg, seed=0, device="cuda"):
     return gen.generate(cfg, seed=seed, device=device)
 
 
-def oracle_problem(inp: gen.MoEInputs, E=None, quantize_x=False, h_e4m3=False, h_scale=1.0):
+def activation_kw(inp: gen.MoEInputs, experts=None):
+    """The oracle's activation arguments for `inp` (its biases restricted to
+    `experts`, in that order, when given)."""
+    if inp.cfg.activation != "swiglu_oai":
+        return {}
+    sel = slice(None) if experts is None else np.asarray(experts)
+    return dict(activation=oracle.ACT_SWIGLU_CLAMP, swiglu_alpha=inp.swiglu_alpha,
+                swiglu_limit=inp.swiglu_limit, gate_up_interleaved=True,
+                w13_bias=inp.w13_bias.cpu().numpy()[sel], w2_bias=inp.w2_bias.cpu().numpy()[sel])
+
+
+def problem_kw(inp: gen.MoEInputs):
+    """The library's make_problem arguments for the activation of `inp`."""
+    if inp.cfg.activation != "swiglu_oai":
+        return {}
+    import mixture_experts_grouped_02_gb300 as moe
+    return dict(activation=moe.MOE_ACT_SWIGLU_CLAMP, swiglu_alpha=inp.swiglu_alpha,
+                swiglu_limit=inp.swiglu_limit, gate_up_interleaved=True,
+                w13_bias=inp.w13_bias, w2_bias=inp.w2_bias)
+
+
+def oracle_problem(inp: gen.MoEInputs, E=None, quantize_x=False, h_e4m3=False, h_scale=1.0,
+                   experts=None):
     c = inp.cfg
     xs = np_store(inp.x[:1])
     ws = np_store(inp.w13[:1])
     return oracle.make_problem(c.T, c.H, c.I, c.E if E is None else E, c.K, xs, ws,
-                               quantize_x=quantize_x, h_e4m3=h_e4m3, h_scale=h_scale)
+                               quantize_x=quantize_x, h_e4m3=h_e4m3, h_scale=h_scale,
+                               **activation_kw(inp, experts))
 
 
 def oracle_forward_tokens(inp: gen.MoEInputs, tokens, mode=oracle.EXACT, **kw):
@@ -46,7 +69,7 @@ def oracle_forward_tokens(inp: gen.MoEInputs, tokens, mode=oracle.EXACT, **kw):
     w2 = np_store(inp.w2.index_select(0, sel))
     s13 = None if inp.w13_scale is None else np_store(inp.w13_scale.index_select(0, sel))
     s2 = None if inp.w2_scale is None else np_store(inp.w2_scale.index_select(0, sel))
-    P = oracle_problem(inp, E=len(used), **kw)
+    P = oracle_problem(inp, E=len(used), experts=used, **kw)
     return oracle.forward(P, np_store(inp.x), sub_ids, inp.topk_weights.cpu().numpy(), w13, w2,
                           s13, s2, mode=mode, tokens=tokens)
 

@@ -125,6 +125,16 @@ def test_entry_points_reject_bad_arguments_before_launch():
     assert L.moe_quantize_x_fp8(fake, _abi.MOE_BF16, 4, 7, fake, fake, None) == \
         _abi.MOE_ERR_INVALID_ARG
     assert L.moe_get_device_status(None, None) == _abi.MOE_ERR_INVALID_ARG
+    # routing: K within [1, min(E, 32)], logits fp32 or bf16
+    args9 = [fake] * 9
+    assert L.moe_route_align(fake, _abi.MOE_F32, 4, 8, 9, 0, 8, 128, *args9, None, None) == \
+        _abi.MOE_ERR_INVALID_ARG
+    assert L.moe_route_align(fake, _abi.MOE_F32, 4, 64, 33, 0, 64, 128, *args9, None, None) == \
+        _abi.MOE_ERR_UNSUPPORTED
+    assert L.moe_route_align(fake, _abi.MOE_E4M3, 4, 8, 2, 0, 8, 128, *args9, None, None) == \
+        _abi.MOE_ERR_INVALID_ARG
+    assert L.moe_route_align(None, _abi.MOE_F32, 0, 8, 2, 0, 8, 128, *([None] * 9), None,
+                             None) == _abi.MOE_OK
     # expert shards: the range must lie inside [0, E)
     for base, local in ((-1, 2), (7, 2), (0, 0), (0, 9)):
         assert L.moe_align_local(fake, 4, 2, 8, base, local, 128, *([fake] * 7), None, None) == \

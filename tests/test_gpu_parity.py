@@ -10,7 +10,7 @@ import torch
 import oracle
 import oracle_pins as pins
 from gpu_util import (assert_close, errors, generate, np_store, oracle_forward_tokens,
-                      oracle_problem, sample_tokens)
+                      oracle_problem, problem_kw, sample_tokens)
 import mixture_experts_grouped_02_gb300 as moe
 from mixture_experts_grouped_02_gb300 import _abi
 from mixture_experts_grouped_02_gb300 import inputs as gen
@@ -86,6 +86,54 @@ def test_align_local_bit_exact(case, shard):
     for k in ("counts", "offsets", "padded_offsets", "sorted_ids", "inv_perm", "block_info"):
         assert np.array_equal(got[k].cpu().numpy(), ref[k]), k
     assert int(got["num_blocks"].item()) == ref["num_blocks"]
+
+
+ROUTE_CASES = [
+    # T, E, K, logit dtype, kind; up to 1024 tokens the align kernel routes
+    (37, 8, 2, torch.float32, "normal"),
+    (1000, 256, 8, torch.float32, "zipf"),
+    (5000, 256, 8, torch.float32, "zipf"),     # separate routing kernel
+    (2048, 128, 4, torch.bfloat16, "normal"),
+    (300, 64, 6, torch.float32, "ties"),       # small integers: many equal logits
+    (1, 1024, 32, torch.float32, "normal"),
+]
+
+
+@pytest.mark.parametrize("case", ROUTE_CASES, ids=lambda c: "T%d_E%d_K%d_%s_%s" % (
+    c[0], c[1], c[2], str(c[3]).split(".")[-1], c[4]))
+def test_route_align_vs_oracle(case):
+    T, E, K, dt, kind = case
+    g = torch.Generator().manual_seed(T + E)
+    if kind == "ties":
+        logits = torch.randint(-3, 4, (T, E), generator=g).to(torch.float32)
+    else:
+        logits = torch.randn((T, E), generator=g)
+        if kind == "zipf":
+            logits = logits + gen.zipf_bias(E, 1)
+    logits = logits.to(dt)
+    ids_ref, w_ref = oracle.route(np_store(logits), K)
+    bm = 128
+    st = _status()
+    got = moe.route_align(logits.cuda(), K, bm, dev_status=st)
+    assert moe.moe_get_device_status(st) == 0
+    assert np.array_equal(got["topk_ids"].cpu().numpy(), ids_ref)
+    w = got["topk_weights"].cpu().numpy().astype(np.float64)
+    assert np.allclose(w, w_ref, rtol=2e-6, atol=1e-7)
+    al = oracle.align(ids_ref, E, bm)
+    for k in ("counts", "offsets", "padded_offsets", "sorted_ids", "inv_perm", "block_info"):
+        assert np.array_equal(got[k].cpu().numpy(), al[k]), k
+    assert int(got["num_blocks"].item()) == al["num_blocks"]
+
+
+def test_route_align_shard():
+    T, E, K = 700, 64, 4
+    logits = torch.randn((T, E), generator=torch.Generator().manual_seed(3))
+    ids_ref, _ = oracle.route(np_store(logits), K)
+    got = moe.route_align(logits.cuda(), K, 64, expert_base=16, local_experts=16)
+    al = oracle.align(ids_ref, E, 64, expert_base=16, local_experts=16)
+    assert np.array_equal(got["topk_ids"].cpu().numpy(), ids_ref)
+    for k in ("counts", "padded_offsets", "sorted_ids", "inv_perm", "block_info"):
+        assert np.array_equal(got[k].cpu().numpy(), al[k]), k
 
 
 # ------------------------------------------------------------------ stages
@@ -581,3 +629,66 @@ def test_forward_expert_shard_mx():
     emu = _oracle_shard(inp, base, L, np.arange(cfg.T), mode=oracle.EMULATE, quantize_x=True,
                         h_e4m3=True)
     assert_close(out, emu, max_abs=MX_MAX_ABS, rel_l2=MX_REL_EMU, what="mx shard vs emulate")
+
+
+# ------------------------------------------------------------------ GPT-OSS expert FFN
+
+OAI_CASES = [
+    # T, H, I, E, K, dtype -- clamped SwiGLU, biases, interleaved gate/linear rows
+    (300, 256, 320, 3, 2, "bf16"),
+    (8, 256, 1536, 8, 2, "bf16"),    # few tokens: the down projection splits K
+    (40, 128, 256, 8, 2, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", OAI_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s" % c)
+def test_forward_swiglu_oai(case):
+    cfg = gen.MoEConfig("oai", *case, "normal", "swiglu_oai")
+    inp = gen.generate(cfg, seed=51)
+    d = inp.to("cuda")
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype, **problem_kw(d))
+    if cfg.T <= 8:
+        assert moe.moe_gemm2_default_splits(p) > 1
+    out = moe.forward(d.x, d.topk_ids, d.topk_weights, d.w13, d.w2, **problem_kw(d))
+    ref = oracle_forward_tokens(inp, np.arange(cfg.T))
+    assert_close(out, ref, what=cfg.name)
+
+
+def test_pack_mx_interleaved_equals_halves():
+    E, R, K = 3, 2 * 96, 320
+    g = torch.Generator().manual_seed(9)
+    w = torch.randint(0, 256, (E, R, K // 2), generator=g, dtype=torch.uint8)
+    sc = torch.randint(100, 140, (E, R, K // 32), generator=g, dtype=torch.uint8)
+    inter_w = torch.empty_like(w)
+    inter_s = torch.empty_like(sc)
+    inter_w[:, 0::2], inter_w[:, 1::2] = w[:, :R // 2], w[:, R // 2:]
+    inter_s[:, 0::2], inter_s[:, 1::2] = sc[:, :R // 2], sc[:, R // 2:]
+    a = moe.pack_mx(w.cuda(), sc.cuda(), 2)
+    b = moe.pack_mx(inter_w.cuda(), inter_s.cuda(), 2, interleaved=True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def _run_oai_mx(d, cfg):
+    kw = problem_kw(d)
+    w13p, s13p = moe.pack_mx(d.w13, d.w13_scale, 2, interleaved=True)
+    w2p, s2p = moe.pack_mx(d.w2, d.w2_scale, 1)
+    return moe.forward(d.x, d.topk_ids, d.topk_weights, w13p, w2p, w13_scale=s13p, w2_scale=s2p,
+                       weight="mxfp4", h_scale=d.h_scale, **kw)
+
+
+@pytest.mark.parametrize("case", [(96, 256, 320, 16, 4), (5, 512, 256, 8, 2)],
+                         ids=lambda c: "T%d_H%d_I%d_E%d_K%d" % c)
+def test_forward_swiglu_oai_mx(case):
+    cfg = gen.MoEConfig("oai_mx", *case, "mxfp4", "uniform", "swiglu_oai")
+    inp = gen.generate(cfg, seed=52)
+    d = inp.to("cuda")
+    out = _run_oai_mx(d, cfg)
+    _check_mx(out, inp, np.arange(cfg.T), h_scale=inp.h_scale)
+
+
+def test_forward_lowp_oai_full_size_sampled():
+    cfg = gen.config("lowp_oai")
+    d = gen.generate(cfg, seed=0, device="cuda")
+    out = _run_oai_mx(d, cfg)
+    assert torch.isfinite(out.float()).all()
+    _check_mx(out, d, sample_tokens(cfg.T, 24, seed=5), h_scale=d.h_scale)
