@@ -1,6 +1,7 @@
 // ptx.cuh -- thin inline-PTX wrappers for the sm_103a features the kernels
-// use: mbarrier phases, TMA tile / gather4 loads, tensor memory (TMEM)
-// allocation, tcgen05 MMA / commit / load, and the fences between them.
+// use: mbarrier phases, TMA tile and bulk loads, tensor memory (TMEM)
+// allocation and copies, tcgen05 MMA / commit / load, and the fences between
+// them.
 // Everything here is a single PTX instruction or a bounded loop around one.
 #pragma once
 
@@ -94,13 +95,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
-                   cluster_addr),
-               "r"(bytes)
-               : "memory");
-}
-
 // try_wait that acquires at cluster scope (for barriers other CTAs arrive on).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -182,50 +176,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// Gather four rows r0..r3 (each one box of the tensor map: inner extent
-// starting at column `col`, one row high) into consecutive shared memory.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
-                                            int col, int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(bar)
-      : "memory");
-}
-
-// ---------------------------------------------------------------- cp.async
-
-// 16-byte global -> shared copy that bypasses L1 (cached in L2 only).
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-// 16-byte copy of which only the first `src_bytes` (0 or 16) come from
-// global memory; the rest of the 16 bytes are zero-filled.
-__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-
-// 8-byte copy (through L1), zero-filled beyond `src_bytes` (0 or 8).
-__device__ __forceinline__ void cp_async_8_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// Wait until at most N of this thread's most recent cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // ---------------------------------------------------------------- TMEM
 
 // Warp-collective: allocate `ncols` TMEM columns, base address -> *dst (smem).
@@ -290,24 +240,6 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_fmt, int M, int N)
          | (ab_fmt << 10)                           // B format
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 // Shared-memory descriptor of an unswizzled matrix whose 8-row x 16-byte core
