@@ -121,6 +121,7 @@ __device__ __forceinline__ void route_token(const RouteArgs& r, int t, int lane)
 }
 
 __global__ void __launch_bounds__(256) route_kernel(const RouteArgs r) {
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -195,6 +196,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
   const int na = p.n_assign;
   const int bm = p.block_m;
 
+  pdl_wait();  // ids written by the routing kernel, when it ran first
+  pdl_launch_dependents();
   if (tid == 0) s_bad = 0;
   for (int i = tid; i < kAlignWarps * L; i += kAlignThreads) hist[i] = 0;
   // 0. routing of small batches, in this CTA: a warp per token; the ids it
@@ -354,8 +357,9 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  align_kernel<<<1, kAlignThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(1), dim3(kAlignThreads), smem, s, attr);
+  return cudaLaunchKernelEx(&cfg, align_kernel, a);
 }
 
 }  // namespace moe

@@ -150,6 +150,9 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
   const uint32_t smemB = smemA + C::kStages * C::kABytes;
   const uint32_t smemS = smemB + C::kStages * C::kBBytes;
 
+  // the earlier kernels of the stream have finished before their output is read
+  pdl_wait();
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     s_skip = (a.status != nullptr && *reinterpret_cast<volatile int32_t*>(a.status) != 0);
     s_abort = 0;
@@ -436,8 +439,9 @@ cudaError_t launch(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& t
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(a, tmA, tmW);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, attr);
+  return cudaLaunchKernelEx(&cfg, kern, a, tmA, tmW);
 }
 
 // ------------------------------------------------------------------ packing

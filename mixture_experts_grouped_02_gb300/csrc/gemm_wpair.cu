@@ -173,6 +173,10 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
   float* xchg = reinterpret_cast<float*>(smem_raw + (smem_base - smem_u32(smem_raw)) +
                                          C::kStages * C::kStageBytes);
 
+  // the earlier kernels of the stream (align, gather or the gate/up GEMM)
+  // have finished before anything they wrote is read
+  pdl_wait();
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     s_skip = (a.status != nullptr && *reinterpret_cast<volatile int32_t*>(a.status) != 0);
     s_abort = 0;
@@ -421,18 +425,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
 template <int KIND, typename T>
 cudaLaunchConfig_t wpair_config(int grid, cudaStream_t s, cudaLaunchAttribute* attr) {
   using C = WCfg<KIND, T>;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(C::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = s;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
+  return pdl_config(dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, attr, 2);
 }
 
 template <int KIND, typename T>
@@ -444,7 +437,7 @@ int max_pairs() {
     cudaGetLastError();
     return 0;
   }
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = wpair_config<KIND, T>(2, nullptr, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
@@ -462,7 +455,7 @@ cudaError_t launch(const GemmArgs& a, const CUtensorMap& tmTok, const CUtensorMa
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = wpair_config<KIND, T>(grid, s, attr);
   return cudaLaunchKernelEx(&cfg, kern, a, tmTok, tmTokS, tmW, tmWu);
 }

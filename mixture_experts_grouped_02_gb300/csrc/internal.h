@@ -17,6 +17,34 @@ constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 // the two automatic block sizes of the bf16/fp32 GEMMs.
 constexpr int kBlockM = 128;
 
+// Launch configuration with programmatic stream serialisation: the kernel
+// may be launched while the previous kernel of the stream is still running
+// and waits for it in pdl_wait() (every kernel of the path does so before it
+// reads anything an earlier kernel wrote).  cluster_x > 1 adds a cluster
+// dimension.  `attr` must hold two entries and outlive the launch call.
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     cudaLaunchAttribute* attr, unsigned cluster_x = 1) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cfg;
+}
+
 // Activation and biases of the expert FFN (moe_problem_t).
 struct Epilogue {
   int act;             // MOE_ACT_SILU / MOE_ACT_SWIGLU_CLAMP

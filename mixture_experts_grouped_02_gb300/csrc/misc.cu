@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ inv_perm, int T,
                                                       int K, int H, OutT* __restrict__ out,
                                                       const int32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (status != nullptr && *status != 0) return;
   const int h4 = H >> 2;
   const int c_end = min(h4, static_cast<int>(blockIdx.y + 1) * 256);
@@ -88,6 +90,8 @@ __device__ __forceinline__ float load_act(const void* x, int bf16, long long idx
 __global__ void __launch_bounds__(256) quantize_x_kernel(const void* __restrict__ x, int bf16,
                                                          int T, int H, uint8_t* __restrict__ xq,
                                                          float* __restrict__ row_scale) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float s_red[8];
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     const long long base = static_cast<long long>(t) * H;
@@ -120,6 +124,8 @@ __global__ void __launch_bounds__(256) quantize_x_kernel(const void* __restrict_
 __global__ void __launch_bounds__(256) quantize_gather_x_kernel(
     const void* __restrict__ x, int bf16, int T, int H, int K, const int32_t* __restrict__ inv_perm,
     uint8_t* __restrict__ xq_sorted, float* __restrict__ row_scale, const int32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (status != nullptr && *status != 0) return;
   __shared__ float s_red[8];
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
@@ -158,6 +164,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ inv_perm,
                                                           uint4* __restrict__ xs,
                                                           const int32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (status != nullptr && *status != 0) return;
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     const uint4* src = x + static_cast<long long>(t) * row_vec;
@@ -176,39 +184,43 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 cudaError_t launch_gather_rows(const void* x, int T, int row_bytes, int K, const int32_t* inv_perm,
                                void* xs, const int32_t* status, cudaStream_t s) {
   const int grid = T < 65535 ? T : 65535;
-  gather_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(x), T, row_bytes / 16, K,
-                                          inv_perm, static_cast<uint4*>(xs), status);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, s, attr);
+  return cudaLaunchKernelEx(&cfg, gather_rows_kernel, static_cast<const uint4*>(x), T,
+                            row_bytes / 16, K, inv_perm, static_cast<uint4*>(xs), status);
 }
 
 cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, int K,
                                      const int32_t* inv_perm, uint8_t* xq_sorted,
                                      float* row_scale, const int32_t* status, cudaStream_t s) {
   const int grid = T < 65535 ? T : 65535;
-  quantize_gather_x_kernel<<<grid, 256, 0, s>>>(x, x_dtype == MOE_BF16 ? 1 : 0, T, H, K, inv_perm,
-                                                xq_sorted, row_scale, status);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, s, attr);
+  return cudaLaunchKernelEx(&cfg, quantize_gather_x_kernel, x, x_dtype == MOE_BF16 ? 1 : 0, T, H,
+                            K, inv_perm, xq_sorted, row_scale, status);
 }
 
 cudaError_t launch_combine(const float* y, int splits, long long cap, const int32_t* inv_perm,
                            int T, int K, int H, int out_dtype, void* out, int32_t* status,
                            cudaStream_t s) {
   const dim3 grid(T < 65535 ? T : 65535, (H / 4 + 255) / 256);
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pdl_config(grid, dim3(256), 0, s, attr);
   if (out_dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(y, splits, cap, inv_perm, T, K, H,
-                                                        reinterpret_cast<__nv_bfloat16*>(out),
-                                                        status);
-  else
-    combine_kernel<float><<<grid, 256, 0, s>>>(y, splits, cap, inv_perm, T, K, H,
-                                                reinterpret_cast<float*>(out), status);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, y, splits, cap, inv_perm, T,
+                              K, H, reinterpret_cast<__nv_bfloat16*>(out),
+                              static_cast<const int32_t*>(status));
+  return cudaLaunchKernelEx(&cfg, combine_kernel<float>, y, splits, cap, inv_perm, T, K, H,
+                            reinterpret_cast<float*>(out), static_cast<const int32_t*>(status));
 }
 
 cudaError_t launch_quantize_x(const void* x, int x_dtype, int T, int H, uint8_t* xq,
                               float* row_scale, cudaStream_t s) {
   const int grid = T < 65535 ? T : 65535;
-  quantize_x_kernel<<<grid, 256, 0, s>>>(x, x_dtype == MOE_BF16 ? 1 : 0, T, H, xq, row_scale);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, s, attr);
+  return cudaLaunchKernelEx(&cfg, quantize_x_kernel, x, x_dtype == MOE_BF16 ? 1 : 0, T, H, xq,
+                            row_scale);
 }
 
 }  // namespace moe

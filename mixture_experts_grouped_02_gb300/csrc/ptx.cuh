@@ -364,6 +364,16 @@ __device__ __forceinline__ void tmem_wait_ld() {
 
 // ---------------------------------------------------------------- misc
 
+// Programmatic dependent launch.  pdl_wait: block until the grids this one
+// depends on have completed and their memory is visible (returns at once
+// when the kernel was launched without such a dependency).
+// pdl_launch_dependents: allow the next kernel in the stream to be launched
+// once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void report_error(int32_t* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
