@@ -323,6 +323,7 @@ def build_stages(moe, _abi, cfg, inp, dev, block_m=0, shard=None):
         part(_abi.MOE_WS_PADDED_OFFSETS)
     sorted_ids, inv = part(_abi.MOE_WS_SORTED_IDS), part(_abi.MOE_WS_INV_PERM)
     binfo, nblk = part(_abi.MOE_WS_BLOCK_INFO), part(_abi.MOE_WS_NUM_BLOCKS)
+    scratch = part(_abi.MOE_WS_ALIGN)  # empty below 16384 assignments: one-CTA align
     h = part(_abi.MOE_WS_H, torch.uint8)
     y = part(_abi.MOE_WS_Y, torch.float32)
     xq = part(_abi.MOE_WS_XQ, torch.uint8) if mx else None
@@ -343,7 +344,7 @@ def build_stages(moe, _abi, cfg, inp, dev, block_m=0, shard=None):
     stages = []
     stages.append(("align", lambda: moe.moe_align_local(
         inp.topk_ids, cfg.T, cfg.K, cfg.E, base, L if L else cfg.E, bm, counts, offs, poffs,
-        sorted_ids, inv, binfo, nblk, st, stream)))
+        sorted_ids, inv, binfo, nblk, st, stream, scratch)))
     if mx:
         stages.append(("quantize_gather_x", lambda: moe.moe_quantize_gather_x_fp8(
             inp.x, _abi.MOE_BF16, cfg.T, cfg.H, cfg.K, inv, xq, xs, st, stream)))
@@ -517,7 +518,9 @@ def run_ours(args, ws, rank, local):
             "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": len(stages) * args.steps,
+            # one kernel per stage, the align three when it runs over many CTAs
+            "gpu_launches": (len(stages) + (2 if wsp.sizes[_abi.MOE_WS_ALIGN] else 0)) *
+                            args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

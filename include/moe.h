@@ -129,7 +129,9 @@ typedef enum {
     MOE_WS_X_SCALE = 9,        /* fp32[T]      (MX weights only)            */
     MOE_WS_H = 10,             /* act or e4m3 [cap][I]                      */
     MOE_WS_Y = 11,             /* fp32[splits][cap][H]                      */
-    MOE_WS_NUM = 12
+    MOE_WS_ALIGN = 12,         /* int32 per-warp counts of the align of     */
+                               /* large batches (T*K >= 16384), else empty  */
+    MOE_WS_NUM = 13
 } moe_ws_part_t;
 
 /* Static string for a status code (never NULL). */
@@ -198,11 +200,22 @@ int moe_align(const int32_t* topk_ids, int T, int K, int E, int block_m, int32_t
  * Source: "MOE Bmm1 Fused Gather", init_routing_data (the local experts'
  * histogram of one shard).  1 <= local_experts <= 1024,
  * expert_base + local_experts <= E, else MOE_ERR_INVALID_ARG /
- * MOE_ERR_UNSUPPORTED. */
+ * MOE_ERR_UNSUPPORTED.
+ * scratch / scratch_bytes: device memory of at least
+ * moe_align_scratch_bytes(T, K, local_experts) bytes (16-byte aligned, may
+ * be NULL when that is 0 or to keep one CTA).  With it, batches of 16384 or
+ * more assignments are aligned by many CTAs (per-warp histograms in the
+ * scratch, one scan CTA, a scatter over many CTAs) -- the same outputs,
+ * as moe_forward does; without it, by one CTA. */
 int moe_align_local(const int32_t* topk_ids, int T, int K, int E, int expert_base,
                     int local_experts, int block_m, int32_t* counts, int32_t* offsets,
                     int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
-                    int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream);
+                    int32_t* block_info, int32_t* num_blocks, void* scratch,
+                    size_t scratch_bytes, int32_t* dev_status, void* stream);
+
+/* Scratch bytes moe_align_local uses for T*K assignments over
+ * local_experts experts: 0 below 16384 assignments. */
+size_t moe_align_scratch_bytes(int T, int K, int local_experts);
 
 /* ---- routing + align ------------------------------------------------------
  * The router step before the path, folded into align.  Source: "MOE Bmm1

@@ -14,7 +14,7 @@ from . import _abi
 from ._abi import (MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP, MOE_BF16, MOE_E2M1_MX, MOE_E4M3, MOE_F32,
                    MoEError, Problem, moe_abi_version,
                    moe_align, moe_align_capacity, moe_align_local, moe_combine, moe_forward,
-                   moe_route_align,
+                   moe_route_align, moe_align_scratch_bytes,
                    moe_forward_noalloc, moe_gather_rows, moe_gemm1_silu, moe_gemm2_default_splits,
                    moe_gemm2_weighted, moe_get_device_status, moe_mx_packed_bytes,
                    moe_pack_mx_weights, moe_quantize_gather_x_fp8, moe_quantize_x_fp8,
@@ -24,6 +24,7 @@ __all__ = ["MOE_ACT_SILU", "MOE_ACT_SWIGLU_CLAMP", "MoEError", "Problem", "make_
            "pack_mx", "moe_forward_noalloc", "moe_mx_packed_bytes", "moe_pack_mx_weights",
            "moe_quantize_gather_x_fp8", "moe_gather_rows",
            "moe_abi_version", "moe_align", "moe_align_capacity", "moe_align_local",
+           "moe_align_scratch_bytes",
            "moe_route_align", "route_align",
            "moe_combine", "moe_forward",
            "moe_gemm1_silu", "moe_gemm2_default_splits", "moe_gemm2_weighted",
@@ -66,9 +67,11 @@ def make_problem(T, H, I, E, K, act="bf16", weight=None, block_m=0, h_scale=1.0,
 
 
 def align(topk_ids: torch.Tensor, E: int, block_m: int = 128, dev_status=None, stream=None,
-          expert_base: int = 0, local_experts: int = 0):
-    """Run moe_align (moe_align_local for a shard) on (T, K) int32 ids;
-    returns the outputs as a dict of device tensors."""
+          expert_base: int = 0, local_experts: int = 0, many_cta: bool = True):
+    """Run moe_align_local on (T, K) int32 ids; returns the outputs as a
+    dict of device tensors.  many_cta: give the call the scratch with which
+    batches of 16384 or more ids are aligned by many CTAs (as moe_forward
+    does); False keeps the one-CTA kernel."""
     T, K = topk_ids.shape
     L = local_experts if local_experts > 0 else E
     cap = moe_align_capacity(T, K, L, block_m)
@@ -79,9 +82,11 @@ def align(topk_ids: torch.Tensor, E: int, block_m: int = 128, dev_status=None, s
                inv_perm=torch.empty(T * K, **i32),
                block_info=torch.empty((cap // block_m, 4), **i32),
                num_blocks=torch.empty(1, **i32))
+    nbytes = moe_align_scratch_bytes(T, K, L) if many_cta else 0
+    scratch = torch.empty(nbytes // 4, **i32) if nbytes > 0 else None
     moe_align_local(topk_ids, T, K, E, expert_base, L, block_m, out["counts"], out["offsets"],
                     out["padded_offsets"], out["sorted_ids"], out["inv_perm"], out["block_info"],
-                    out["num_blocks"], dev_status, stream)
+                    out["num_blocks"], dev_status, stream, scratch)
     return out
 
 

@@ -28,7 +28,7 @@ MOE_F32, MOE_BF16, MOE_E4M3, MOE_E2M1_MX = 0, 1, 2, 3
 
 (MOE_WS_STATUS, MOE_WS_COUNTS, MOE_WS_OFFSETS, MOE_WS_PADDED_OFFSETS, MOE_WS_SORTED_IDS,
  MOE_WS_INV_PERM, MOE_WS_BLOCK_INFO, MOE_WS_NUM_BLOCKS, MOE_WS_XQ, MOE_WS_X_SCALE, MOE_WS_H,
- MOE_WS_Y, MOE_WS_NUM) = range(13)
+ MOE_WS_Y, MOE_WS_ALIGN, MOE_WS_NUM) = range(14)
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_align_capacity",
@@ -36,7 +36,7 @@ EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_a
            "moe_quantize_x_fp8", "moe_gemm1_silu", "moe_gemm2_weighted", "moe_combine",
            "moe_forward", "moe_forward_noalloc", "moe_get_device_status", "moe_mx_packed_bytes",
            "moe_pack_mx_weights", "moe_quantize_gather_x_fp8", "moe_device_info",
-           "moe_gather_rows", "moe_align_local", "moe_route_align")
+           "moe_gather_rows", "moe_align_local", "moe_route_align", "moe_align_scratch_bytes")
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
 MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP = 0, 1
@@ -105,7 +105,9 @@ def _declare(L):
     L.moe_route_align.restype = i32
     L.moe_route_align.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32] + [vp] * 9 + [vp, vp]
     L.moe_align_local.restype = i32
-    L.moe_align_local.argtypes = [vp, i32, i32, i32, i32, i32, i32] + [vp] * 8 + [vp]
+    L.moe_align_local.argtypes = [vp, i32, i32, i32, i32, i32, i32] + [vp] * 7 + [vp, sz] + [vp, vp]
+    L.moe_align_scratch_bytes.restype = sz
+    L.moe_align_scratch_bytes.argtypes = [i32, i32, i32]
     L.moe_quantize_x_fp8.restype = i32
     L.moe_quantize_x_fp8.argtypes = [vp, i32, i32, i32, vp, vp, vp]
     L.moe_gather_rows.restype = i32
@@ -204,11 +206,16 @@ def moe_align(topk_ids, T, K, E, block_m, counts, offsets, padded_offsets, sorte
 
 def moe_align_local(topk_ids, T, K, E, expert_base, local_experts, block_m, counts, offsets,
                     padded_offsets, sorted_ids, inv_perm, block_info, num_blocks, dev_status=None,
-                    stream=None):
+                    stream=None, scratch=None):
+    nbytes = 0 if scratch is None else scratch.numel() * scratch.element_size()
     _check(lib().moe_align_local(_p(topk_ids), T, K, E, expert_base, local_experts, block_m,
                                  _p(counts), _p(offsets), _p(padded_offsets), _p(sorted_ids),
-                                 _p(inv_perm), _p(block_info), _p(num_blocks), _p(dev_status),
-                                 _stream(stream)), "moe_align_local")
+                                 _p(inv_perm), _p(block_info), _p(num_blocks), _p(scratch),
+                                 nbytes, _p(dev_status), _stream(stream)), "moe_align_local")
+
+
+def moe_align_scratch_bytes(T, K, local_experts):
+    return int(lib().moe_align_scratch_bytes(T, K, local_experts))
 
 
 def moe_route_align(logits, logit_dtype, T, E, K, expert_base, local_experts, block_m, topk_ids,

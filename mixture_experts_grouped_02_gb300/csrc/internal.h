@@ -153,6 +153,16 @@ inline int mx_scale_groups(int rows) { return 2 * ((rows + 191) / 192); }
 inline int mx_padded_k(int K) { return (K + 127) / 128 * 128; }
 
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
+// The many-CTA align of large batches: CTAs of 8 warps, each warp counting a
+// chunk of align_multi_chunk(n) ids; int32 scratch of per-warp counts
+// whist[warps][e_local] and per-CTA totals ctot[ctas][e_local], then one
+// scan CTA over the CTA totals, then the scatter.  Same outputs as
+// launch_align (num_blocks is cleared with a memset first).
+constexpr long long kAlignMultiMin = 16384;
+int align_multi_chunk(long long n_assign);
+int align_multi_warps(long long n_assign);
+size_t align_multi_scratch_ints(long long n_assign, int e_local);
+cudaError_t launch_align_multi(const AlignArgs& a, int32_t* scratch, cudaStream_t s);
 // The routing step alone, a warp per token over many CTAs (large batches).
 cudaError_t launch_route(const RouteArgs& r, cudaStream_t s);
 // Largest batch whose routing the single-CTA align kernel does itself.

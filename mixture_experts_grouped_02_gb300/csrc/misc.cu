@@ -13,66 +13,87 @@ namespace {
 // expert another shard holds) adds nothing.  Source: the index_add of the "Current
 // PyTorch path" in "factor_moe_fused_gemm.cu" and its
 // weighted_scatter_add_kernel, made deterministic: each token owns its row,
-// so no atomics and a fixed summation order.  CTA (x, y) handles token rows
-// x, x + gridDim.x, ... and the y-th run of 1024 columns of them, so that a
-// handful of tokens still spreads over many SMs; 16-byte loads of y.
+// so no atomics and a fixed summation order.  CTA (x, y) handles groups of
+// `tpc` token rows x*tpc, (x + gridDim.x)*tpc, ... and the y-th run of 1024
+// columns of them, so that a handful of tokens still spreads over many SMs;
+// 16-byte loads of y.  With one split, a thread issues the loads of all
+// tpc*K <= 8 assignments of its group before it sums any (tpc = 8/K tokens:
+// four for top-2), which keeps enough bytes in flight when K is small.
 constexpr int kCombineBatch = 8;
+
+template <typename OutT>
+__device__ __forceinline__ void store_out4(OutT* row, int c, float4 acc) {
+  if constexpr (sizeof(OutT) == 2) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(row)[c] = pk;
+  } else {
+    reinterpret_cast<float4*>(row)[c] = acc;
+  }
+}
+
+__device__ __forceinline__ void add4(float4& acc, const float4 v) {
+  acc.x += v.x;
+  acc.y += v.y;
+  acc.z += v.z;
+  acc.w += v.w;
+}
 
 template <typename OutT>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int splits,
                                                       long long cap,
                                                       const int32_t* __restrict__ inv_perm, int T,
-                                                      int K, int H, OutT* __restrict__ out,
+                                                      int K, int H, int tpc,
+                                                      OutT* __restrict__ out,
                                                       const int32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   if (status != nullptr && *status != 0) return;
   const int h4 = H >> 2;
   const int c_end = min(h4, static_cast<int>(blockIdx.y + 1) * 256);
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    const int32_t* slots = inv_perm + static_cast<long long>(t) * K;
+  const int n = K * tpc;  // assignments of one group
+  for (int t0 = blockIdx.x * tpc; t0 < T; t0 += gridDim.x * tpc) {
+    const int32_t* slots = inv_perm + static_cast<long long>(t0) * K;
+    const int n_valid = min(n, (T - t0) * K);
     for (int c = blockIdx.y * 256 + threadIdx.x; c < c_end; c += blockDim.x) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (splits == 1 && K <= kCombineBatch) {
-        // all K loads in flight at once, then the sum in k order
+      if (splits == 1 && n <= kCombineBatch) {
         float4 v[kCombineBatch];
+        int slot[kCombineBatch];
 #pragma unroll
-        for (int k = 0; k < kCombineBatch; ++k)
-          if (k < K && slots[k] >= 0)
-            v[k] = __ldg(reinterpret_cast<const float4*>(y + static_cast<long long>(slots[k]) * H) +
+        for (int j = 0; j < kCombineBatch; ++j) {
+          slot[j] = j < n_valid ? slots[j] : -1;
+          if (slot[j] >= 0)
+            v[j] = __ldg(reinterpret_cast<const float4*>(y + static_cast<long long>(slot[j]) * H) +
                          c);
+        }
+        // the sum of each token in k order, stored after its last assignment
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < kCombineBatch; ++k)
-          if (k < K && slots[k] >= 0) {
-            acc.x += v[k].x;
-            acc.y += v[k].y;
-            acc.z += v[k].z;
-            acc.w += v[k].w;
-          }
-      } else {
-        for (int k = 0; k < K; ++k) {
-          const long long row = slots[k];
-          if (row < 0) continue;
-          for (int q = 0; q < splits; ++q) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(
-                                       y + (static_cast<long long>(q) * cap + row) * H) +
-                                   c);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+        for (int j = 0; j < kCombineBatch; ++j) {
+          if (j < n_valid) {
+            if (slot[j] >= 0) add4(acc, v[j]);
+            if ((j + 1) % K == 0) {
+              store_out4(out + static_cast<long long>(t0 + j / K) * H, c, acc);
+              acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
           }
         }
-      }
-      if constexpr (sizeof(OutT) == 2) {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&lo);
-        pk.y = *reinterpret_cast<uint32_t*>(&hi);
-        reinterpret_cast<uint2*>(out + static_cast<long long>(t) * H)[c] = pk;
       } else {
-        reinterpret_cast<float4*>(out + static_cast<long long>(t) * H)[c] = acc;
+        for (int t = t0; t < min(T, t0 + tpc); ++t) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int k = 0; k < K; ++k) {
+            const long long row = inv_perm[static_cast<long long>(t) * K + k];
+            if (row < 0) continue;
+            for (int q = 0; q < splits; ++q)
+              add4(acc, __ldg(reinterpret_cast<const float4*>(
+                                  y + (static_cast<long long>(q) * cap + row) * H) +
+                              c));
+          }
+          store_out4(out + static_cast<long long>(t) * H, c, acc);
+        }
       }
     }
   }
@@ -203,14 +224,16 @@ cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, i
 cudaError_t launch_combine(const float* y, int splits, long long cap, const int32_t* inv_perm,
                            int T, int K, int H, int out_dtype, void* out, int32_t* status,
                            cudaStream_t s) {
-  const dim3 grid(T < 65535 ? T : 65535, (H / 4 + 255) / 256);
+  const int tpc = splits == 1 && K <= kCombineBatch ? kCombineBatch / K : 1;
+  const int groups = (T + tpc - 1) / tpc;
+  const dim3 grid(groups < 65535 ? groups : 65535, (H / 4 + 255) / 256);
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pdl_config(grid, dim3(256), 0, s, attr);
   if (out_dtype == MOE_BF16)
     return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, y, splits, cap, inv_perm, T,
-                              K, H, reinterpret_cast<__nv_bfloat16*>(out),
+                              K, H, tpc, reinterpret_cast<__nv_bfloat16*>(out),
                               static_cast<const int32_t*>(status));
-  return cudaLaunchKernelEx(&cfg, combine_kernel<float>, y, splits, cap, inv_perm, T, K, H,
+  return cudaLaunchKernelEx(&cfg, combine_kernel<float>, y, splits, cap, inv_perm, T, K, H, tpc,
                             reinterpret_cast<float*>(out), static_cast<const int32_t*>(status));
 }
 

@@ -20,7 +20,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 constexpr size_t kWsAlign = 1024;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxDevices = 64;
@@ -194,6 +194,7 @@ void layout_of(const moe_problem_t* p, Layout* L) {
   sz[MOE_WS_X_SCALE] = mx ? 4ull * p->T : 0;
   sz[MOE_WS_H] = static_cast<size_t>(cap) * p->I * (mx ? 1 : act_bytes(p->act));
   sz[MOE_WS_Y] = 4ull * splits * static_cast<size_t>(cap) * p->H;
+  sz[MOE_WS_ALIGN] = na >= kAlignMultiMin ? 4 * align_multi_scratch_ints(na, local_experts(p)) : 0;
   size_t off = 0;
   for (int i = 0; i < MOE_WS_NUM; ++i) {
     L->off[i] = off;
@@ -552,13 +553,22 @@ int moe_align(const int32_t* topk_ids, int T, int K, int E, int block_m, int32_t
               int32_t* offsets, int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
               int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream) {
   return moe_align_local(topk_ids, T, K, E, 0, E, block_m, counts, offsets, padded_offsets,
-                         sorted_ids, inv_perm, block_info, num_blocks, dev_status, stream);
+                         sorted_ids, inv_perm, block_info, num_blocks, nullptr, 0, dev_status,
+                         stream);
+}
+
+size_t moe_align_scratch_bytes(int T, int K, int local_experts) {
+  if (T < 0 || K <= 0 || local_experts <= 0) return 0;
+  const long long na = static_cast<long long>(T) * K;
+  if (na < kAlignMultiMin) return 0;
+  return 4 * align_multi_scratch_ints(na, local_experts);
 }
 
 int moe_align_local(const int32_t* topk_ids, int T, int K, int E, int expert_base,
                     int local_experts, int block_m, int32_t* counts, int32_t* offsets,
                     int32_t* padded_offsets, int32_t* sorted_ids, int32_t* inv_perm,
-                    int32_t* block_info, int32_t* num_blocks, int32_t* dev_status, void* stream) {
+                    int32_t* block_info, int32_t* num_blocks, void* scratch,
+                    size_t scratch_bytes, int32_t* dev_status, void* stream) {
   if (T < 0 || K <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
   if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128 && block_m != 256)
     return MOE_ERR_INVALID_ARG;
@@ -572,6 +582,30 @@ int moe_align_local(const int32_t* topk_ids, int T, int K, int E, int expert_bas
       !block_info || !num_blocks)
     return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(block_info) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_align_scratch_bytes(T, K, local_experts);
+  if (need > 0 && scratch != nullptr) {
+    if (scratch_bytes < need || (reinterpret_cast<uintptr_t>(scratch) & 15u) != 0)
+      return MOE_ERR_WORKSPACE;
+    AlignArgs al;
+    std::memset(&al, 0, sizeof(al));
+    al.ids = topk_ids;
+    al.n_assign = T * K;
+    al.E = E;
+    al.e_base = expert_base;
+    al.e_local = local_experts;
+    al.block_m = block_m;
+    al.cap = capacity(T, K, local_experts, block_m);
+    al.counts = counts;
+    al.offsets = offsets;
+    al.padded_offsets = padded_offsets;
+    al.sorted_ids = sorted_ids;
+    al.inv_perm = inv_perm;
+    al.block_info = block_info;
+    al.num_blocks = num_blocks;
+    al.status = dev_status;
+    return cuda_status(launch_align_multi(al, static_cast<int32_t*>(scratch),
+                                          static_cast<cudaStream_t>(stream)));
+  }
   return run_align(topk_ids, T, K, E, expert_base, local_experts, block_m, counts, offsets,
                    padded_offsets, sorted_ids, inv_perm, block_info, num_blocks, dev_status,
                    static_cast<cudaStream_t>(stream));
@@ -733,11 +767,12 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
   const int bm = block_m_of(p);
 
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
-  rc = run_align(topk_ids, p->T, p->K, p->E, p->expert_base, local_experts(p), bm,
-                 reinterpret_cast<int32_t*>(part(MOE_WS_COUNTS)),
-                 reinterpret_cast<int32_t*>(part(MOE_WS_OFFSETS)),
-                 reinterpret_cast<int32_t*>(part(MOE_WS_PADDED_OFFSETS)), sorted_ids, inv_perm,
-                 block_info, num_blocks, status, s);
+  rc = moe_align_local(topk_ids, p->T, p->K, p->E, p->expert_base, local_experts(p), bm,
+                       reinterpret_cast<int32_t*>(part(MOE_WS_COUNTS)),
+                       reinterpret_cast<int32_t*>(part(MOE_WS_OFFSETS)),
+                       reinterpret_cast<int32_t*>(part(MOE_WS_PADDED_OFFSETS)), sorted_ids,
+                       inv_perm, block_info, num_blocks, part(MOE_WS_ALIGN),
+                       L.size[MOE_WS_ALIGN], status, stream);
   if (rc != MOE_OK) return rc;
   if (is_mx(p)) {
     uint8_t* xq = part(MOE_WS_XQ);

@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
     L = _abi.lib()
     for name in declared_functions():
         assert hasattr(L, name), name
-    assert _abi.moe_abi_version() == 2
+    assert _abi.moe_abi_version() == 3
 
 
 def test_status_strings():
@@ -137,8 +137,20 @@ def test_entry_points_reject_bad_arguments_before_launch():
                              None) == _abi.MOE_OK
     # expert shards: the range must lie inside [0, E)
     for base, local in ((-1, 2), (7, 2), (0, 0), (0, 9)):
-        assert L.moe_align_local(fake, 4, 2, 8, base, local, 128, *([fake] * 7), None, None) == \
-            _abi.MOE_ERR_INVALID_ARG
+        assert L.moe_align_local(fake, 4, 2, 8, base, local, 128, *([fake] * 7), None, 0, None,
+                                 None) == _abi.MOE_ERR_INVALID_ARG
+    # the many-CTA align: scratch only from 16384 assignments on, one int per
+    # (warp of 256 ids, local expert) and per (CTA of 8 warps, local expert);
+    # too small a scratch is refused
+    assert L.moe_align_scratch_bytes(2048, 4, 64) == 0
+    assert L.moe_align_scratch_bytes(4096, 4, 64) == 4 * (64 + 8) * 64
+    assert L.moe_align_scratch_bytes(16384, 8, 256) == 4 * (512 + 64) * 256
+    assert L.moe_align_scratch_bytes(20001, 6, 64) == 4 * (59 * 8 + 59) * 64  # 469 warps
+    # at most 4864 warps: larger chunks for the largest batches
+    big = L.moe_align_scratch_bytes(1 << 20, 32, 1024)
+    assert big == 4 * (607 * 8 + 607) * 1024  # chunks of 6912 ids: 4855 warps
+    assert L.moe_align_local(fake, 4096, 4, 64, 0, 64, 128, *([fake] * 7), fake, 64, None,
+                             None) == _abi.MOE_ERR_WORKSPACE
     for base, local in ((1, 0), (-1, 3), (6, 3)):
         bad = make_problem(16, 128, 256, 8, 2, "bf16", expert_base=base, local_experts=local)
         assert _abi.moe_workspace_size(bad) == 0

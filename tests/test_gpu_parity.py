@@ -88,6 +88,46 @@ def test_align_local_bit_exact(case, shard):
     assert int(got["num_blocks"].item()) == ref["num_blocks"]
 
 
+ALIGN_MANY_CTA_CASES = [
+    # T, K, E, block_m, routing, (expert_base, local_experts); T*K >= 16384
+    # assignments go to the many-CTA align (chunks of 1024 ids per warp)
+    (4096, 4, 64, 128, "skewed", (0, 64)),
+    (16384, 8, 256, 256, "normal", (0, 256)),
+    (20001, 6, 160, 16, "skewed", (32, 64)),   # ragged last chunk, a shard
+    (3000, 8, 1024, 64, "normal", (0, 1024)),  # the most experts
+    (8192, 2, 8, 256, "skewed", (7, 1)),       # one local expert
+]
+
+
+@pytest.mark.parametrize("case,shard", [(c[:5], c[5]) for c in ALIGN_MANY_CTA_CASES],
+                         ids=lambda c: "_".join(map(str, c)))
+def test_align_many_cta_bit_exact(case, shard):
+    T, K, E, bm, kind = case
+    base, L = shard
+    assert moe.moe_align_scratch_bytes(T, K, L) > 0
+    ids = pins.align_ids(T, K, E, kind)
+    ref = oracle.align(ids, E, bm, expert_base=base, local_experts=L)
+    d_ids = torch.from_numpy(ids).cuda()
+    st = _status()
+    got = moe.align(d_ids, E, bm, dev_status=st, expert_base=base, local_experts=L)
+    one = moe.align(d_ids, E, bm, dev_status=st, expert_base=base, local_experts=L,
+                    many_cta=False)
+    assert moe.moe_get_device_status(st) == 0
+    for k in ("counts", "offsets", "padded_offsets", "sorted_ids", "inv_perm", "block_info"):
+        assert np.array_equal(got[k].cpu().numpy(), ref[k]), k
+        assert torch.equal(got[k], one[k]), k
+    assert int(got["num_blocks"].item()) == ref["num_blocks"]
+
+
+def test_align_many_cta_bad_id_sets_status():
+    ids = pins.align_ids(4096, 4, 64, "normal")
+    ids[4000, 3] = 64  # outside [0, E), in the last chunk
+    st = _status()
+    got = moe.align(torch.from_numpy(ids).cuda(), 64, 128, dev_status=st)
+    assert moe.moe_get_device_status(st) == _abi.MOE_ERR_DEVICE_BAD_ID
+    assert int(got["num_blocks"].item()) == 0
+
+
 ROUTE_CASES = [
     # T, E, K, logit dtype, kind; up to 1024 tokens the align kernel routes
     (37, 8, 2, torch.float32, "normal"),
@@ -220,6 +260,10 @@ def test_gemm2_weighted_stage(case, splits, bm):
     got = y[:, torch.from_numpy(rows).long().cuda()].sum(0)
     tol = 1e-4 if dt == "bf16" else 5e-3  # bf16 products are exact; tf32 rounds operands
     assert_close(got, ref, max_abs=2e-2, rel_l2=tol, what="y")
+    # padding rows are never written
+    pad = np.nonzero(al_ref["sorted_ids"] >= T * K)[0]
+    if len(pad):
+        assert torch.isnan(y[:, torch.from_numpy(pad).long().cuda()]).all()
 
 
 @pytest.mark.parametrize("splits", [1, 2])
@@ -345,11 +389,22 @@ def test_forward_decode_full_size(name):
 def test_forward_prefill_full_size_sampled(name):
     cfg = gen.config(name)
     inp = generate(cfg, seed=0, device="cuda")
-    out, _ = _run_forward(inp, cfg, poison=False)
+    out, ws = _run_forward(inp, cfg, poison=False)
     toks = sample_tokens(cfg.T, 6, seed=1)
     ref = oracle_forward_tokens(inp, toks)
     assert_close(out[torch.from_numpy(toks).long().cuda()], ref, what=name)
     assert torch.isfinite(out.float()).all()
+    # the align's outputs in the workspace (over many CTAs from T*K = 16384
+    # on, the DeepSeek-V3 shape), bit for bit against the oracle's
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype)
+    al = oracle.align(inp.topk_ids.cpu().numpy(), cfg.E, moe.moe_resolve_block_m(p))
+    cap = len(al["sorted_ids"])
+    for k, part, n in (("counts", _abi.MOE_WS_COUNTS, cfg.E),
+                       ("padded_offsets", _abi.MOE_WS_PADDED_OFFSETS, cfg.E + 1),
+                       ("sorted_ids", _abi.MOE_WS_SORTED_IDS, cap),
+                       ("inv_perm", _abi.MOE_WS_INV_PERM, cfg.T * cfg.K)):
+        assert np.array_equal(ws.part(part, torch.int32)[:n].cpu().numpy(), al[k]), k
+    assert int(ws.part(_abi.MOE_WS_NUM_BLOCKS, torch.int32)[0]) == al["num_blocks"]
     del inp, out
     torch.cuda.empty_cache()
 
