@@ -14,11 +14,12 @@ namespace {
 // PyTorch path" in "factor_moe_fused_gemm.cu" and its
 // weighted_scatter_add_kernel, made deterministic: each token owns its row,
 // so no atomics and a fixed summation order.  CTA (x, y) handles groups of
-// `tpc` token rows x*tpc, (x + gridDim.x)*tpc, ... and the y-th run of 1024
+// TPC token rows x*TPC, (x + gridDim.x)*TPC, ... and the y-th run of 1024
 // columns of them, so that a handful of tokens still spreads over many SMs;
 // 16-byte loads of y.  With one split, a thread issues the loads of all
-// tpc*K <= 8 assignments of its group before it sums any (tpc = 8/K tokens:
-// four for top-2), which keeps enough bytes in flight when K is small.
+// TPC*K <= 8 assignments of its group before it sums any (TPC = 4 tokens for
+// top-2, 2 for top-3/4, 1 above), which keeps enough bytes in flight when K
+// is small.
 constexpr int kCombineBatch = 8;
 
 template <typename OutT>
@@ -42,58 +43,65 @@ __device__ __forceinline__ void add4(float4& acc, const float4 v) {
   acc.w += v.w;
 }
 
-template <typename OutT>
+// One split, K <= kCombineBatch / TPC: the loads of the group's TPC tokens
+// all in flight, then each token's sum in k order.
+template <typename OutT, int TPC>
+__device__ __forceinline__ void combine_group(const float* __restrict__ y,
+                                              const int32_t* __restrict__ inv_perm, int T, int K,
+                                              int H, int t0, int c, OutT* __restrict__ out) {
+  constexpr int KM = kCombineBatch / TPC;
+  float4 v[TPC][KM];
+  unsigned live = 0;  // bit u*KM + k: assignment k of token t0 + u has a slot here
+#pragma unroll
+  for (int u = 0; u < TPC; ++u)
+#pragma unroll
+    for (int k = 0; k < KM; ++k)
+      if (k < K && t0 + u < T) {
+        const int sl = inv_perm[static_cast<long long>(t0 + u) * K + k];
+        if (sl >= 0) {
+          v[u][k] = __ldg(reinterpret_cast<const float4*>(y + static_cast<long long>(sl) * H) + c);
+          live |= 1u << (u * KM + k);
+        }
+      }
+#pragma unroll
+  for (int u = 0; u < TPC; ++u) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < KM; ++k)
+      if ((live >> (u * KM + k)) & 1u) add4(acc, v[u][k]);
+    if (t0 + u < T) store_out4(out + static_cast<long long>(t0 + u) * H, c, acc);
+  }
+}
+
+// TPC > 1 is launched only with one split and K <= kCombineBatch / TPC.
+template <typename OutT, int TPC>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int splits,
                                                       long long cap,
                                                       const int32_t* __restrict__ inv_perm, int T,
-                                                      int K, int H, int tpc,
-                                                      OutT* __restrict__ out,
+                                                      int K, int H, OutT* __restrict__ out,
                                                       const int32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   if (status != nullptr && *status != 0) return;
   const int h4 = H >> 2;
   const int c_end = min(h4, static_cast<int>(blockIdx.y + 1) * 256);
-  const int n = K * tpc;  // assignments of one group
-  for (int t0 = blockIdx.x * tpc; t0 < T; t0 += gridDim.x * tpc) {
-    const int32_t* slots = inv_perm + static_cast<long long>(t0) * K;
-    const int n_valid = min(n, (T - t0) * K);
+  for (int t0 = blockIdx.x * TPC; t0 < T; t0 += gridDim.x * TPC) {
     for (int c = blockIdx.y * 256 + threadIdx.x; c < c_end; c += blockDim.x) {
-      if (splits == 1 && n <= kCombineBatch) {
-        float4 v[kCombineBatch];
-        int slot[kCombineBatch];
-#pragma unroll
-        for (int j = 0; j < kCombineBatch; ++j) {
-          slot[j] = j < n_valid ? slots[j] : -1;
-          if (slot[j] >= 0)
-            v[j] = __ldg(reinterpret_cast<const float4*>(y + static_cast<long long>(slot[j]) * H) +
-                         c);
-        }
-        // the sum of each token in k order, stored after its last assignment
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < kCombineBatch; ++j) {
-          if (j < n_valid) {
-            if (slot[j] >= 0) add4(acc, v[j]);
-            if ((j + 1) % K == 0) {
-              store_out4(out + static_cast<long long>(t0 + j / K) * H, c, acc);
-              acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-          }
-        }
+      if constexpr (TPC > 1) {
+        combine_group<OutT, TPC>(y, inv_perm, T, K, H, t0, c, out);
+      } else if (splits == 1 && K <= kCombineBatch) {
+        combine_group<OutT, 1>(y, inv_perm, T, K, H, t0, c, out);
       } else {
-        for (int t = t0; t < min(T, t0 + tpc); ++t) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int k = 0; k < K; ++k) {
-            const long long row = inv_perm[static_cast<long long>(t) * K + k];
-            if (row < 0) continue;
-            for (int q = 0; q < splits; ++q)
-              add4(acc, __ldg(reinterpret_cast<const float4*>(
-                                  y + (static_cast<long long>(q) * cap + row) * H) +
-                              c));
-          }
-          store_out4(out + static_cast<long long>(t) * H, c, acc);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < K; ++k) {
+          const long long row = inv_perm[static_cast<long long>(t0) * K + k];
+          if (row < 0) continue;
+          for (int q = 0; q < splits; ++q)
+            add4(acc, __ldg(reinterpret_cast<const float4*>(
+                                y + (static_cast<long long>(q) * cap + row) * H) +
+                            c));
         }
+        store_out4(out + static_cast<long long>(t0) * H, c, acc);
       }
     }
   }
@@ -224,17 +232,30 @@ cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, i
 cudaError_t launch_combine(const float* y, int splits, long long cap, const int32_t* inv_perm,
                            int T, int K, int H, int out_dtype, void* out, int32_t* status,
                            cudaStream_t s) {
-  const int tpc = splits == 1 && K <= kCombineBatch ? kCombineBatch / K : 1;
+  // tokens per group: all loads of a group in flight at once (one split)
+  const int tpc = splits != 1 ? 1 : K <= 1 ? 8 : K <= 2 ? 4 : K <= 4 ? 2 : 1;
   const int groups = (T + tpc - 1) / tpc;
   const dim3 grid(groups < 65535 ? groups : 65535, (H / 4 + 255) / 256);
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pdl_config(grid, dim3(256), 0, s, attr);
-  if (out_dtype == MOE_BF16)
-    return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, y, splits, cap, inv_perm, T,
-                              K, H, tpc, reinterpret_cast<__nv_bfloat16*>(out),
-                              static_cast<const int32_t*>(status));
-  return cudaLaunchKernelEx(&cfg, combine_kernel<float>, y, splits, cap, inv_perm, T, K, H, tpc,
-                            reinterpret_cast<float*>(out), static_cast<const int32_t*>(status));
+  const int32_t* st = static_cast<const int32_t*>(status);
+  if (out_dtype == MOE_BF16) {
+    using bf16 = __nv_bfloat16;
+    bf16* o = reinterpret_cast<bf16*>(out);
+    switch (tpc) {
+      case 8: return cudaLaunchKernelEx(&cfg, combine_kernel<bf16, 8>, y, splits, cap, inv_perm, T, K, H, o, st);
+      case 4: return cudaLaunchKernelEx(&cfg, combine_kernel<bf16, 4>, y, splits, cap, inv_perm, T, K, H, o, st);
+      case 2: return cudaLaunchKernelEx(&cfg, combine_kernel<bf16, 2>, y, splits, cap, inv_perm, T, K, H, o, st);
+      default: return cudaLaunchKernelEx(&cfg, combine_kernel<bf16, 1>, y, splits, cap, inv_perm, T, K, H, o, st);
+    }
+  }
+  float* o = reinterpret_cast<float*>(out);
+  switch (tpc) {
+    case 8: return cudaLaunchKernelEx(&cfg, combine_kernel<float, 8>, y, splits, cap, inv_perm, T, K, H, o, st);
+    case 4: return cudaLaunchKernelEx(&cfg, combine_kernel<float, 4>, y, splits, cap, inv_perm, T, K, H, o, st);
+    case 2: return cudaLaunchKernelEx(&cfg, combine_kernel<float, 2>, y, splits, cap, inv_perm, T, K, H, o, st);
+    default: return cudaLaunchKernelEx(&cfg, combine_kernel<float, 1>, y, splits, cap, inv_perm, T, K, H, o, st);
+  }
 }
 
 cudaError_t launch_quantize_x(const void* x, int x_dtype, int T, int H, uint8_t* xq,
