@@ -77,7 +77,7 @@ struct WCfg {
   static constexpr int kRowBytes = 128;
   static constexpr int kBK = kRowBytes / sizeof(T);
   static constexpr int kUmmaK = 32 / sizeof(T);
-  static constexpr int kStages = 6;
+  static constexpr int kStages = KIND == kDown ? 7 : 6;  // down: no exchange buffer, room for 7
   static constexpr int kABytes = kWRows * kRowBytes;            // 16 KB of weights
   static constexpr int kBigRows = kNMax / 2;                    // token box rows
   static constexpr int kSmallRows = 16;
@@ -101,9 +101,9 @@ __device__ __forceinline__ float activate(const Epilogue& ep, float g, float u) 
   if (ep.act == MOE_ACT_SWIGLU_CLAMP) {
     g = fminf(g, ep.limit);
     u = fmaxf(fminf(u, ep.limit), -ep.limit);
-    return g / (1.0f + __expf(-ep.alpha * g)) * (u + 1.0f);
+    return __fdividef(g, 1.0f + __expf(-ep.alpha * g)) * (u + 1.0f);
   }
-  return g / (1.0f + __expf(-g)) * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 __device__ __forceinline__ void settle(uint64_t ns) {
@@ -371,14 +371,34 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
           named_bar_sync(1 + pq, 64);
           // gate warp: tokens c0..c0+15; up warp: tokens c0+16..c0+31
           const int nb = gate_warp ? c0 : c0 + 16;
-          if (j < a.I) {
+          float hv[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float g = gate_warp ? __uint_as_float(v[i]) + bias : x_g[i * 32 + lane];
-              const float u = gate_warp ? x_u[i * 32 + lane] : __uint_as_float(v[16 + i]) + bias;
-              if (nb + i < valid)
-                store_h<T>(hcol + static_cast<long long>(bi.z + nb + i) * a.I, activate(a.ep, g, u));
+          for (int i = 0; i < 16; ++i) {
+            const float g = gate_warp ? __uint_as_float(v[i]) + bias : x_g[i * 32 + lane];
+            const float u = gate_warp ? x_u[i * 32 + lane] : __uint_as_float(v[16 + i]) + bias;
+            hv[i] = activate(a.ep, g, u);
+          }
+          if constexpr (sizeof(T) == 2) {
+            // lanes 2m and 2m+1 hold columns j and j+1: per pair of rows the
+            // even lane stores row i and the odd lane row i+1, each as one
+            // bf16x2 word, after one exchange (j < I is the same for the
+            // whole warp, as I is a multiple of 64)
+            const bool odd = lane & 1;
+            __nv_bfloat16* hpair = reinterpret_cast<__nv_bfloat16*>(a.out) + (j & ~1);
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              const float recv = __shfl_xor_sync(0xffffffffu, odd ? hv[i] : hv[i + 1], 1);
+              const int r = odd ? i + 1 : i;
+              const __nv_bfloat162 pk =
+                  odd ? __floats2bfloat162_rn(recv, hv[i + 1]) : __floats2bfloat162_rn(hv[i], recv);
+              if (j < a.I && nb + r < valid)
+                *reinterpret_cast<__nv_bfloat162*>(
+                    hpair + static_cast<long long>(bi.z + nb + r) * a.I) = pk;
             }
+          } else if (j < a.I) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (nb + i < valid) store_h<T>(hcol + static_cast<long long>(bi.z + nb + i) * a.I, hv[i]);
           }
           named_bar_sync(1 + pq, 64);  // the exchange slots are free again
         }
