@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--config", default="mixtral_prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="combine fused into GEMM2 (fp32 atomics into a (T, H) accumulator)")
     ap.add_argument("--block-m", type=int, default=0,
                     help="align block (token tile) of the GEMMs; 0 picks it from the problem")
     ap.add_argument("--shrink", type=int, default=1,
@@ -302,10 +304,12 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
-def build_stages(moe, _abi, cfg, inp, dev, block_m=0, shard=None):
+def build_stages(moe, _abi, cfg, inp, dev, block_m=0, shard=None, fused=False):
     """Problem, workspace, packed weights and the exact launches moe_forward
     makes, one C-ABI call per stage.  shard = (expert_base, local_experts):
-    inp's weights hold those experts only."""
+    inp's weights hold those experts only.  fused: the combine fused into
+    GEMM2 (an fp32 accumulator the gather step zeroes, then one rounding
+    pass)."""
     mx = cfg.dtype == "mxfp4"
     act = {}
     if cfg.activation == "swiglu_oai":  # GPT-OSS expert FFN
@@ -315,7 +319,7 @@ def build_stages(moe, _abi, cfg, inp, dev, block_m=0, shard=None):
     base, L = shard if shard is not None else (0, 0)
     p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "bf16" if mx else cfg.dtype,
                          "mxfp4" if mx else None, block_m=block_m, h_scale=inp.h_scale,
-                         expert_base=base, local_experts=L, **act)
+                         expert_base=base, local_experts=L, fused_combine=fused, **act)
     wsp = moe.Workspace(p, dev)
     part = lambda i, dt=torch.int32: wsp.part(i, dt)
     st = wsp.status
@@ -325,7 +329,8 @@ def build_stages(moe, _abi, cfg, inp, dev, block_m=0, shard=None):
     binfo, nblk = part(_abi.MOE_WS_BLOCK_INFO), part(_abi.MOE_WS_NUM_BLOCKS)
     scratch = part(_abi.MOE_WS_ALIGN)  # empty below 16384 assignments: one-CTA align
     h = part(_abi.MOE_WS_H, torch.uint8)
-    y = part(_abi.MOE_WS_Y, torch.float32)
+    y = part(_abi.MOE_WS_Y, torch.float32)  # or, fused, the (T, H) accumulator
+    acc = y if fused else None
     xq = part(_abi.MOE_WS_XQ, torch.uint8) if mx else None
     xs = part(_abi.MOE_WS_X_SCALE, torch.float32) if mx else None
     # model weights as the kernels read them (mxfp4: packed once, at load time)
@@ -347,18 +352,22 @@ def build_stages(moe, _abi, cfg, inp, dev, block_m=0, shard=None):
         sorted_ids, inv, binfo, nblk, st, stream, scratch)))
     if mx:
         stages.append(("quantize_gather_x", lambda: moe.moe_quantize_gather_x_fp8(
-            inp.x, _abi.MOE_BF16, cfg.T, cfg.H, cfg.K, inv, xq, xs, st, stream)))
+            inp.x, _abi.MOE_BF16, cfg.T, cfg.H, cfg.K, inv, xq, xs, st, stream, acc)))
     else:  # token rows to their sorted slots
         x_sorted = part(_abi.MOE_WS_XQ, inp.x.dtype)
         stages.append(("gather", lambda: moe.moe_gather_rows(
-            inp.x, p.act, cfg.T, cfg.H, cfg.K, inv, x_sorted, st, stream)))
+            inp.x, p.act, cfg.T, cfg.H, cfg.K, inv, x_sorted, st, stream, acc)))
     a_rows = xq if mx else x_sorted
     stages.append(("gemm_gate_up", lambda: moe.moe_gemm1_silu(
         p, a_rows, xs, w13, s13, sorted_ids, binfo, nblk, h, st, stream)))
     stages.append(("gemm_down", lambda: moe.moe_gemm2_weighted(
         p, h, w2, s2, inp.topk_weights, sorted_ids, binfo, nblk, y, splits, st, stream)))
-    stages.append(("combine", lambda: moe.moe_combine(
-        y, splits, cap, inv, cfg.T, cfg.K, cfg.H, p.act, out, st, stream)))
+    if fused:
+        stages.append(("combine", lambda: moe.moe_combine_finish(
+            y, cfg.T, cfg.H, p.act, out, st, stream)))
+    else:
+        stages.append(("combine", lambda: moe.moe_combine(
+            y, splits, cap, inv, cfg.T, cfg.K, cfg.H, p.act, out, st, stream)))
     return stages, p, wsp, (w13, s13, w2, s2), out, bm, stream
 
 
@@ -380,7 +389,7 @@ def run_ours(args, ws, rank, local):
         inp.x = gen.draw_x(cfg, seed=seed, device=dev)
         inp.topk_ids, inp.topk_weights = gen.route(gen.router_logits(cfg, seed, dev), cfg.K)
     stages, p, wsp, (w13, s13, w2, s2), out, bm, stream = build_stages(
-        moe, _abi, cfg, inp, dev, args.block_m)
+        moe, _abi, cfg, inp, dev, args.block_m, fused=args.fused_combine)
     st = wsp.status
     mx = cfg.dtype == "mxfp4"
     splits = moe.moe_gemm2_default_splits(p)
@@ -528,6 +537,8 @@ def run_ours(args, ws, rank, local):
                       "mxfp4": "e4m3 x mxfp4 (fp32 acc)"}[cfg.dtype], "data": "synthetic",
             "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
                        "top_k": cfg.K, "global_batch_tokens": tokens_all, "block_m": bm,
+                       "combine": "fused into GEMM2 (fp32 atomics)" if args.fused_combine
+                                  else "separate, deterministic",
                        "parallelism": f"replicas{ws}",
                        "l2": "inputs larger than L2 (expert weights %.2f GB)" %
                              (bytes_alg / 1e9)},

@@ -96,7 +96,18 @@ typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SWIGLU_CLAMP = 1 } moe_activation_t;
  *            activation.  gate_up_interleaved: w13 (and w13_bias) hold gate
  *            and up in alternating rows, that page's layout, instead of the
  *            two halves; for MX weights pass the same flag to
- *            moe_pack_mx_weights, whose packed form is always in halves. */
+ *            moe_pack_mx_weights, whose packed form is always in halves.
+ *   fused_combine: 0 = the deterministic combine: GEMM2 writes each weighted
+ *            expert row in sorted order and moe_combine sums every token's K
+ *            rows in k order.  1 = the combine fused into GEMM2, after the
+ *            scatter-add of "factor_moe_fused_gemm.cu"
+ *            (weighted_scatter_add_kernel): GEMM2's epilogue adds each
+ *            weighted row into an fp32 (T, H) accumulator with atomic adds
+ *            (zeroed by the gather step before) and moe_combine_finish
+ *            rounds it to out.  The order of the adds is not fixed, so the
+ *            fp32 sums, and rarely the rounded outputs, may differ between
+ *            runs in the last bits.  The workspace then holds T*H fp32
+ *            instead of k_splits*cap*H. */
 typedef struct {
     int T, H, I, E, K;
     int act;
@@ -111,6 +122,7 @@ typedef struct {
     int gate_up_interleaved;  /* w13 rows 2j = gate j, 2j+1 = up j         */
     const float* w13_bias;    /* device (L, 2I) fp32 in w13's row order    */
     const float* w2_bias;     /* device (L, H) fp32                        */
+    int fused_combine;        /* 0 or 1, see above                         */
 } moe_problem_t;
 
 /* Sub-buffers of the moe_forward workspace (byte offsets, see
@@ -128,7 +140,8 @@ typedef enum {
                                /* (MX weights) or act rows                  */
     MOE_WS_X_SCALE = 9,        /* fp32[T]      (MX weights only)            */
     MOE_WS_H = 10,             /* act or e4m3 [cap][I]                      */
-    MOE_WS_Y = 11,             /* fp32[splits][cap][H]                      */
+    MOE_WS_Y = 11,             /* fp32[splits][cap][H], or fp32[T][H] when  */
+                               /* fused_combine (the accumulator)           */
     MOE_WS_ALIGN = 12,         /* int32 per-warp counts of the align of     */
                                /* large batches (T*K >= 16384), else empty  */
     MOE_WS_NUM = 13
@@ -282,10 +295,12 @@ int moe_quantize_x_fp8(const void* x, int x_dtype, int T, int H, uint8_t* xq, fl
  * each token's codes are written to every slot of the expert-sorted list the
  * token occupies, xq_sorted[inv_perm[t*K + k], :] (cap rows of H bytes; rows
  * of padding slots are not written), scales as above in token order.
- * inv_perm as written by moe_align.  Skipped when *dev_status != 0. */
+ * inv_perm as written by moe_align.  acc_zero: NULL, or the fp32 (T, H)
+ * accumulator of a fused combine, whose rows this step sets to zero.
+ * Skipped when *dev_status != 0. */
 int moe_quantize_gather_x_fp8(const void* x, int x_dtype, int T, int H, int K,
                               const int32_t* inv_perm, uint8_t* xq_sorted, float* row_scale,
-                              int32_t* dev_status, void* stream);
+                              float* acc_zero, int32_t* dev_status, void* stream);
 
 /* ---- gather step (bf16/fp32 weights) ---------------------------------------
  * Source: "MOE Bmm1 Fused Gather", load_activations (token rows gathered by
@@ -295,9 +310,11 @@ int moe_quantize_gather_x_fp8(const void* x, int x_dtype, int T, int H, int K,
  * negative inv_perm entry, another shard's slot, is skipped); x (T, H) in
  * dtype (MOE_BF16 / MOE_F32), x_sorted (cap, H), inv_perm from moe_align.
  * The bf16/fp32 gate/up GEMM reads its token rows in this sorted form.
+ * acc_zero: NULL, or the fp32 (T, H) accumulator of a fused combine, whose
+ * rows this step sets to zero (H a multiple of 4).
  * Skipped when *dev_status != 0. */
 int moe_gather_rows(const void* x, int dtype, int T, int H, int K, const int32_t* inv_perm,
-                    void* x_sorted, int32_t* dev_status, void* stream);
+                    void* x_sorted, float* acc_zero, int32_t* dev_status, void* stream);
 
 /* ---- gather + GEMM1 + SiLU*up -------------------------------------------
  * Source: "factor_moe_fused_gemm.cu", fused_silu_gate_kernel (gate = first
@@ -335,7 +352,11 @@ int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_sca
  * h (cap, I) as written by moe_gemm1_silu; w2 (E, H, I) weight dtype (MX:
  * packed by moe_pack_mx_weights with R = H, K = I, sections = 1);
  * y (k_splits, cap, H) fp32, padding rows not written.  MX splits cut the
- * 128-element K tiles. */
+ * 128-element K tiles.
+ * With p->fused_combine, y is instead the fp32 (T, H) accumulator, zeroed
+ * beforehand (moe_gather_rows / moe_quantize_gather_x_fp8 with acc_zero),
+ * and every split of every valid slot s adds its part of
+ * topk_weights[i] * (W2[e] h[s] + b2) into row i / K with atomic adds. */
 int moe_gemm2_weighted(const moe_problem_t* p, const void* h, const void* w2,
                        const uint8_t* w2_scale, const float* topk_weights,
                        const int32_t* sorted_ids, const int32_t* block_info,
@@ -353,9 +374,17 @@ int moe_gemm2_weighted(const moe_problem_t* p, const void* h, const void* w2,
 int moe_combine(const float* y, int k_splits, size_t cap, const int32_t* inv_perm, int T, int K,
                 int H, int out_dtype, void* out, int32_t* dev_status, void* stream);
 
+/* The last step of a fused combine (moe_problem_t.fused_combine):
+ * out[t, c] = acc[t, c] rounded once to out_dtype (MOE_F32 / MOE_BF16).
+ * acc (T, H) fp32 as GEMM2 left it; H a multiple of 4.  Skipped when
+ * *dev_status != 0. */
+int moe_combine_finish(const float* acc, int T, int H, int out_dtype, void* out,
+                       int32_t* dev_status, void* stream);
+
 /* ---- the whole forward -----------------------------------------------------
  * Runs align -> [fp8 step with the gather (MX) | gather] -> GEMM1 -> GEMM2
- * -> combine on
+ * -> combine (with p->fused_combine: GEMM2 adding into the accumulator the
+ * gather step zeroed -> moe_combine_finish) on
  * `stream`, with every intermediate in `workspace` (device memory of at
  * least moe_workspace_size(p) bytes, 256-byte aligned, owned by the caller,
  * reusable across calls but not shared by calls in flight at once).

@@ -14,7 +14,7 @@ from . import _abi
 from ._abi import (MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP, MOE_BF16, MOE_E2M1_MX, MOE_E4M3, MOE_F32,
                    MoEError, Problem, moe_abi_version,
                    moe_align, moe_align_capacity, moe_align_local, moe_combine, moe_forward,
-                   moe_route_align, moe_align_scratch_bytes,
+                   moe_route_align, moe_align_scratch_bytes, moe_combine_finish,
                    moe_forward_noalloc, moe_gather_rows, moe_gemm1_silu, moe_gemm2_default_splits,
                    moe_gemm2_weighted, moe_get_device_status, moe_mx_packed_bytes,
                    moe_pack_mx_weights, moe_quantize_gather_x_fp8, moe_quantize_x_fp8,
@@ -24,7 +24,7 @@ __all__ = ["MOE_ACT_SILU", "MOE_ACT_SWIGLU_CLAMP", "MoEError", "Problem", "make_
            "pack_mx", "moe_forward_noalloc", "moe_mx_packed_bytes", "moe_pack_mx_weights",
            "moe_quantize_gather_x_fp8", "moe_gather_rows",
            "moe_abi_version", "moe_align", "moe_align_capacity", "moe_align_local",
-           "moe_align_scratch_bytes",
+           "moe_align_scratch_bytes", "moe_combine_finish",
            "moe_route_align", "route_align",
            "moe_combine", "moe_forward",
            "moe_gemm1_silu", "moe_gemm2_default_splits", "moe_gemm2_weighted",
@@ -45,13 +45,15 @@ def dtype_code(dt) -> int:
 def make_problem(T, H, I, E, K, act="bf16", weight=None, block_m=0, h_scale=1.0,
                  expert_base=0, local_experts=0, activation=MOE_ACT_SILU, swiglu_alpha=1.0,
                  swiglu_limit=float("inf"), gate_up_interleaved=False, w13_bias=None,
-                 w2_bias=None) -> Problem:
+                 w2_bias=None, fused_combine=False) -> Problem:
     """local_experts > 0: an expert-parallel shard holding experts
     [expert_base, expert_base + local_experts) of E; its weights hold those
     experts only.  activation MOE_ACT_SWIGLU_CLAMP selects the clamped
     SwiGLU (swiglu_alpha, swiglu_limit); gate_up_interleaved: w13 rows
     alternate gate and up; w13_bias (experts, 2I) / w2_bias (experts, H):
-    fp32 device tensors, kept alive by the returned problem."""
+    fp32 device tensors, kept alive by the returned problem.  fused_combine:
+    GEMM2 adds its rows into an fp32 accumulator (atomics) instead of the
+    separate, deterministic combine."""
     a = dtype_code(act)
     w = a if weight is None else dtype_code(weight)
     for b in (w13_bias, w2_bias):
@@ -61,7 +63,7 @@ def make_problem(T, H, I, E, K, act="bf16", weight=None, block_m=0, h_scale=1.0,
     P = Problem(T, H, I, E, K, a, w, block_m, h_scale, expert_base, local_experts, activation,
                 swiglu_alpha, lim, int(gate_up_interleaved),
                 None if w13_bias is None else w13_bias.data_ptr(),
-                None if w2_bias is None else w2_bias.data_ptr())
+                None if w2_bias is None else w2_bias.data_ptr(), int(fused_combine))
     P._keep = (w13_bias, w2_bias)
     return P
 
@@ -159,7 +161,8 @@ def forward(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=None, o
     w13.shape[0]) of num_experts (an expert-parallel shard) and out is this
     shard's share of the layer output.  `activation`: make_problem's
     activation, swiglu_alpha, swiglu_limit, gate_up_interleaved, w13_bias,
-    w2_bias.  MX weights (weight="mxfp4") come packed by pack_mx."""
+    w2_bias, fused_combine.  MX weights (weight="mxfp4") come packed by
+    pack_mx."""
     T, H = x.shape
     L, I = w13.shape[0], w13.shape[1] // 2
     E = L if num_experts is None else num_experts

@@ -36,7 +36,8 @@ EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_a
            "moe_quantize_x_fp8", "moe_gemm1_silu", "moe_gemm2_weighted", "moe_combine",
            "moe_forward", "moe_forward_noalloc", "moe_get_device_status", "moe_mx_packed_bytes",
            "moe_pack_mx_weights", "moe_quantize_gather_x_fp8", "moe_device_info",
-           "moe_gather_rows", "moe_align_local", "moe_route_align", "moe_align_scratch_bytes")
+           "moe_gather_rows", "moe_align_local", "moe_route_align", "moe_align_scratch_bytes",
+           "moe_combine_finish")
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
 MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP = 0, 1
@@ -56,7 +57,8 @@ class Problem(ctypes.Structure):
                 ("expert_base", ctypes.c_int), ("local_experts", ctypes.c_int),
                 ("activation", ctypes.c_int), ("swiglu_alpha", ctypes.c_float),
                 ("swiglu_limit", ctypes.c_float), ("gate_up_interleaved", ctypes.c_int),
-                ("w13_bias", ctypes.c_void_p), ("w2_bias", ctypes.c_void_p)]
+                ("w13_bias", ctypes.c_void_p), ("w2_bias", ctypes.c_void_p),
+                ("fused_combine", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -111,9 +113,11 @@ def _declare(L):
     L.moe_quantize_x_fp8.restype = i32
     L.moe_quantize_x_fp8.argtypes = [vp, i32, i32, i32, vp, vp, vp]
     L.moe_gather_rows.restype = i32
-    L.moe_gather_rows.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
+    L.moe_gather_rows.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     L.moe_quantize_gather_x_fp8.restype = i32
-    L.moe_quantize_gather_x_fp8.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+    L.moe_quantize_gather_x_fp8.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    L.moe_combine_finish.restype = i32
+    L.moe_combine_finish.argtypes = [vp, i32, i32, i32, vp, vp, vp]
     L.moe_gemm1_silu.restype = i32
     L.moe_gemm1_silu.argtypes = [PP] + [vp] * 10
     L.moe_gemm2_weighted.restype = i32
@@ -233,16 +237,24 @@ def moe_quantize_x_fp8(x, x_dtype, T, H, xq, row_scale, stream=None):
                                     _stream(stream)), "moe_quantize_x_fp8")
 
 
-def moe_gather_rows(x, dtype, T, H, K, inv_perm, x_sorted, dev_status=None, stream=None):
+def moe_gather_rows(x, dtype, T, H, K, inv_perm, x_sorted, dev_status=None, stream=None,
+                    acc_zero=None):
     _check(lib().moe_gather_rows(_p(x), dtype, T, H, K, _p(inv_perm), _p(x_sorted),
-                                 _p(dev_status), _stream(stream)), "moe_gather_rows")
+                                 _p(acc_zero), _p(dev_status), _stream(stream)),
+           "moe_gather_rows")
 
 
 def moe_quantize_gather_x_fp8(x, x_dtype, T, H, K, inv_perm, xq_sorted, row_scale,
-                              dev_status=None, stream=None):
+                              dev_status=None, stream=None, acc_zero=None):
     _check(lib().moe_quantize_gather_x_fp8(_p(x), x_dtype, T, H, K, _p(inv_perm), _p(xq_sorted),
-                                           _p(row_scale), _p(dev_status), _stream(stream)),
+                                           _p(row_scale), _p(acc_zero), _p(dev_status),
+                                           _stream(stream)),
            "moe_quantize_gather_x_fp8")
+
+
+def moe_combine_finish(acc, T, H, out_dtype, out, dev_status=None, stream=None):
+    _check(lib().moe_combine_finish(_p(acc), T, H, out_dtype, _p(out), _p(dev_status),
+                                    _stream(stream)), "moe_combine_finish")
 
 
 def moe_gemm1_silu(p: Problem, x, x_row_scale, w13, w13_scale, sorted_ids, block_info,

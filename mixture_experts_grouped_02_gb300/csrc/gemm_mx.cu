@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
       }
       const bool row_ok = r < valid;
       float rs = 0.0f, wt = 0.0f;
+      int tok = 0;  // down, fused combine: the accumulator row
       if (row_ok) {
         const int i = a.sorted_ids[r0 + r];
         if constexpr (KIND == kMxGateUp) {
@@ -349,6 +350,7 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
         } else {
           wt = a.topk_weights[i];
           rs = wt * a.h_scale;
+          tok = i / a.K;
         }
       }
       int good = 1;
@@ -392,8 +394,10 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
           }
         }
       } else {
+        // the row of y, or (fused combine) the token's accumulator row
         float* y = static_cast<float*>(a.out) +
-                   (static_cast<long long>(t.split) * a.cap + r0 + r) * a.H;
+                   (a.fused ? static_cast<long long>(tok)
+                            : static_cast<long long>(t.split) * a.cap + r0 + r) * a.H;
 #pragma unroll 1
         for (int c = 0; c < 6; ++c) {
           uint32_t v[32];
@@ -410,7 +414,10 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
               for (int w = 0; w < 4; ++w)
                 o[w] = rs * __uint_as_float(v[4 * i + w]) +
                        (has_bias ? wt * sb[c * 32 + 4 * i + w] : 0.0f);
-              dst[i] = make_float4(o[0], o[1], o[2], o[3]);
+              if (a.fused)
+                atomicAdd(dst + i, make_float4(o[0], o[1], o[2], o[3]));
+              else
+                dst[i] = make_float4(o[0], o[1], o[2], o[3]);
             }
           }
         }

@@ -413,15 +413,34 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
         for (int c0 = 0; c0 < n; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(taddr + c0, v);
-          // routing weight of token c0 + lane, broadcast below
+          // routing weight (and, for a fused combine, the token row) of slot
+          // c0 + lane, broadcast below
           const int my = c0 + lane;
-          const float w_l = my < valid ? a.topk_weights[a.sorted_ids[bi.z + my]] : 0.0f;
+          float w_l = 0.0f;
+          int tok_l = 0;
+          if (my < valid) {
+            const int i = a.sorted_ids[bi.z + my];
+            w_l = a.topk_weights[i];
+            tok_l = i / a.K;
+          }
           tmem_wait_ld();
+          if (a.fused) {
+            // the scatter-add: 32 lanes add 128 contiguous bytes of one row
+            float* acc_c = reinterpret_cast<float*>(a.out) + c;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float w = __shfl_sync(0xffffffffu, w_l, i);
-            if (c0 + i < valid && c < a.H)
-              ycol[static_cast<long long>(bi.z + c0 + i) * a.H] = w * (__uint_as_float(v[i]) + bias);
+            for (int i = 0; i < 32; ++i) {
+              const float w = __shfl_sync(0xffffffffu, w_l, i);
+              const int tok = __shfl_sync(0xffffffffu, tok_l, i);
+              if (c0 + i < valid && c < a.H)
+                atomicAdd(acc_c + static_cast<long long>(tok) * a.H, w * (__uint_as_float(v[i]) + bias));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float w = __shfl_sync(0xffffffffu, w_l, i);
+              if (c0 + i < valid && c < a.H)
+                ycol[static_cast<long long>(bi.z + c0 + i) * a.H] = w * (__uint_as_float(v[i]) + bias);
+            }
           }
         }
       }

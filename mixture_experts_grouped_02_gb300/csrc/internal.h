@@ -104,7 +104,9 @@ struct GemmArgs {
   const int32_t* block_info;
   const int32_t* num_blocks;
   const float* topk_weights;  // down projection: routing weight per flat index
-  void* out;                  // gate/up: h (cap, I); down: y (splits, cap, H) fp32
+  void* out;                  // gate/up: h (cap, I); down: y (splits, cap, H) fp32, or
+                              // the (T, H) fp32 accumulator when `fused`
+  int fused;                  // down: add rows into the accumulator (atomics)
   int32_t* status;
   unsigned long long timeout_ns;
   Epilogue ep;
@@ -129,7 +131,9 @@ struct MxArgs {
   const int32_t* block_info;
   const int32_t* num_blocks;
   const float* topk_weights;   // down: routing weight per flat index
-  void* out;                   // gate/up: hq (cap, I) e4m3; down: y (splits, cap, H) fp32
+  void* out;                   // gate/up: hq (cap, I) e4m3; down: y (splits, cap, H) fp32,
+                               // or the (T, H) fp32 accumulator when `fused`
+  int fused;                   // down: add rows into the accumulator (atomics)
   float h_scale;               // hq = e4m3(a / h_scale)
   int32_t* status;
   unsigned long long timeout_ns;
@@ -172,11 +176,17 @@ cudaError_t launch_combine(const float* y, int splits, long long cap, const int3
                            cudaStream_t s);
 cudaError_t launch_quantize_x(const void* x, int x_dtype, int T, int H, uint8_t* xq,
                               float* row_scale, cudaStream_t s);
+// acc_zero (nullable): rows of H fp32 of a fused combine's accumulator,
+// set to zero for every token by the same CTAs.
 cudaError_t launch_gather_rows(const void* x, int T, int row_bytes, int K, const int32_t* inv_perm,
-                               void* xs, const int32_t* status, cudaStream_t s);
+                               void* xs, float* acc_zero, int H, const int32_t* status,
+                               cudaStream_t s);
 cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, int K,
                                      const int32_t* inv_perm, uint8_t* xq_sorted,
-                                     float* row_scale, const int32_t* status, cudaStream_t s);
+                                     float* row_scale, float* acc_zero, const int32_t* status,
+                                     cudaStream_t s);
+cudaError_t launch_combine_finish(const float* acc, int T, int H, int out_dtype, void* out,
+                                  const int32_t* status, cudaStream_t s);
 
 // Align blocks of 256 rows: the largest token tile of the bf16/fp32 GEMMs.
 constexpr int kPairBlockM = 256;

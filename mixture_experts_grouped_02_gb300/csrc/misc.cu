@@ -2,6 +2,8 @@
 // and the per-row fp8 (e4m3) activation step.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -152,13 +154,17 @@ __global__ void __launch_bounds__(256) quantize_x_kernel(const void* __restrict_
 // (another shard's experts) are skipped.
 __global__ void __launch_bounds__(256) quantize_gather_x_kernel(
     const void* __restrict__ x, int bf16, int T, int H, int K, const int32_t* __restrict__ inv_perm,
-    uint8_t* __restrict__ xq_sorted, float* __restrict__ row_scale, const int32_t* status) {
+    uint8_t* __restrict__ xq_sorted, float* __restrict__ row_scale, float4* __restrict__ acc_zero,
+    const int32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   if (status != nullptr && *status != 0) return;
   __shared__ float s_red[8];
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     const long long base = static_cast<long long>(t) * H;
+    if (acc_zero != nullptr)  // the fused combine's accumulator row of this token
+      for (int c = threadIdx.x; c < (H >> 2); c += blockDim.x)
+        acc_zero[(base >> 2) + c] = make_float4(0.f, 0.f, 0.f, 0.f);
     float amax = 0.0f;
     for (int c = threadIdx.x; c < H; c += blockDim.x) amax = fmaxf(amax, fabsf(load_act(x, bf16, base + c)));
 #pragma unroll
@@ -192,11 +198,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           int T, int row_vec, int K,
                                                           const int32_t* __restrict__ inv_perm,
                                                           uint4* __restrict__ xs,
-                                                          const int32_t* status) {
+                                                          float4* __restrict__ acc_zero,
+                                                          int acc_vec, const int32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   if (status != nullptr && *status != 0) return;
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    if (acc_zero != nullptr)  // the fused combine's accumulator row of this token
+      for (int c = threadIdx.x; c < acc_vec; c += blockDim.x)
+        acc_zero[static_cast<long long>(t) * acc_vec + c] = make_float4(0.f, 0.f, 0.f, 0.f);
     const uint4* src = x + static_cast<long long>(t) * row_vec;
     for (int c = threadIdx.x; c < row_vec; c += blockDim.x) {
       const uint4 v = __ldg(src + c);
@@ -208,25 +218,58 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   }
 }
 
+// out = acc rounded once to the output type, 4 columns per thread.  Source:
+// the final cast of the scatter-add path of "factor_moe_fused_gemm.cu"
+// (fp32 accumulation, then the model dtype).
+template <typename OutT>
+__global__ void __launch_bounds__(256) combine_finish_kernel(const float4* __restrict__ acc,
+                                                             long long n4, OutT* __restrict__ out,
+                                                             const int32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  if (status != nullptr && *status != 0) return;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    store_out4(out + 4 * i, 0, __ldg(acc + i));
+}
+
 }  // namespace
 
 cudaError_t launch_gather_rows(const void* x, int T, int row_bytes, int K, const int32_t* inv_perm,
-                               void* xs, const int32_t* status, cudaStream_t s) {
+                               void* xs, float* acc_zero, int H, const int32_t* status,
+                               cudaStream_t s) {
   const int grid = T < 65535 ? T : 65535;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, s, attr);
   return cudaLaunchKernelEx(&cfg, gather_rows_kernel, static_cast<const uint4*>(x), T,
-                            row_bytes / 16, K, inv_perm, static_cast<uint4*>(xs), status);
+                            row_bytes / 16, K, inv_perm, static_cast<uint4*>(xs),
+                            reinterpret_cast<float4*>(acc_zero), H / 4, status);
 }
 
 cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, int K,
                                      const int32_t* inv_perm, uint8_t* xq_sorted,
-                                     float* row_scale, const int32_t* status, cudaStream_t s) {
+                                     float* row_scale, float* acc_zero, const int32_t* status,
+                                     cudaStream_t s) {
   const int grid = T < 65535 ? T : 65535;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, s, attr);
   return cudaLaunchKernelEx(&cfg, quantize_gather_x_kernel, x, x_dtype == MOE_BF16 ? 1 : 0, T, H,
-                            K, inv_perm, xq_sorted, row_scale, status);
+                            K, inv_perm, xq_sorted, row_scale, reinterpret_cast<float4*>(acc_zero),
+                            status);
+}
+
+cudaError_t launch_combine_finish(const float* acc, int T, int H, int out_dtype, void* out,
+                                  const int32_t* status, cudaStream_t s) {
+  const long long n4 = static_cast<long long>(T) * (H / 4);
+  const int grid = static_cast<int>(std::min<long long>((n4 + 255) / 256, 152ll * 16));
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, s, attr);
+  const float4* a4 = reinterpret_cast<const float4*>(acc);
+  if (out_dtype == MOE_BF16)
+    return cudaLaunchKernelEx(&cfg, combine_finish_kernel<__nv_bfloat16>, a4, n4,
+                              static_cast<__nv_bfloat16*>(out), status);
+  return cudaLaunchKernelEx(&cfg, combine_finish_kernel<float>, a4, n4, static_cast<float*>(out),
+                            status);
 }
 
 cudaError_t launch_combine(const float* y, int splits, long long cap, const int32_t* inv_perm,

@@ -58,6 +58,7 @@ int check_problem(const moe_problem_t* p) {
         p->swiglu_alpha < 3.0e38f))
     return MOE_ERR_INVALID_ARG;
   if (p->gate_up_interleaved != 0 && p->gate_up_interleaved != 1) return MOE_ERR_INVALID_ARG;
+  if (p->fused_combine != 0 && p->fused_combine != 1) return MOE_ERR_INVALID_ARG;
   const long long na = static_cast<long long>(p->T) * p->K;
   if (na >= (1ll << 30)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -193,7 +194,9 @@ void layout_of(const moe_problem_t* p, Layout* L) {
   sz[MOE_WS_XQ] = static_cast<size_t>(cap) * p->H * (mx ? 1 : act_bytes(p->act));
   sz[MOE_WS_X_SCALE] = mx ? 4ull * p->T : 0;
   sz[MOE_WS_H] = static_cast<size_t>(cap) * p->I * (mx ? 1 : act_bytes(p->act));
-  sz[MOE_WS_Y] = 4ull * splits * static_cast<size_t>(cap) * p->H;
+  // y rows in sorted order per split, or the fused combine's accumulator
+  sz[MOE_WS_Y] = p->fused_combine ? 4ull * p->T * p->H
+                                  : 4ull * splits * static_cast<size_t>(cap) * p->H;
   sz[MOE_WS_ALIGN] = na >= kAlignMultiMin ? 4 * align_multi_scratch_ints(na, local_experts(p)) : 0;
   size_t off = 0;
   for (int i = 0; i < MOE_WS_NUM; ++i) {
@@ -397,6 +400,7 @@ int run_gemm2(const moe_problem_t* p, const void* h, const void* w2, const float
   a.num_blocks = num_blocks;
   a.topk_weights = topk_weights;
   a.out = y;
+  a.fused = p->fused_combine;
   a.status = status;
   CUtensorMap tmTok, tmTokS, tmW;
   int rc = make_map(&tmW, p->act, w2, p->I, 1ll * p->H * local_experts(p), bk, 128);
@@ -477,6 +481,7 @@ int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const u
   a.sections = 1;
   a.groups = mx_scale_groups(p->H);
   a.kp_tiles = Ip / 128;
+  a.fused = p->fused_combine;
   CUtensorMap tmA, tmW;
   int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq, p->I, a.cap, p->I, 128, 128);
   if (rc != MOE_OK) return rc;
@@ -659,28 +664,47 @@ int moe_quantize_x_fp8(const void* x, int x_dtype, int T, int H, uint8_t* xq, fl
 }
 
 int moe_gather_rows(const void* x, int dtype, int T, int H, int K, const int32_t* inv_perm,
-                    void* x_sorted, int32_t* dev_status, void* stream) {
+                    void* x_sorted, float* acc_zero, int32_t* dev_status, void* stream) {
   if (T < 0 || H <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
   if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
   const long long row_bytes = static_cast<long long>(H) * act_bytes(dtype);
   if (row_bytes % 16 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!x || !inv_perm || !x_sorted) return MOE_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_sorted) & 15u))
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_sorted) & 15u) ||
+      (reinterpret_cast<uintptr_t>(acc_zero) & 15u))
     return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_gather_rows(x, T, static_cast<int>(row_bytes), K, inv_perm, x_sorted,
-                                        dev_status, static_cast<cudaStream_t>(stream)));
+                                        acc_zero, H, dev_status,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 int moe_quantize_gather_x_fp8(const void* x, int x_dtype, int T, int H, int K,
                               const int32_t* inv_perm, uint8_t* xq_sorted, float* row_scale,
-                              int32_t* dev_status, void* stream) {
+                              float* acc_zero, int32_t* dev_status, void* stream) {
   if (T < 0 || H <= 0 || (H & 1) != 0 || K <= 0) return MOE_ERR_INVALID_ARG;
   if (x_dtype != MOE_BF16 && x_dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (acc_zero != nullptr && H % 4 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!x || !inv_perm || !xq_sorted || !row_scale) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(acc_zero) & 15u) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_quantize_gather_x(x, x_dtype, T, H, K, inv_perm, xq_sorted, row_scale,
-                                              dev_status, static_cast<cudaStream_t>(stream)));
+                                              acc_zero, dev_status,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+int moe_combine_finish(const float* acc, int T, int H, int out_dtype, void* out,
+                       int32_t* dev_status, void* stream) {
+  if (T < 0 || H <= 0) return MOE_ERR_INVALID_ARG;
+  if (out_dtype != MOE_BF16 && out_dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (H % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!acc || !out) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(acc) & 15u) ||
+      (reinterpret_cast<uintptr_t>(out) & (out_dtype == MOE_BF16 ? 7u : 15u)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine_finish(acc, T, H, out_dtype, out, dev_status,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_scale,
@@ -762,6 +786,7 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
   int32_t* num_blocks = reinterpret_cast<int32_t*>(part(MOE_WS_NUM_BLOCKS));
   int32_t* inv_perm = reinterpret_cast<int32_t*>(part(MOE_WS_INV_PERM));
   float* y = reinterpret_cast<float*>(part(MOE_WS_Y));
+  float* acc_zero = p->fused_combine ? y : nullptr;  // zeroed by the gather step
   void* h = part(MOE_WS_H);
   const int splits = default_splits(p);
   const int bm = block_m_of(p);
@@ -777,7 +802,8 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
   if (is_mx(p)) {
     uint8_t* xq = part(MOE_WS_XQ);
     float* xs = reinterpret_cast<float*>(part(MOE_WS_X_SCALE));
-    if (launch_quantize_gather_x(x, p->act, p->T, p->H, p->K, inv_perm, xq, xs, status, s) !=
+    if (launch_quantize_gather_x(x, p->act, p->T, p->H, p->K, inv_perm, xq, xs, acc_zero, status,
+                                 s) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     rc = run_gemm1_mx(p, xq, xs, w13, w13_scale, sorted_ids, block_info, num_blocks, h, status, s);
@@ -788,7 +814,7 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
   } else {
     void* xs = part(MOE_WS_XQ);  // token rows in sorted order
     if (launch_gather_rows(x, p->T, static_cast<int>(p->H * act_bytes(p->act)), p->K, inv_perm,
-                           xs, status, s) != cudaSuccess)
+                           xs, acc_zero, p->H, status, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     rc = run_gemm1(p, xs, w13, sorted_ids, block_info, num_blocks, h, status, s);
     if (rc != MOE_OK) return rc;
@@ -796,6 +822,8 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                    s);
     if (rc != MOE_OK) return rc;
   }
+  if (p->fused_combine)
+    return cuda_status(launch_combine_finish(y, p->T, p->H, p->act, out, status, s));
   return cuda_status(launch_combine(y, splits, capacity(p->T, p->K, local_experts(p), bm),
                                     inv_perm, p->T, p->K, p->H, p->act, out, status, s));
 }

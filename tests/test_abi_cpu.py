@@ -86,6 +86,10 @@ def test_workspace_layout_is_disjoint_and_aligned():
     assert size[_abi.MOE_WS_H] == 2 * cap * 14336
     splits = _abi.moe_gemm2_default_splits(p)
     assert size[_abi.MOE_WS_Y] == 4 * splits * cap * 4096
+    # a fused combine keeps the (T, H) fp32 accumulator instead of y
+    pf = make_problem(4096, 4096, 14336, 8, 2, "bf16", fused_combine=True)
+    assert _abi.moe_workspace_offsets(pf)[1][_abi.MOE_WS_Y] == 4 * 4096 * 4096
+    assert _abi.moe_workspace_size(make_problem(16, 128, 256, 8, 2, "bf16", fused_combine=2)) == 0
 
 
 def test_entry_points_reject_bad_arguments_before_launch():
@@ -116,6 +120,14 @@ def test_entry_points_reject_bad_arguments_before_launch():
         _abi.MOE_ERR_UNSUPPORTED
     assert L.moe_combine(fake, 1, 64, fake, 4, 2, 128, _abi.MOE_E4M3, fake, None, None) == \
         _abi.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_finish(fake, 4, 126, _abi.MOE_BF16, fake, None, None) == \
+        _abi.MOE_ERR_UNSUPPORTED
+    assert L.moe_combine_finish(fake, 4, 128, _abi.MOE_E4M3, fake, None, None) == \
+        _abi.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_finish(vp((1 << 20) + 4), 4, 128, _abi.MOE_BF16, fake, None, None) == \
+        _abi.MOE_ERR_INVALID_ARG  # the accumulator is read as 16-byte vectors
+    assert L.moe_gather_rows(fake, _abi.MOE_BF16, 4, 128, 2, fake, fake, vp((1 << 20) + 4), None,
+                             None) == _abi.MOE_ERR_INVALID_ARG
     # workspace too small / misaligned
     ws_ok = _abi.moe_workspace_size(p)
     assert L.moe_forward(ctypes.byref(p), *([fake] * 8), fake, ws_ok - 1, None) == \

@@ -286,6 +286,48 @@ def test_combine_stage(splits, out_dtype):
     assert_close(out, ref, max_abs=2e-2, rel_l2=tol, what="out")
 
 
+@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("case", STAGE_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s" % c)
+def test_gemm2_fused_combine_stage(case, splits):
+    """GEMM2 adding its weighted rows into the (T, H) accumulator the gather
+    step zeroed: every token row equals the sum of its K weighted expert rows
+    (the oracle's rows, summed per token in fp64)."""
+    T, H, I, E, K, dt = case
+    bm = 128
+    cfg = gen.MoEConfig("stage", T, H, I, E, K, dt, "normal")
+    inp = gen.generate(cfg, seed=23)
+    d = inp.to("cuda")
+    cap = moe.moe_align_capacity(T, K, E, bm)
+    hin = torch.randn((cap, I), generator=torch.Generator().manual_seed(7)).to(inp.x.dtype)
+    al_ref = oracle.align(inp.topk_ids.numpy(), E, bm)
+    al = moe.align(d.topk_ids, E, bm)
+    p = moe.make_problem(T, H, I, E, K, dt, block_m=bm, fused_combine=True)
+    acc = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    xs = torch.empty((cap, H), dtype=d.x.dtype, device="cuda")
+    st = _status()
+    moe.moe_gather_rows(d.x, p.act, T, H, K, al["inv_perm"], xs, st, acc_zero=acc)
+    moe.moe_gemm2_weighted(p, hin.cuda(), d.w2, None, d.topk_weights, al["sorted_ids"],
+                           al["block_info"], al["num_blocks"], acc, splits, st)
+    assert moe.moe_get_device_status(st) == 0
+    rows = _valid_rows(al_ref, T * K)
+    eor = _expert_of_rows(al_ref, rows, inp.topk_ids.numpy().ravel())
+    per_row = oracle.gemm2_weighted_rows(oracle_problem(inp), np_store(hin), np_store(inp.w2),
+                                         inp.topk_weights.numpy(), al_ref["sorted_ids"], eor, rows)
+    ref = np.zeros((T, H))
+    np.add.at(ref, al_ref["sorted_ids"][rows] // K, per_row)
+    tol = 1e-4 if dt == "bf16" else 5e-3
+    assert_close(acc, ref, max_abs=2e-2, rel_l2=tol, what="accumulator")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_combine_finish_rounds_once(out_dtype):
+    T, H = 37, 96
+    acc = (torch.randn((T, H), generator=torch.Generator().manual_seed(8)) * 3).cuda()
+    out = torch.empty((T, H), dtype=out_dtype, device="cuda")
+    moe.moe_combine_finish(acc, T, H, moe.dtype_code(out_dtype), out)
+    assert torch.equal(out, acc.to(out_dtype))  # round to nearest even, bit for bit
+
+
 # ------------------------------------------------------------------ forward
 
 FORWARD_CASES = [
@@ -684,6 +726,103 @@ def test_forward_expert_shard_mx():
     emu = _oracle_shard(inp, base, L, np.arange(cfg.T), mode=oracle.EMULATE, quantize_x=True,
                         h_e4m3=True)
     assert_close(out, emu, max_abs=MX_MAX_ABS, rel_l2=MX_REL_EMU, what="mx shard vs emulate")
+
+
+# ------------------------------------------------------------------ fused combine
+
+def _run_forward_fused(d, cfg, block_m=0, **kw):
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype, block_m=block_m,
+                         fused_combine=True, **kw)
+    ws = moe.Workspace(p)
+    ws.buffer.fill_(0xFF)  # the accumulator starts as NaN: the gather step must zero it
+    out = torch.full((cfg.T, cfg.H), float("nan"), dtype=d.x.dtype, device="cuda")
+    moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, d.w13, None, d.w2, None, out, ws.buffer,
+                    ws.nbytes)
+    assert moe.moe_get_device_status(ws.status) == 0
+    return out, p
+
+
+@pytest.mark.parametrize("bm", [0, 16, 256])
+@pytest.mark.parametrize("case", FORWARD_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s_%s" % c)
+def test_forward_fused_combine(case, bm):
+    cfg = gen.MoEConfig("fused", *case)
+    inp = gen.generate(cfg, seed=31)
+    d = inp.to("cuda")
+    out, p = _run_forward_fused(d, cfg, block_m=bm)
+    # the accumulator (T rows) replaces y (k_splits x cap rows)
+    assert moe.moe_workspace_size(p) <= moe.moe_workspace_size(
+        moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype, block_m=bm))
+    assert_close(out, oracle_forward_tokens(inp, np.arange(cfg.T)), what=cfg.name)
+    # the deterministic combine differs only by the order of fp32 adds
+    det, _ = _run_forward(d, cfg, block_m=bm)
+    assert_close(out, det.double().cpu().numpy(), max_abs=2e-2, rel_l2=4e-3, what="vs combine")
+
+
+def test_forward_fused_combine_k_splits_and_biases():
+    """Several K splits of the down projection add into one accumulator row;
+    the w2 bias joins once (first split), with the GPT-OSS epilogue."""
+    cfg = gen.MoEConfig("fused_oai", 8, 256, 1536, 8, 2, "bf16", "normal", "swiglu_oai")
+    inp = gen.generate(cfg, seed=53)
+    d = inp.to("cuda")
+    out, p = _run_forward_fused(d, cfg, **problem_kw(d))
+    assert moe.moe_gemm2_default_splits(p) > 1
+    assert_close(out, oracle_forward_tokens(inp, np.arange(cfg.T)), what="fused, split K")
+
+
+def test_forward_fused_combine_shard():
+    cfg = gen.MoEConfig("fused_shard", 200, 256, 320, 8, 2, "bf16", "normal")
+    inp = gen.generate(cfg, seed=41)
+    d = inp.to("cuda")
+    base, L = 3, 4
+    out = moe.forward(d.x, d.topk_ids, d.topk_weights, d.w13[base:base + L].contiguous(),
+                      d.w2[base:base + L].contiguous(), num_experts=cfg.E, expert_base=base,
+                      fused_combine=True)
+    assert_close(out, _oracle_shard(inp, base, L, np.arange(cfg.T)), what="fused shard")
+    ids = inp.topk_ids.numpy()
+    none = ~((ids >= base) & (ids < base + L)).any(1)
+    assert torch.all(out[torch.from_numpy(none).cuda()] == 0)
+
+
+def test_forward_fused_combine_mx():
+    cfg, inp = _mx_problem(MX_CASES[0], 44)
+    d = inp.to("cuda")
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "bf16", "mxfp4", h_scale=0.5,
+                         fused_combine=True)
+    ws = moe.Workspace(p)
+    ws.buffer.fill_(0xFF)
+    out = torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    w13p, s13p = moe.pack_mx(d.w13, d.w13_scale, 2)
+    w2p, s2p = moe.pack_mx(d.w2, d.w2_scale, 1)
+    moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, w13p, s13p, w2p, s2p, out, ws.buffer,
+                    ws.nbytes)
+    assert moe.moe_get_device_status(ws.status) == 0
+    _check_mx(out, inp, np.arange(cfg.T), h_scale=0.5)
+
+
+def test_forward_fused_combine_status_blocks_output():
+    cfg = gen.MoEConfig("fwd", 64, 128, 128, 4, 2, "bf16", "normal")
+    d = gen.generate(cfg, seed=33).to("cuda")
+    d.topk_ids[5, 1] = 4  # outside [0, E)
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype, fused_combine=True)
+    ws = moe.Workspace(p)
+    out = torch.zeros((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, d.w13, None, d.w2, None, out, ws.buffer,
+                    ws.nbytes)
+    assert moe.moe_get_device_status(ws.status) == _abi.MOE_ERR_DEVICE_BAD_ID
+    assert (out == 0).all()
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "dsv3_prefill"])
+def test_forward_fused_combine_full_size_sampled(name):
+    cfg = gen.config(name)
+    inp = generate(cfg, seed=0, device="cuda")
+    out, _ = _run_forward_fused(inp, cfg)
+    toks = sample_tokens(cfg.T, 6, seed=3)
+    assert_close(out[torch.from_numpy(toks).long().cuda()], oracle_forward_tokens(inp, toks),
+                 what=name + " fused")
+    assert torch.isfinite(out.float()).all()
+    del inp, out
+    torch.cuda.empty_cache()
 
 
 # ------------------------------------------------------------------ GPT-OSS expert FFN
