@@ -136,10 +136,6 @@ __device__ __forceinline__ int tile_n(int valid) {
 template <typename T>
 __device__ __forceinline__ void store_h(T* p, float v);
 template <>
-__device__ __forceinline__ void store_h<__nv_bfloat16>(__nv_bfloat16* p, float v) {
-  *p = __float2bfloat16_rn(v);
-}
-template <>
 __device__ __forceinline__ void store_h<float>(float* p, float v) {
   *p = v;
 }
@@ -337,6 +333,31 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
       const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
       const int valid = bi.w;
       const int n = tile_n(valid);
+      // down: the routing weight and token row of slot 32j + lane, and this
+      // lane's w2 bias, loaded before the accumulator is ready so that
+      // their latency hides behind the MMAs (short-K tiles are otherwise
+      // bound by these dependent loads)
+      constexpr int kChunks = C::kNMax / 32;
+      float w_r[kChunks];
+      int tok_r[kChunks];
+      float bias2 = 0.0f;
+      if constexpr (KIND == kDown) {
+        int sid[kChunks];
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+          const int my = 32 * j + lane;
+          sid[j] = my < valid ? a.sorted_ids[bi.z + my] : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+          w_r[j] = sid[j] >= 0 ? a.topk_weights[sid[j]] : 0.0f;
+          tok_r[j] = sid[j] >= 0 ? sid[j] / a.K : 0;
+        }
+        // the w2 bias joins once, in the first K split
+        const int c = t.nt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
+        if (a.ep.b2 != nullptr && t.split == 0 && c < a.H)
+          bias2 = a.ep.b2[static_cast<long long>(bi.x) * a.H + c];
+      }
       int good = 1;
       if (lane == 0) good = mbar_wait_bounded(smem_u32(&accf_bar[acc]), acc_phase, &s_abort, to);
       good = __shfl_sync(0xffffffffu, good, 0);
@@ -406,23 +427,17 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
         const int c = t.nt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
         float* ycol = reinterpret_cast<float*>(a.out) +
                       static_cast<long long>(t.split) * a.cap * a.H + c;
-        // the w2 bias joins once, in the first K split
-        const float bias = (a.ep.b2 != nullptr && t.split == 0 && c < a.H)
-                               ? a.ep.b2[static_cast<long long>(bi.x) * a.H + c]
-                               : 0.0f;
-        for (int c0 = 0; c0 < n; c0 += 32) {
+        const float bias = bias2;
+#pragma unroll
+        for (int jc = 0; jc < kChunks; ++jc) {
+          const int c0 = 32 * jc;
+          if (c0 >= n) break;
           uint32_t v[32];
           tmem_ld32(taddr + c0, v);
           // routing weight (and, for a fused combine, the token row) of slot
           // c0 + lane, broadcast below
-          const int my = c0 + lane;
-          float w_l = 0.0f;
-          int tok_l = 0;
-          if (my < valid) {
-            const int i = a.sorted_ids[bi.z + my];
-            w_l = a.topk_weights[i];
-            tok_l = i / a.K;
-          }
+          const float w_l = w_r[jc];
+          const int tok_l = tok_r[jc];
           tmem_wait_ld();
           if (a.fused) {
             // the scatter-add: 32 lanes add 128 contiguous bytes of one row
