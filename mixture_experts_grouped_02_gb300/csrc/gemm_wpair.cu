@@ -70,19 +70,27 @@ struct Elem<float> {
   static constexpr uint32_t kFmt = 2;
 };
 
-template <int KIND, typename T>
+// DUAL: the launch is made of small tiles (decode-like): each stage of a
+// tile of at most 32 tokens carries two K steps of weights (W and X slots)
+// and their two 16-row token boxes (T slot), twice the weight bytes in
+// flight per pair.  Mixed with large tiles this measured slower, so it is a
+// separate instantiation, chosen by the host (GemmArgs::dual_small).
+template <int KIND, typename T, bool DUAL = false>
 struct WCfg {
   static constexpr int kWRows = 128;          // weight rows per CTA (MMA M = 256 per pair)
   static constexpr int kNMax = 256;           // tokens per tile at most
   static constexpr int kRowBytes = 128;
   static constexpr int kBK = kRowBytes / sizeof(T);
   static constexpr int kUmmaK = 32 / sizeof(T);
-  static constexpr int kStages = KIND == kDown ? 7 : 6;  // down: no exchange buffer, room for 7
-  static constexpr int kABytes = kWRows * kRowBytes;            // 16 KB of weights
+  // down without DUAL: no exchange buffer or T slots, room for 7
+  static constexpr int kStages = (KIND == kDown && !DUAL) ? 7 : 6;
+  static constexpr int kABytes = kWRows * kRowBytes;            // W slot: 16 KB of weights
   static constexpr int kBigRows = kNMax / 2;                    // token box rows
   static constexpr int kSmallRows = 16;
-  static constexpr int kBBytes = kBigRows * kRowBytes;          // 16 KB slot
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBBytes = kBigRows * kRowBytes;          // X slot: 16 KB
+  static constexpr int kSmallBytes = kSmallRows * kRowBytes;    // one 16-row token box
+  static constexpr int kTBytes = DUAL ? 2 * kSmallBytes : 0;    // T slot (DUAL)
+  static constexpr int kStageBytes = kABytes + kBBytes + kTBytes;
   static constexpr int kAccCols = kNMax;
   static constexpr int kTmemCols = 2 * kAccCols;
   static constexpr int kProducerWarp = 0;
@@ -140,13 +148,13 @@ __device__ __forceinline__ void store_h<float>(float* p, float v) {
   *p = v;
 }
 
-template <int KIND, typename T>
-__global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
+template <int KIND, typename T, bool DUAL>
+__global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
     wpair_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmTok,
                       const __grid_constant__ CUtensorMap tmTokS,
                       const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmWu) {
-  using C = WCfg<KIND, T>;
+  using C = WCfg<KIND, T, DUAL>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::kStages];
   __shared__ __align__(8) uint64_t empty_bar[C::kStages];
@@ -164,8 +172,9 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t smemA = smem_base;
-  const uint32_t smemB = smem_base + C::kStages * C::kABytes;
+  const uint32_t smemA = smem_base;                               // W slots
+  const uint32_t smemB = smem_base + C::kStages * C::kABytes;     // X slots
+  const uint32_t smemT = smemB + C::kStages * C::kBBytes;         // T slots (DUAL)
   float* xchg = reinterpret_cast<float*>(smem_raw + (smem_base - smem_u32(smem_raw)) +
                                          C::kStages * C::kStageBytes);
 
@@ -238,6 +247,38 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
                              : e * a.H + t.nt * 256 + static_cast<int>(rank) * 128;
         int kb, ke;
         split_range(a, t.split, kb, ke);
+        if (DUAL && small) {
+          // two K steps per stage: weights in the W and X slots, token boxes
+          // in the two halves of the T slot
+          for (int kt = kb; kt < ke; kt += 2) {
+            if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, to)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full0 + stage * 8u;
+            const int nk = min(2, ke - kt);
+            const uint32_t st = smemT + stage * C::kTBytes;
+            if (leader)
+              mbar_arrive_expect_tx(smem_u32(&full_bar[stage]),
+                                    2u * static_cast<uint32_t>(nk * (C::kABytes + C::kSmallBytes)));
+            for (int u = 0; u < nk; ++u) {
+              const uint32_t sw = u == 0 ? smemA + stage * C::kABytes : smemB + stage * C::kBBytes;
+              if constexpr (KIND == kGateUp) {
+                tma_load_2d_pair(sw, &tmW, fb, (kt + u) * C::kBK, wrow);
+                tma_load_2d_pair(sw + C::kABytes / 2, &tmWu, fb, (kt + u) * C::kBK,
+                                 wrow + a.up_row_offset);
+              } else {
+                tma_load_2d_pair(sw, &tmW, fb, (kt + u) * C::kBK, wrow);
+              }
+              tma_load_2d_pair(st + u * C::kSmallBytes, &tmTokS, fb, (kt + u) * C::kBK, tok_row);
+            }
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          continue;
+        }
         for (int kt = kb; kt < ke; ++kt) {
           if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, to)) {
             ok = false;
@@ -280,6 +321,41 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * C::kAccCols;
+        if (DUAL && (tile_n(bi.w) >> 1) <= C::kSmallRows) {  // as the producer decides
+          for (int kt = kb; kt < ke; kt += 2) {
+            if (!mbar_wait_bounded_cluster(smem_u32(&full_bar[stage]), phase, &s_abort, to)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const int nk = min(2, ke - kt);
+            for (int u = 0; u < nk; ++u) {
+              const uint32_t a_base =
+                  u == 0 ? smemA + stage * C::kABytes : smemB + stage * C::kBBytes;
+              const uint32_t b_base = smemT + stage * C::kTBytes + u * C::kSmallBytes;
+#pragma unroll
+              for (int k = 0; k < C::kBK / C::kUmmaK; ++k) {
+                const uint64_t ad = sw128_kmajor_desc(a_base + k * 32);
+                const uint64_t bd = sw128_kmajor_desc(b_base + k * 32);
+                const uint32_t accum = (kt > kb || u > 0 || k > 0) ? 1u : 0u;
+                if constexpr (Elem<T>::kFmt == 1)
+                  umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+                else
+                  umma_tf32_pair(d_tmem, ad, bd, idesc, accum);
+              }
+            }
+            umma_commit_pair(smem_u32(&empty_bar[stage]), 0x3);
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          umma_commit_pair(smem_u32(&accf_bar[acc]), 0x3);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+          continue;
+        }
         for (int kt = kb; kt < ke; ++kt) {
           if (!mbar_wait_bounded_cluster(smem_u32(&full_bar[stage]), phase, &s_abort, to)) {
             ok = false;
@@ -476,23 +552,24 @@ __global__ void __launch_bounds__(WCfg<KIND, T>::kThreads, 1)
   }
 }
 
-template <int KIND, typename T>
+template <int KIND, typename T, bool DUAL>
 cudaLaunchConfig_t wpair_config(int grid, cudaStream_t s, cudaLaunchAttribute* attr) {
-  using C = WCfg<KIND, T>;
+  using C = WCfg<KIND, T, DUAL>;
   return pdl_config(dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, attr, 2);
 }
 
-template <int KIND, typename T>
+// Pairs held at once (both instantiations keep one CTA per SM).
+template <int KIND, typename T, bool DUAL = false>
 int max_pairs() {
-  using C = WCfg<KIND, T>;
-  auto kern = wpair_gemm_kernel<KIND, T>;
+  using C = WCfg<KIND, T, DUAL>;
+  auto kern = wpair_gemm_kernel<KIND, T, DUAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = wpair_config<KIND, T>(2, nullptr, attr);
+  cudaLaunchConfig_t cfg = wpair_config<KIND, T, DUAL>(2, nullptr, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
     cudaGetLastError();
@@ -501,17 +578,24 @@ int max_pairs() {
   return n;
 }
 
-template <int KIND, typename T>
-cudaError_t launch(const GemmArgs& a, const CUtensorMap& tmTok, const CUtensorMap& tmTokS,
-                   const CUtensorMap& tmW, const CUtensorMap& tmWu, int grid, cudaStream_t s) {
-  using C = WCfg<KIND, T>;
-  auto kern = wpair_gemm_kernel<KIND, T>;
+template <int KIND, typename T, bool DUAL>
+cudaError_t launch_as(const GemmArgs& a, const CUtensorMap& tmTok, const CUtensorMap& tmTokS,
+                      const CUtensorMap& tmW, const CUtensorMap& tmWu, int grid, cudaStream_t s) {
+  using C = WCfg<KIND, T, DUAL>;
+  auto kern = wpair_gemm_kernel<KIND, T, DUAL>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = wpair_config<KIND, T>(grid, s, attr);
+  cudaLaunchConfig_t cfg = wpair_config<KIND, T, DUAL>(grid, s, attr);
   return cudaLaunchKernelEx(&cfg, kern, a, tmTok, tmTokS, tmW, tmWu);
+}
+
+template <int KIND, typename T>
+cudaError_t launch(const GemmArgs& a, const CUtensorMap& tmTok, const CUtensorMap& tmTokS,
+                   const CUtensorMap& tmW, const CUtensorMap& tmWu, int grid, cudaStream_t s) {
+  if (a.dual_small) return launch_as<KIND, T, true>(a, tmTok, tmTokS, tmW, tmWu, grid, s);
+  return launch_as<KIND, T, false>(a, tmTok, tmTokS, tmW, tmWu, grid, s);
 }
 
 }  // namespace

@@ -107,6 +107,7 @@ struct GemmArgs {
   void* out;                  // gate/up: h (cap, I); down: y (splits, cap, H) fp32, or
                               // the (T, H) fp32 accumulator when `fused`
   int fused;                  // down: add rows into the accumulator (atomics)
+  int dual_small;             // tiles of at most 32 tokens load two K steps per stage
   int32_t* status;
   unsigned long long timeout_ns;
   Epilogue ep;
