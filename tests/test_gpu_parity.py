@@ -183,6 +183,10 @@ STAGE_CASES = [
     (300, 256, 320, 3, 2, "bf16"),   # 2 blocks per expert, ragged I tile
     (77, 192, 256, 5, 2, "bf16"),
     (40, 128, 256, 8, 2, "f32"),     # tf32 path
+    # T <= 32: the decode-like launch, two K steps per stage; 5 K steps of
+    # the down projection leave a last stage with one
+    (8, 256, 320, 8, 2, "bf16"),
+    (12, 128, 256, 4, 3, "f32"),
 ]
 
 
