@@ -17,7 +17,9 @@
 // padding costs next to no tensor-core time and a sparsely used expert's
 // tiles are pure weight streaming.  Per CTA and 64-wide K step (one stage):
 // 128 weight rows (16 KB) and N/2 token rows, loaded as a 16-row box when
-// N <= 32 (decode) and as a 128-row box otherwise; six 32 KB stages.
+// N <= 32 (decode) and as a 128-row box otherwise; six 32 KB stages (seven
+// for the down projection).  Decode-like launches use the DUAL
+// instantiation (WCfg), whose stages of small tiles carry two K steps.
 //  * gate/up: a CTA's 128 weight rows are 64 gate rows and the 64 up rows
 //    with the same indices j, so TMEM lanes 0-63 hold gate and 64-127 up of
 //    the same j for every token column.  The epilogue warp of lanes
