@@ -732,6 +732,40 @@ def test_forward_expert_shard_mx():
     assert_close(out, emu, max_abs=MX_MAX_ABS, rel_l2=MX_REL_EMU, what="mx shard vs emulate")
 
 
+@pytest.mark.parametrize("case", [(300, 256, 320, 3, 2, "bf16", "normal"),
+                                  (8, 256, 320, 8, 2, "bf16", "normal"),
+                                  (33, 128, 256, 8, 2, "f32", "normal")],
+                         ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s_%s" % c)
+def test_forward_cuda_graph_replay(case):
+    """moe_forward captured in a CUDA graph: every replay gives the eager
+    output bit for bit (the default combine is deterministic)."""
+    cfg = gen.MoEConfig("graph", *case)
+    d = gen.generate(cfg, seed=34).to("cuda")
+    eager, _ = _run_forward(d, cfg)
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype)
+    ws = moe.Workspace(p)
+    out = torch.full((cfg.T, cfg.H), float("nan"), dtype=d.x.dtype, device="cuda")
+    s = torch.cuda.Stream()
+
+    def fwd():
+        moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, d.w13, None, d.w2, None, out,
+                        ws.buffer, ws.nbytes, s)
+
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fwd()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
+        fwd()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_status(ws.status) == 0
+        assert torch.equal(out, eager)
+
+
 # ------------------------------------------------------------------ fused combine
 
 def _run_forward_fused(d, cfg, block_m=0, **kw):
