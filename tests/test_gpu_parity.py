@@ -712,6 +712,20 @@ def test_forward_expert_shards(dtype):
     assert_close(total, full.double().cpu().numpy(), max_abs=4e-2, what="sum of shards")
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_forward_expert_shard_decode(fused):
+    """A decode-sized batch (two K steps per stage) on one shard of 8 of 16
+    experts, with either combine."""
+    cfg = gen.MoEConfig("shard_dec", 8, 256, 1536, 16, 2, "bf16", "normal")
+    inp = gen.generate(cfg, seed=45)
+    d = inp.to("cuda")
+    base, L = 4, 8
+    out = moe.forward(d.x, d.topk_ids, d.topk_weights, d.w13[base:base + L].contiguous(),
+                      d.w2[base:base + L].contiguous(), num_experts=cfg.E, expert_base=base,
+                      fused_combine=fused)
+    assert_close(out, _oracle_shard(inp, base, L, np.arange(cfg.T)), what="decode shard")
+
+
 def test_forward_expert_shard_mx():
     cfg = gen.MoEConfig("shard_mx", 96, 256, 320, 16, 4, "mxfp4", "uniform")
     inp = gen.generate(cfg, seed=42)
