@@ -312,11 +312,12 @@ GemmArgs base_args(const moe_problem_t* p) {
   a.cap = capacity(p->T, p->K, local_experts(p), block_m_of(p));
   a.timeout_ns = kWaitTimeoutNs;
   a.ep = epilogue_of(p);
-  // decode-like launches, where (nearly) every align block holds at most 32
-  // tokens: at most 32 tokens in all, or at most 8 rows per expert on
-  // average.  Their tiles stream weights, and two K steps per stage double
-  // the bytes in flight; mixed with large tiles that measured slower.
-  a.dual_small = p->T <= 32 || static_cast<long long>(p->T) * p->K <= 8ll * local_experts(p);
+  // decode-like launches, where most align blocks hold at most 32 tokens:
+  // at most 32 tokens in all, or at most 32 rows per expert on average.
+  // Their tiles stream weights, and two K steps per stage double the bytes
+  // in flight; in prefill launches (hundreds of rows per expert) the same
+  // stages measured slower.
+  a.dual_small = p->T <= 32 || static_cast<long long>(p->T) * p->K <= 32ll * local_experts(p);
   return a;
 }
 
