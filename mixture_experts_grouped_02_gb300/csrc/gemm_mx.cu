@@ -112,9 +112,9 @@ __device__ __forceinline__ float activate(const Epilogue& ep, float g, float u) 
   if (ep.act == MOE_ACT_SWIGLU_CLAMP) {
     g = fminf(g, ep.limit);
     u = fmaxf(fminf(u, ep.limit), -ep.limit);
-    return g / (1.0f + __expf(-ep.alpha * g)) * (u + 1.0f);
+    return __fdividef(g, 1.0f + __expf(-ep.alpha * g)) * (u + 1.0f);
   }
-  return g / (1.0f + __expf(-g)) * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // Scale image of (expert, section, 96-row group, K tile).
