@@ -123,15 +123,20 @@ uint8_t orc_float_to_e4m3(float f) {
     return (uint8_t)((neg << 7) | best);
 }
 
-/* double -> bf16 -> double, round to nearest even (EMULATE mode only). */
+/* double -> nearest bfloat16 value (ties to even), rounded once from the
+ * double (EMULATE mode only).  bf16 keeps 8 significant bits: the spacing of
+ * the values around v is 2^(e-8) for v = m 2^e with 0.5 <= |m| < 1, and
+ * 2^-133 at the bottom of the subnormal range; rint rounds half to even.
+ * Values past the largest finite bf16, (2 - 2^-7) 2^127, become infinite. */
 static double round_to_bf16(double v) {
-    float f = (float)v; /* exact for the value range used; EMULATE is diagnostic */
-    uint32_t u;
-    memcpy(&u, &f, 4);
-    uint32_t lsb = (u >> 16) & 1u;
-    u = (u + 0x7FFFu + lsb) & 0xFFFF0000u;
-    memcpy(&f, &u, 4);
-    return (double)f;
+    if (!isfinite(v) || v == 0.0) return v;
+    int e;
+    frexp(v, &e);
+    int q = e - 8;
+    if (q < -133) q = -133;
+    double r = ldexp(rint(ldexp(v, -q)), q);
+    if (fabs(r) > ldexp(2.0 - ldexp(1.0, -7), 127)) r = copysign(INFINITY, v);
+    return r;
 }
 
 /* ------------------------------------------------------------------ */

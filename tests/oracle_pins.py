@@ -442,6 +442,98 @@ def pin_lowp_forward_loop_orders():
     assert 1e-4 < rel < 0.1, rel
 
 
+def _e4m3_nearest_torch(v):
+    """Nearest e4m3 value of each fp32 v by torch's own cast (round to
+    nearest even), after saturating to the largest finite code, 448."""
+    v = np.clip(np.asarray(v, np.float32), -448.0, 448.0)
+    return torch.from_numpy(v).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _hidden_rows(a_over_scale, h_scale, mode):
+    """h of one slot of an expert whose gate pre-activations are all 64 and
+    whose up pre-activations are u_j = v_j h_scale / 64 (H = 1, x = 1).
+    SiLU(64) = 64 in fp64 (e^-64 is far below half an ulp of 1), so the
+    activation is a_j = 64 u_j = v_j h_scale exactly and a_j / h_scale = v_j."""
+    v = np.asarray(a_over_scale, np.float64)
+    I = len(v)
+    u = (v * h_scale / 64.0).astype(np.float32)
+    assert np.array_equal(u.astype(np.float64) * 64.0 / h_scale, v)  # dyadic, exact
+    w13 = np.concatenate([np.full(I, 64.0, np.float32), u]).reshape(1, 2 * I, 1)
+    x = np.ones((1, 1), np.float32)
+    P = oracle.make_problem(1, 1, I, 1, 1, x, w13, h_e4m3=True, h_scale=h_scale)
+    one = np.zeros(1, np.int32)
+    return oracle.gemm1_silu_rows(P, x, w13, one, one, one, mode=mode)[0]
+
+
+def pin_e4m3_hidden_store():
+    """The e4m3 hidden activation of the low-precision path ("MOE Bmm1 Fused
+    Gather", pack_fp8_out_fragment: out times 1/out_scale, then e4m3): in
+    EMULATE mode the oracle keeps e4m3(a / h_scale) h_scale.  a / h_scale is
+    placed on e4m3 grid points, on midpoints between neighbouring codes (ties
+    go to the even code), past the saturation point 448 and below half the
+    smallest subnormal; torch's float8 cast gives the expected codes."""
+    grid = [1.0, 1.125, 2.0 ** -6, 2.0 ** -9, 448.0, 240.0, -3.5, 0.0]
+    mids = [1.0625, 1.1875, 3.125, 3.375, -1.0625, 2.0 ** -6 + 2.0 ** -10, 232.0]
+    extremes = [500.0, -1000.0, 2.0 ** -11]
+    v = np.array(grid + mids + extremes)
+    for h_scale in (4.0, 0.25):
+        got = _hidden_rows(v, h_scale, oracle.EMULATE)
+        assert np.array_equal(got, _e4m3_nearest_torch(v) * h_scale), (h_scale, got)
+        # EXACT mode keeps the activation unrounded
+        assert np.array_equal(_hidden_rows(v, h_scale, oracle.EXACT), v * h_scale)
+    # hand-checked neighbours: ties to the even mantissa, saturation, underflow
+    got = _hidden_rows([1.0625, 1.1875, 500.0, 2.0 ** -11], 4.0, oracle.EMULATE)
+    assert got.tolist() == [4.0, 5.0, 448.0 * 4.0, 0.0], got
+
+
+def pin_e4m3_hidden_in_down_projection():
+    """The down projection reading e4m3 hidden codes decodes code x h_scale:
+    against torch's float8_e4m3fn decode times h_scale, a float64 product
+    with W2 (plain fp32 weights, and mxfp4 weights dequantised by torch ops)
+    and the routing weight of each slot."""
+    rng = np.random.default_rng(15)
+    T, H, I, E, K, hs = 6, 24, 64, 3, 2, 0.25
+    na = T * K
+    codes = rng.integers(0, 256, (na, I)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38  # no NaN codes
+    hdeq = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64) * hs
+    eor = rng.integers(0, E, na).astype(np.int32)
+    topk_w = rng.random(na).astype(np.float32)
+    slots = np.arange(na, dtype=np.int32)
+    w2_f32 = rng.standard_normal((E, H, I)).astype(np.float32)
+    w2_mx = rng.integers(0, 256, (E, H, I // 2)).astype(np.uint8)
+    s2_mx = rng.integers(120, 135, (E, H, I // 32)).astype(np.uint8)
+    for w2, s2, W in ((w2_f32, None, torch.from_numpy(w2_f32).to(torch.float64)),
+                      (w2_mx, s2_mx, dequant_mx(torch.from_numpy(w2_mx), torch.from_numpy(s2_mx)))):
+        x = np.zeros((1, H), np.float32)
+        # the weight format of the problem follows w13's storage type
+        w13 = np.zeros((1, 2 * I, H), np.float32) if s2 is None else np.zeros((1, 2 * I, H // 2),
+                                                                               np.uint8)
+        P = oracle.make_problem(T, H, I, E, K, x, w13, h_e4m3=True, h_scale=hs)
+        y = oracle.gemm2_weighted_rows(P, codes, w2, topk_w, slots, eor, slots, w2_scale=s2,
+                                       h_is_e4m3=True)
+        ref = torch.stack([float(topk_w[r]) * (W[eor[r]] @ hdeq[r]) for r in range(na)])
+        assert np.allclose(y, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_bf16_hidden_store():
+    """EMULATE mode with bf16 activations rounds each a_j once to the nearest
+    bfloat16 (ties to even).  Gate 64 and up 1 + 2^-8 give a = 64.25, the
+    midpoint of the bf16 neighbours 64 and 64.5: the even one, 64.  Up
+    1 + 2^-8 + 2^-30 puts a 2^-24 above that midpoint: 64.5 (rounding through
+    fp32 first would lose the 2^-24 and give 64)."""
+    x = torch.ones(1, 3, dtype=torch.bfloat16)
+    for up, want in (([1.0, 2.0 ** -8, 0.0], 64.0), ([1.0, 2.0 ** -8, 2.0 ** -30], 64.5),
+                     ([1.0, 3 * 2.0 ** -9, 0.0], 64.5)):
+        w13 = torch.tensor([[[64.0, 0.0, 0.0], up]], dtype=torch.bfloat16)
+        assert w13.to(torch.float64)[0, 1].tolist() == up  # each entry exact in bf16
+        P = oracle.make_problem(1, 3, 1, 1, 1, np_store(x), np_store(w13))
+        one = np.zeros(1, np.int32)
+        h = oracle.gemm1_silu_rows(P, np_store(x), np_store(w13), one, one, one,
+                                   mode=oracle.EMULATE)
+        assert h[0, 0] == want, (up, h[0, 0])
+
+
 # ---------------------------------------------------------------- shard pins
 
 SHARDS = [(0, 3), (3, 3), (6, 2)]  # an uneven partition of E = 8 experts
@@ -676,7 +768,8 @@ FFN_PINS = [
     pin_weighted_sum_over_slots, pin_loop_orders_agree, pin_zero_input, pin_linearity,
     pin_silu_closed_forms, pin_token_subset, pin_emulate_close_to_exact, pin_stage_composition,
     pin_mx_weights_dense_mlp, pin_mx_scale_block_is_32, pin_mx_nibble_order,
-    pin_lowp_forward_loop_orders,
+    pin_lowp_forward_loop_orders, pin_e4m3_hidden_store, pin_e4m3_hidden_in_down_projection,
+    pin_bf16_hidden_store,
 ]
 FORMAT_PINS = [pin_e4m3_decode_vs_torch, pin_float_to_e4m3_vs_torch, pin_e2m1_e8m0,
                pin_quantize_x_fp8]

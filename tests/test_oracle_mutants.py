@@ -60,6 +60,19 @@ MUTANTS = [
      "for (int k = 0; k < K; ++k) sum += exp(v[0] - v[0]);"),
     ("route_keeps_taken", "if (taken[e]) continue;", "if (0) continue;"),
     ("shard_other_slots_keep_slot", "        inv_perm[i] = -1;\n", "        inv_perm[i] = 0;\n"),
+    ("h_scale_multiplies_in_store", "float q = (float)(a / p->h_scale);",
+     "float q = (float)(a * p->h_scale);"),
+    ("h_scale_dropped_in_store", "return orc_e4m3_to_double(orc_float_to_e4m3(q)) * p->h_scale;",
+     "return orc_e4m3_to_double(orc_float_to_e4m3(q));"),
+    ("h_scale_twice_in_store", "return orc_e4m3_to_double(orc_float_to_e4m3(q)) * p->h_scale;",
+     "return orc_e4m3_to_double(orc_float_to_e4m3(q)) * p->h_scale * p->h_scale;"),
+    ("h_scale_dropped_in_down",
+     "a[j] = orc_e4m3_to_double(((const uint8_t*)hin)[base + j]) * p->h_scale;",
+     "a[j] = orc_e4m3_to_double(((const uint8_t*)hin)[base + j]);"),
+    ("bf16_rounds_through_fp32", "double r = ldexp(rint(ldexp(v, -q)), q);",
+     "double r = ldexp(rint(ldexp((double)(float)v, -q)), q);"),
+    ("bf16_ties_away_from_zero", "double r = ldexp(rint(ldexp(v, -q)), q);",
+     "double r = ldexp(round(ldexp(v, -q)), q);"),
     ("shard_weight_index_global", "e -= p->expert_base; /* index into this shard's weights */",
      "e = e % shard_size(p);"),
 ]
