@@ -414,13 +414,22 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
  *    contents; the status word that must start at zero is cleared by each
  *    call.  Calls whose execution overlaps on the GPU race on the array:
  *    issue them in one stream order.
- * The device status word of the last call is at offset 0 of the array and
- * is reported by the call's own errors only; use moe_forward with a
- * workspace to read it with moe_get_device_status. */
+ *  - Argument errors give the same status codes as moe_forward.
+ * Errors the kernels find (an expert id outside [0, E), a pipeline wait
+ * that ran out) go to the device status word at offset 0 of the array, as
+ * they do to a workspace's: the call still returns MOE_OK, later stages skip
+ * their writes and out is left unspecified.  Read the word with
+ * moe_forward_noalloc_status. */
 #define MOE_STATIC_SCRATCH_BYTES (64u << 20)
 int moe_forward_noalloc(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                         const float* topk_weights, const void* w13, const uint8_t* w13_scale,
                         const void* w2, const uint8_t* w2_scale, void* out, void* stream);
+
+/* The device status word of the last moe_forward_noalloc on the current
+ * device: synchronises `stream` and returns MOE_OK when the word is 0, its
+ * code otherwise (as moe_get_device_status does for a workspace), or
+ * MOE_ERR_CUDA.  No counterpart on the pages.  Allocates nothing. */
+int moe_forward_noalloc_status(void* stream);
 
 /* Launch geometry of the current device: its SM count and how many CTA pairs
  * of the bf16 gate/up kernel it holds at once (0 if unknown). */

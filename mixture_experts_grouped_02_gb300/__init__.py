@@ -15,13 +15,13 @@ from ._abi import (MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP, MOE_BF16, MOE_E2M1_MX, MO
                    MoEError, Problem, moe_abi_version,
                    moe_align, moe_align_capacity, moe_align_local, moe_combine, moe_forward,
                    moe_route_align, moe_align_scratch_bytes, moe_combine_finish,
-                   moe_forward_noalloc, moe_gather_rows, moe_gemm1_silu, moe_gemm2_default_splits,
+                   moe_forward_noalloc, moe_forward_noalloc_status, moe_gather_rows, moe_gemm1_silu, moe_gemm2_default_splits,
                    moe_gemm2_weighted, moe_get_device_status, moe_mx_packed_bytes,
                    moe_pack_mx_weights, moe_quantize_gather_x_fp8, moe_quantize_x_fp8,
                    moe_resolve_block_m, moe_workspace_offsets, moe_workspace_size)
 
 __all__ = ["MOE_ACT_SILU", "MOE_ACT_SWIGLU_CLAMP", "MoEError", "Problem", "make_problem", "dtype_code", "align", "Workspace", "forward",
-           "pack_mx", "moe_forward_noalloc", "moe_mx_packed_bytes", "moe_pack_mx_weights",
+           "pack_mx", "moe_forward_noalloc", "moe_forward_noalloc_status", "moe_mx_packed_bytes", "moe_pack_mx_weights",
            "moe_quantize_gather_x_fp8", "moe_gather_rows",
            "moe_abi_version", "moe_align", "moe_align_capacity", "moe_align_local",
            "moe_align_scratch_bytes", "moe_combine_finish",

@@ -37,7 +37,7 @@ EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_a
            "moe_forward", "moe_forward_noalloc", "moe_get_device_status", "moe_mx_packed_bytes",
            "moe_pack_mx_weights", "moe_quantize_gather_x_fp8", "moe_device_info",
            "moe_gather_rows", "moe_align_local", "moe_route_align", "moe_align_scratch_bytes",
-           "moe_combine_finish")
+           "moe_combine_finish", "moe_forward_noalloc_status")
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
 MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP = 0, 1
@@ -128,6 +128,8 @@ def _declare(L):
     L.moe_forward.argtypes = [PP] + [vp] * 9 + [sz, vp]
     L.moe_forward_noalloc.restype = i32
     L.moe_forward_noalloc.argtypes = [PP] + [vp] * 9
+    L.moe_forward_noalloc_status.restype = i32
+    L.moe_forward_noalloc_status.argtypes = [vp]
     L.moe_get_device_status.restype = i32
     L.moe_get_device_status.argtypes = [vp, vp]
     L.moe_device_info.restype = i32
@@ -295,6 +297,15 @@ def moe_forward_noalloc(p: Problem, x, topk_ids, topk_weights, w13, w13_scale, w
     _check(lib().moe_forward_noalloc(ctypes.byref(p), _p(x), _p(topk_ids), _p(topk_weights),
                                      _p(w13), _p(w13_scale), _p(w2), _p(w2_scale), _p(out),
                                      _stream(stream)), "moe_forward_noalloc")
+
+
+def moe_forward_noalloc_status(stream=None) -> int:
+    """The device status word of the last moe_forward_noalloc on the current
+    device (synchronises the stream): 0, or the kernels' error code."""
+    rc = lib().moe_forward_noalloc_status(_stream(stream))
+    if rc == MOE_ERR_CUDA:
+        raise MoEError(rc, "moe_forward_noalloc_status")
+    return rc
 
 
 def moe_mx_packed_bytes(E, R, K, sections):

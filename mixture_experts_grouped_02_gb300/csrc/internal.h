@@ -10,6 +10,11 @@
 
 namespace moe {
 
+// The argument checks moe_forward makes on a problem before any launch
+// (shapes, dtypes, shard, epilogue, GEMM shape support): MOE_OK or the
+// status moe_forward returns for it.
+int validate_forward_problem(const moe_problem_t* p);
+
 // Default wall-clock limit of any single pipeline wait inside a kernel.
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 

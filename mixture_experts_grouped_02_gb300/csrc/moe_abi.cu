@@ -507,6 +507,11 @@ int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const u
 
 }  // namespace
 
+int moe::validate_forward_problem(const moe_problem_t* p) {
+  const int rc = check_problem(p);
+  return rc != MOE_OK ? rc : check_gemm_shapes(p);
+}
+
 extern "C" {
 
 const char* moe_status_string(int status) {
@@ -771,9 +776,7 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                 const float* topk_weights, const void* w13, const uint8_t* w13_scale,
                 const void* w2, const uint8_t* w2_scale, void* out, void* workspace,
                 size_t workspace_bytes, void* stream) {
-  int rc = check_problem(p);
-  if (rc != MOE_OK) return rc;
-  rc = check_gemm_shapes(p);
+  int rc = validate_forward_problem(p);
   if (rc != MOE_OK) return rc;
   if (p->T == 0) return MOE_OK;
   if (!x || !topk_ids || !topk_weights || !w13 || !w2 || !out || !workspace)

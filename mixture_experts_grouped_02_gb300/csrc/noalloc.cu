@@ -57,12 +57,26 @@ extern "C" int moe_forward_noalloc(const moe_problem_t* p, const void* x, const 
                                    const float* topk_weights, const void* w13,
                                    const uint8_t* w13_scale, const void* w2,
                                    const uint8_t* w2_scale, void* out, void* stream) {
-  const size_t need = moe_workspace_size(p);
-  if (need == 0) return MOE_ERR_INVALID_ARG;
-  if (need > static_cast<size_t>(MOE_STATIC_SCRATCH_BYTES)) return MOE_ERR_WORKSPACE;
+  // the same argument checks, and so the same status codes, as moe_forward;
+  // the size limit of the static array comes after them
+  int rc = moe::validate_forward_problem(p);
+  if (rc != MOE_OK) return rc;
+  if (moe_workspace_size(p) > static_cast<size_t>(MOE_STATIC_SCRATCH_BYTES))
+    return MOE_ERR_WORKSPACE;
   void* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
+  rc = scratch_address(&scratch);
   if (rc != MOE_OK) return rc;
   return moe_forward(p, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, out, scratch,
                      static_cast<size_t>(MOE_STATIC_SCRATCH_BYTES), stream);
+}
+
+// The status word of the last moe_forward_noalloc on the current device
+// sits at offset 0 of the static array (moe_forward's workspace layout puts
+// it first).  Reading it needs the array's device address, which only this
+// file knows, and a copy of 4 bytes to the host: nothing is allocated.
+extern "C" int moe_forward_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != MOE_OK) return rc;
+  return moe_get_device_status(static_cast<const int32_t*>(scratch), stream);
 }

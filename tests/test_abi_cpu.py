@@ -166,6 +166,17 @@ def test_entry_points_reject_bad_arguments_before_launch():
     for base, local in ((1, 0), (-1, 3), (6, 3)):
         bad = make_problem(16, 128, 256, 8, 2, "bf16", expert_base=base, local_experts=local)
         assert _abi.moe_workspace_size(bad) == 0
+    # the forward without a workspace returns moe_forward's codes for the
+    # same arguments, and refuses problems beyond its static array
+    for p, code in ((make_problem(16, 100, 256, 8, 2, "bf16"), _abi.MOE_ERR_UNSUPPORTED),
+                    (make_problem(16, 128, 256, 2048, 2, "bf16"), _abi.MOE_ERR_UNSUPPORTED),
+                    (make_problem(16, 128, 256, 8, 2, "bf16", block_m=48),
+                     _abi.MOE_ERR_INVALID_ARG),
+                    (make_problem(4096, 4096, 14336, 8, 2, "bf16"), _abi.MOE_ERR_WORKSPACE)):
+        assert L.moe_forward_noalloc(ctypes.byref(p), *([fake] * 9)) == code
+        if code != _abi.MOE_ERR_WORKSPACE:
+            assert L.moe_forward(ctypes.byref(p), *([fake] * 9), 1 << 40, None) == code
+    assert L.moe_forward_noalloc(None, *([fake] * 9)) == _abi.MOE_ERR_INVALID_ARG
 
 
 def test_product_package_does_not_import_oracle():
