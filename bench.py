@@ -36,11 +36,20 @@ import torch  # noqa: E402
 from mixture_experts_grouped_02_gb300 import inputs as gen  # noqa: E402
 
 METRIC = "MoE layer tokens/sec and TFLOP/s (prefill); HBM GB/s (decode) vs GB300 peak"
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_gate_up_mixtral_prefill.md")
-# the gate/up kernel's own sources (the shared headers also serve the other
-# kernels, whose edits do not change this one)
-KERNEL_SOURCES = [os.path.join(ROOT, "mixture_experts_grouped_02_gb300", "csrc", f)
-                  for f in ("gemm_wpair.cu", "sched.cuh")]
+# per-launch DRAM bytes of the dominant kernels from ncu captures, with the
+# hash of the kernel sources they were taken on
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+CSRC = os.path.join(ROOT, "mixture_experts_grouped_02_gb300", "csrc")
+# each GEMM's own sources (the shared headers also serve the other kernels,
+# whose edits do not change this one)
+KERNEL_SOURCES = {"wpair": ("gemm_wpair.cu", "sched.cuh"), "mx": ("gemm_mx.cu", "sched.cuh")}
+# nominal dense GB300 figures (context beside the measured ones): HBM3e
+# 8 TB/s, bf16 tensor 2.25 PFLOP/s, fp8 4.5 PFLOP/s
+NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}
+# the workloads timed besides the default one, each graded on its own bound
+# (ordered so that workloads sharing a weight shape run one after another)
+WORKLOADS = ([f"mixtral_decode_T{t}" for t in gen.DECODE_T] + ["dsv3_prefill"] +
+             [f"dsv3_decode_T{t}" for t in gen.DECODE_T] + ["lowp", "lowp_oai"])
 
 
 def parse():
@@ -65,6 +74,10 @@ def parse():
     ap.add_argument("--ep-shards", type=int, default=8,
                     help="expert shards of the layer in the sweep (one is timed)")
     ap.add_argument("--ep-rank", type=int, default=0, help="the shard the sweep times")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip timing the other workloads (the 'workloads' list)")
+    ap.add_argument("--workload-steps", type=int, default=10,
+                    help="timed steps per workload of the 'workloads' list (3 warm-up steps)")
     return ap.parse_args()
 
 
@@ -123,31 +136,26 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(family: str) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+    for f in KERNEL_SOURCES[family]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """Per-launch DRAM bytes of the gate/up GEMM from the committed ncu
-    summary, or None when the kernel changed since it was captured."""
+def profiled_traffic(workload: str, kernel: str, mx: bool):
+    """Per-launch DRAM bytes (read + write) of `kernel` on `workload` from the
+    committed ncu figures, or None when there are none or the kernel's
+    sources changed since they were taken."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
-    vals = {}
     with open(PROFILE_TRAFFIC) as f:
-        for line in f:
-            if ":" in line and line.strip().startswith("- "):
-                k, v = line.strip()[2:].split(":", 1)
-                vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        table = json.load(f)
+    rec = table.get(workload, {}).get(kernel)
+    if not rec or rec.get("kernel_source_sha256") != kernel_source_hash("mx" if mx else "wpair"):
         return None
-    try:
-        return int(float(vals["traffic_bytes_per_launch_full"]))
-    except (KeyError, ValueError):
-        return None
+    return int(rec["traffic_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -374,6 +382,106 @@ def build_stages(moe, _abi, cfg, inp, dev, block_m=0, shard=None, fused=False):
     return stages, p, wsp, (w13, s13, w2, s2), out, bm, stream
 
 
+def time_stage_loop(stages, stream, dev, warmup, steps):
+    """Run `warmup` untimed steps, then `steps` timed ones with an event
+    before the first stage and after every stage of every step; returns
+    (mean ms per step, {stage: mean ms})."""
+    for _ in range(warmup):
+        for _, f in stages:
+            f()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+          for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        for j, (_, f) in enumerate(stages):
+            f()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    total = statistics.mean(ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps))
+    stage_ms = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
+                for j, (n, _) in enumerate(stages)}
+    return total, stage_ms
+
+
+def graded_roofline(cfg, kern, ms_step, bytes_alg, hbm_gbs, bf16_tflops):
+    """The workload's grade: prefill on the tensor cores (bf16 dense), decode
+    and the low-precision layer on HBM bandwidth, taken for the dominant GEMM
+    and for the whole step (roofline time max(FLOPs / tensor peak, bytes /
+    HBM peak) over the step time), against the measured and nominal peaks."""
+    dom = max(kern, key=lambda k: kern[k]["ms"])
+    d = kern[dom]
+    tensor = "prefill" in cfg.name
+    out = {"kernel": dom, "kernel_ms": d["ms"], "bound": "tensor" if tensor else "hbm"}
+    if tensor:
+        out.update(achieved=d["tflops"], unit="TFLOP/s", peak=bf16_tflops,
+                   frac=d["tflops"] / bf16_tflops, peak_nominal=NOMINAL["bf16_tflops"],
+                   frac_nominal=d["tflops"] / NOMINAL["bf16_tflops"],
+                   other_bound_frac={"hbm": d["gbs"] / hbm_gbs})
+    else:
+        out.update(achieved=d["gbs"], unit="GB/s", peak=hbm_gbs, frac=d["gbs"] / hbm_gbs,
+                   peak_nominal=NOMINAL["hbm_gbs"], frac_nominal=d["gbs"] / NOMINAL["hbm_gbs"],
+                   other_bound_frac={"tensor": d["tflops"] / bf16_tflops})
+    mx = cfg.dtype == "mxfp4"
+    # the block-scaled MMAs run at the fp8 rate: twice the bf16 one
+    tc = bf16_tflops * (2 if mx else 1)
+    t_roof = max(cfg.flops / (tc * 1e12), bytes_alg / (hbm_gbs * 1e9)) * 1e3
+    out["step_roofline_ms"] = t_roof
+    out["step_frac"] = t_roof / ms_step
+    return out
+
+
+def run_workloads(moe, _abi, args, dev, main_cfg, main_inp):
+    """Time every other workload at full size (device-drawn inputs, weights
+    drawn once per weight shape and shared by the workloads of that shape),
+    `args.workload_steps` steps each after 3 warm-up steps, with events
+    around every stage.  Returns one record per workload."""
+    hbm_gbs, bf16_burst, _, _ = peaks()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    t0 = time.time()
+    records = []
+    weights = {}
+    for name in WORKLOADS:
+        cfg = gen.config(name)
+        key = (cfg.H, cfg.I, cfg.E, cfg.dtype)
+        if key == (main_cfg.H, main_cfg.I, main_cfg.E, main_cfg.dtype):
+            weights[key] = (main_inp.w13, main_inp.w2, main_inp.w13_scale, main_inp.w2_scale)
+        if key not in weights:
+            weights.clear()  # one weight shape resident at a time
+            torch.cuda.empty_cache()
+            weights[key] = gen.draw_weights(cfg, seed=0, device=dev)
+        w13, w2, s13, s2 = weights[key]
+        ids, w = gen.route(gen.router_logits(cfg, 0, dev), cfg.K)
+        inp = gen.MoEInputs(cfg, gen.draw_x(cfg, 0, dev), w13, w2, ids, w, s13, s2)
+        if cfg.activation == "swiglu_oai":
+            gen.draw_swiglu_oai(inp, seed=0, device=dev)
+        stages, p, wsp, _, _, bm, stream = build_stages(moe, _abi, cfg, inp, dev, 0)
+        ms_step, stage_ms = time_stage_loop(stages, stream, dev, 3, args.workload_steps)
+        status = moe.moe_get_device_status(wsp.status, stream)
+        if status != 0:
+            raise RuntimeError(f"{name}: device status {status}")
+        bytes_alg, active = bytes_algorithmic(cfg, inp)
+        kern = kernel_rooflines(cfg, inp, active, stage_ms["gemm_gate_up"],
+                                stage_ms["gemm_down"], hbm_gbs, bf16_burst)
+        roof = graded_roofline(cfg, kern, ms_step, bytes_alg, hbm_gbs, bf16_burst)
+        roof["traffic"] = profiled_traffic(name, roof["kernel"], cfg.dtype == "mxfp4")
+        records.append({
+            "workload": name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.K,
+            "dtype": cfg.dtype, "block_m": bm, "k_splits": moe.moe_gemm2_default_splits(p),
+            "steps": args.workload_steps, "ms_per_step": ms_step,
+            "tokens_per_s": cfg.T / (ms_step * 1e-3),
+            "tflops": cfg.flops / (ms_step * 1e-3) / 1e12,
+            "hbm_gbs_algorithmic": bytes_alg / (ms_step * 1e-3) / 1e9,
+            "algorithmic_bytes": bytes_alg, "flops": cfg.flops, "active_experts": active,
+            "stage_ms": stage_ms, "kernels": kern, "roofline": roof})
+        del stages, p, wsp, inp
+    weights.clear()
+    torch.cuda.empty_cache()
+    clocks = sampler.stop(t0, time.time())
+    return records, clocks
+
+
 def cuda_graph_ms(moe, p, buf, weights, wsp, dev, reps):
     """Capture moe_forward on its own stream into a CUDA graph (after one
     eager call on that stream) and time `reps` back-to-back replays."""
@@ -490,8 +598,7 @@ def run_ours(args, ws, rank, local):
     d = kern[dom]
     # the bound of the dominant kernel: its algorithmic intensity against the ridge
     tensor_bound = d["flops"] / d["bytes"] > bf16_tflops * 1e12 / (hbm_gbs * 1e9)
-    traffic = profiled_traffic() if (cfg.name == "mixtral_prefill" and dom == "gemm_gate_up") \
-        else None
+    traffic = profiled_traffic(cfg.name, dom, mx)
     if tensor_bound:
         roof = {"bound": "tensor", "achieved": d["tflops"], "peak": bf16_tflops,
                 "unit": "TFLOP/s", "frac": d["tflops"] / bf16_tflops,
@@ -499,10 +606,13 @@ def run_ours(args, ws, rank, local):
                                + ("(sustained: sw_power_cap seen in the timed region)" if capped
                                   else "(burst)"),
                 "frac_of_burst": d["tflops"] / bf16_burst,
-                "frac_of_sustained": d["tflops"] / bf16_sustained}
+                "frac_of_sustained": d["tflops"] / bf16_sustained,
+                "peak_nominal": NOMINAL["bf16_tflops"],
+                "frac_nominal": d["tflops"] / NOMINAL["bf16_tflops"]}
     else:
         roof = {"bound": "hbm", "achieved": d["gbs"], "peak": hbm_gbs, "unit": "GB/s",
-                "frac": d["gbs"] / hbm_gbs, "peak_source": f"{peak_kind} HBM copy"}
+                "frac": d["gbs"] / hbm_gbs, "peak_source": f"{peak_kind} HBM copy",
+                "peak_nominal": NOMINAL["hbm_gbs"], "frac_nominal": d["gbs"] / NOMINAL["hbm_gbs"]}
     roof.update({"kernel": dom, "traffic": traffic, "flops_per_launch": d["flops"],
                  "algorithmic_bytes_per_launch": d["bytes"]})
 
@@ -569,6 +679,11 @@ def run_ours(args, ws, rank, local):
     if moe.moe_get_device_status(st, stream) != 0:
         raise RuntimeError("device status after the graph replays")
 
+    workloads, workloads_clocks = None, None
+    if rank == 0 and ws == 1 and not args.no_workloads and args.shrink == 1 and \
+            cfg.name == "mixtral_prefill":
+        workloads, workloads_clocks = run_workloads(moe, _abi, args, dev, cfg, inp)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         inp_cpu = inp.to("cpu")
@@ -611,6 +726,14 @@ def run_ours(args, ws, rank, local):
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
+        if workloads is not None:
+            line["workloads"] = workloads
+            line["workloads_clocks"] = workloads_clocks
+            line["workloads_note"] = (
+                "every other workload at full size, device-drawn inputs, 3 warm-up and "
+                f"{args.workload_steps} timed steps each, stage-by-stage C-ABI calls with CUDA "
+                "events around every stage; roofline.frac against the measured peaks "
+                "(bf16 burst, HBM copy), frac_nominal against 2.25 PFLOP/s and 8 TB/s")
         print(json.dumps(line), flush=True)
 
 

@@ -104,18 +104,27 @@ int down_tile_k(const moe_problem_t* p) { return is_mx(p) ? 128 : (p->act == MOE
 
 size_t act_bytes(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
 
+// Launch geometry of each device, looked up once per device (the current
+// device at the time of the call).
 struct DeviceInfo {
   int sms = 0;
+  int pairs[2][2] = {{-1, -1}, {-1, -1}};  // [kind][bf16]: CTA pairs held at once
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-int sm_count() {
+int current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
-    return 152;
+    return -1;
   }
+  return dev;
+}
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 152;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   if (g_dev[dev].sms == 0) {
     int n = 0;
@@ -325,10 +334,10 @@ GemmArgs base_args(const moe_problem_t* p) {
 // (cluster placement can leave SMs without a partner), so that every pair
 // is resident from the start, and no more than there are tiles.
 int pair_limit(int kind, int dtype) {
-  static std::mutex mu;
-  static int cache[2][2] = {{-1, -1}, {-1, -1}};
-  std::lock_guard<std::mutex> lk(mu);
-  int& v = cache[kind][dtype == MOE_BF16 ? 1 : 0];
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  int& v = g_dev[dev].pairs[kind][dtype == MOE_BF16 ? 1 : 0];
   if (v < 0) v = wpair_max_active(kind, dtype);
   return v;
 }
