@@ -259,15 +259,24 @@ int moe_route_align(const void* logits, int logit_dtype, int T, int E, int K, in
  *   natural form of a weight tensor with E experts, R rows, K elements along
  *   the reduction: values (E, R, K/2) bytes, e2m1 pairs, lower K index in the
  *   low nibble; scales (E, R, K/32) e8m0 bytes.
- *   packed values: (E, R, Kp/2) bytes, Kp = K rounded up to 128, zero
- *   nibbles past K (so that one TMA copy per 128-element K tile expands a
- *   tile into the 16-byte slots the MMA reads 4-bit operands from);
- *   packed scales: 512-byte images (E, sections, G, Kp/128, 512): the R rows
- *   of an expert form `sections` equal sections (2 for w13: gate rows and up
- *   rows; 1 for w2), each cut into G = 2*ceil((R/sections)/192) groups of 96
- *   rows; byte 16*l + 4*c + b of image (e, s, g, t) is the scale of section
- *   row 96*g + 32*c + l, K block 4*t + b for c < 3, and 127 where that row or
- *   block does not exist -- the layout tensor memory takes the scales in.
+ *   The R rows of an expert form `sections` equal sections (2 for w13: gate
+ *   rows and up rows; 1 for w2), each cut into G = 2*ceil((R/sections)/192)
+ *   groups of 96 rows; K is cut into Kp/128 tiles of 128 elements (Kp = K
+ *   rounded up to 128).  Tile (e, s, g, t) is group g of section s of expert
+ *   e over K tile t.
+ *   packed values: tile-major (E, sections, G, Kp/128, 96, 64) bytes: byte
+ *   64*r + b of tile (e, s, g, t) holds natural bytes 64*t + b of section row
+ *   96*g + r (K elements 128*t + 2b, 2b + 1), zero nibbles past K or past the
+ *   section's rows.  One tile is 6 KB of consecutive bytes, which one TMA
+ *   copy expands into the 16-byte slots the MMA reads 4-bit operands from.
+ *   packed scales: 1 KB images (E, NT, Kp/128, 1024), one per 192-row
+ *   weight tile n and K tile t: NT = ceil((R/2)/96) tiles of 96 rows of
+ *   each section (w13: tile row r < 96 is gate row 96n + r, r >= 96 is up
+ *   row 96n + r - 96), or NT = ceil(R/192) tiles of 192 rows (w2: tile row
+ *   r is row 192n + r).  Byte 512*p + 16*l + 4*c + b of image (e, n, t) is
+ *   the scale of tile row 128*p + 32*c + l, K block 4*t + b, and 127 where
+ *   that row or block does not exist -- the layout tensor memory takes the
+ *   scales in.
  * moe_mx_packed_bytes returns the total bytes (0 on bad arguments) and the
  * two parts; K must be a multiple of 32.  moe_pack_mx_weights writes the
  * packed form on `stream` (all pointers device memory; the packed values

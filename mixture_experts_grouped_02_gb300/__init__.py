@@ -124,10 +124,12 @@ def pack_mx(w: torch.Tensor, w_scale: torch.Tensor, sections: int, stream=None,
     E, R, half_k = w.shape
     K = 2 * half_k
     vb, sb = moe_mx_packed_bytes(E, R, K, sections)
-    Kp = (K + 127) // 128 * 128
-    vals = torch.empty((E, R, Kp // 2), dtype=torch.uint8, device=w.device)
-    imgs = torch.empty(sb, dtype=torch.uint8, device=w.device)
+    # tile-major: (expert, section, 96-row group, 128-element K tile, 96, 64)
+    groups = 2 * (-(-(R // sections) // 192))
+    vals = torch.empty((E, sections, groups, (K + 127) // 128, 96, 64), dtype=torch.uint8,
+                       device=w.device)
     assert vals.numel() == vb
+    imgs = torch.empty(sb, dtype=torch.uint8, device=w.device)
     moe_pack_mx_weights(w.contiguous(), w_scale.contiguous(), E, R, K, sections, int(interleaved),
                         vals, imgs, stream)
     return vals, imgs
@@ -155,16 +157,22 @@ class Workspace:
 
 def forward(x, topk_ids, topk_weights, w13, w2, w13_scale=None, w2_scale=None, out=None,
             workspace: Workspace | None = None, weight=None, h_scale=1.0, stream=None,
-            num_experts=None, expert_base=0, **activation):
+            num_experts=None, expert_base=0, intermediate=None, **activation):
     """out = MoE expert FFN of x routed by (topk_ids, topk_weights).  With
     num_experts given, w13/w2 hold the experts [expert_base, expert_base +
     w13.shape[0]) of num_experts (an expert-parallel shard) and out is this
     shard's share of the layer output.  `activation`: make_problem's
     activation, swiglu_alpha, swiglu_limit, gate_up_interleaved, w13_bias,
     w2_bias, fused_combine.  MX weights (weight="mxfp4") come packed by
-    pack_mx."""
+    pack_mx, whose tiles do not show the intermediate size: pass it as
+    `intermediate`."""
     T, H = x.shape
-    L, I = w13.shape[0], w13.shape[1] // 2
+    if weight in ("mxfp4", MOE_E2M1_MX):
+        if intermediate is None:
+            raise ValueError("packed MX weights: pass the intermediate size")
+        L, I = w13.shape[0], intermediate
+    else:
+        L, I = w13.shape[0], w13.shape[1] // 2
     E = L if num_experts is None else num_experts
     K = topk_ids.shape[1]
     p = make_problem(T, H, I, E, K, x.dtype, weight, 0, h_scale, expert_base,

@@ -15,26 +15,35 @@
 //
 // Layout per CTA (one per SM, persistent, tiles walked in bands of N tiles
 // so that co-resident CTAs share weight tiles in L2):
-//  * tile = 128 sorted rows x 192 weight rows, as two MMAs of N = 96:
-//    gate/up: 96 gate rows and the matching 96 up rows of w13[e];
-//    down: 192 rows of w2[e];
+//  * tile = 128 sorted rows x 192 weight rows, one MMA of N = 192 per
+//    32-element K block: gate/up: 96 gate rows and the matching 96 up rows
+//    of w13[e]; down: 192 rows of w2[e];
 //  * 5 shared-memory stages of 128 K elements: A = 128 rows of e4m3 (128 B,
 //    128-byte swizzled K-major), B = 192 rows of e2m1 expanded by the TMA
 //    unit into the 16-byte slots the block-scaled MMA reads 4-bit operands
-//    from (16 values in the first 8 bytes), swizzled the same way, and two
-//    512-byte scale images (one per MMA half);
+//    from (16 values in the first 8 bytes), swizzled the same way, and the
+//    tile's 1 KB scale image (two 128-row parts of 512 bytes);
+//  * the weights are packed tile-major (moe_pack_mx_weights): the 96 rows x
+//    128 K elements of one MMA half of one stage are 6 KB of consecutive
+//    bytes, so each weight load reads whole DRAM pages instead of 64 bytes
+//    from each of 96 rows;
 //  * one producer thread fills a stage with TMA: A as a plain tile of sorted
 //    rows (gate/up: the fp8 step has already written each token's codes to
 //    the slots it occupies, so the gather happened there; down: hq; the end
 //    of K past the tensor reads as zeros), the weight tile and the two scale
 //    images (bulk copies), all completing one mbarrier;
-//  * the MMA thread copies each stage's scale images into tensor memory
-//    (tcgen05.cp, 32 x 128 bits replicated into the four lane quarters:
-//    column c of lane l holds the 4 K-block scales of row 32c + l) and
-//    issues the MMAs, choosing the scale byte of each 32-element K block by
-//    the instruction descriptor's scale ids;
+//  * the MMA thread copies each stage's scale image into tensor memory (two
+//    tcgen05.cp of 32 x 128 bits replicated into the four lane quarters, at
+//    columns 0 and 4 of the stage's block: column c of lane l holds the 4
+//    K-block scales of tile row 32c + l) and issues the MMAs, choosing the
+//    scale byte of each 32-element K block by the instruction descriptor's
+//    scale ids.  One N = 192 MMA per K block instead of two of N = 96 halves
+//    the MMA instructions and the reads of the A tile: measured, the MMA
+//    instructions of this kernel, not their arithmetic, had set its pace;
 //  * tensor memory: two 192-column fp32 accumulators, 4 columns of unit A
-//    scales, 4 columns of B scales per stage and MMA half.
+//    scales at column 384, and a 16-column block of B scales per stage from
+//    column 400 (6 columns used; every copy and MMA operand starts on a
+//    multiple of 4 columns).
 //
 // Every mbarrier wait is bounded (MxArgs::timeout_ns of wall clock); a thread
 // that gives up raises the CTA's abort flag, which every other wait polls,
@@ -62,12 +71,13 @@ struct MxCfg {
   static constexpr int kABytes = kBM * kRowBytes;     // 16 KB
   static constexpr int kBBytes = kBN * kRowBytes;     // 24 KB in shared memory
   static constexpr int kBDataBytes = kBN * kBK / 2;   // 12 KB of packed values
-  static constexpr int kSfImage = 512;                // one 96-row x 4-block scale image
-  static constexpr int kSfBytes = 2 * kSfImage;
+  static constexpr int kSfImage = 512;                // 128 tile rows x 4 K blocks of scales
+  static constexpr int kSfBytes = 2 * kSfImage;       // the tile's 192 rows (and filler)
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kAccCols = kBN;                // 192 fp32 columns
   static constexpr int kSfaCol = 2 * kAccCols;        // 384: unit A scales (4 columns)
-  static constexpr int kSfbCol0 = kSfaCol + 4;        // 388: B scales, 4 columns per stage/half
+  static constexpr int kSfbCol0 = kSfaCol + 16;       // 400: B scales, 16 columns per stage
+  static constexpr int kSfbStride = 16;
   static constexpr int kTmemCols = 512;
   static constexpr int kProducerWarps = 1;
   static constexpr int kMmaWarp = kProducerWarps;
@@ -75,14 +85,16 @@ struct MxCfg {
   // bytes the TMA unit and the bulk copies deliver per stage
   static constexpr uint32_t kTxBytes = kABytes + kBDataBytes + kSfBytes;
   static constexpr int kSmemBytes = kStages * (kStageBytes + kSfBytes) + 1024;
-  static constexpr uint32_t kIdesc = make_idesc_mx_e4m3_e2m1(kBM, kHalf);
+  static constexpr uint32_t kIdesc = make_idesc_mx_e4m3_e2m1(kBM, kBN);
 };
-static_assert(MxCfg<0>::kSfbCol0 + MxCfg<0>::kStages * 2 * 4 <= MxCfg<0>::kTmemCols,
+static_assert(MxCfg<0>::kSfbCol0 + MxCfg<0>::kStages * MxCfg<0>::kSfbStride <=
+                  MxCfg<0>::kTmemCols,
               "TMEM budget");
 
+// First TMEM column of a stage's B scales (a multiple of 16).
 template <int KIND>
-__device__ __forceinline__ uint32_t sfb_col(int stage, int half) {
-  return MxCfg<KIND>::kSfbCol0 + (stage * 2 + half) * 4;
+__device__ __forceinline__ uint32_t sfb_col(int stage) {
+  return MxCfg<KIND>::kSfbCol0 + stage * MxCfg<KIND>::kSfbStride;
 }
 
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
@@ -117,12 +129,16 @@ __device__ __forceinline__ float activate(const Epilogue& ep, float g, float u) 
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-// Scale image of (expert, section, 96-row group, K tile).
-__device__ __forceinline__ const uint8_t* sf_image(const MxArgs& a, int e, int sec, int grp,
-                                                   int kt) {
-  const long long idx =
-      ((static_cast<long long>(e) * a.sections + sec) * a.groups + grp) * a.kp_tiles + kt;
-  return a.w_scale + idx * 512;
+// Outer coordinate of the first row of the (expert, section, 96-row group,
+// K tile) block in the tile-major value map (rows of 128 K elements; the
+// host checks that it fits in 32 bits).
+__device__ __forceinline__ int value_row(const MxArgs& a, int e, int sec, int grp, int kt) {
+  return static_cast<int>(
+      (((static_cast<long long>(e) * a.sections + sec) * a.groups + grp) * a.kp_tiles + kt) * 96);
+}
+// The 1 KB scale image of weight tile nt of expert e over K tile kt.
+__device__ __forceinline__ const uint8_t* sf_image(const MxArgs& a, int e, int nt, int kt) {
+  return a.w_scale + ((static_cast<long long>(e) * a.n_tiles + nt) * a.kp_tiles + kt) * 1024;
 }
 
 template <int KIND>
@@ -206,17 +222,14 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
     const uint32_t s_dst = smemS + stage * C::kSfBytes;
     mbar_arrive_expect_tx(fb, C::kTxBytes);
     tma_load_2d(smemA + stage * C::kABytes, &tmA, fb, kt * C::kBK, r0);
-    if constexpr (KIND == kMxGateUp) {
-      const int row = e * 2 * a.I + t.nt * C::kHalf;
-      tma_load_2d(b_dst, &tmW, fb, kt * C::kBK, row);
-      tma_load_2d(b_dst + C::kHalf * C::kRowBytes, &tmW, fb, kt * C::kBK, row + a.I);
-      bulk_load(s_dst, sf_image(a, e, 0, t.nt, kt), C::kSfImage, fb);
-      bulk_load(s_dst + C::kSfImage, sf_image(a, e, 1, t.nt, kt), C::kSfImage, fb);
-    } else {
-      tma_load_2d(b_dst, &tmW, fb, kt * C::kBK, e * a.H + t.nt * C::kBN);
-      bulk_load(s_dst, sf_image(a, e, 0, 2 * t.nt, kt), C::kSfImage, fb);
-      bulk_load(s_dst + C::kSfImage, sf_image(a, e, 0, 2 * t.nt + 1, kt), C::kSfImage, fb);
-    }
+    // the two 96-row halves: gate rows and up rows of group nt (gate/up),
+    // or groups 2nt and 2nt+1 of w2 (down)
+    const int sec1 = KIND == kMxGateUp ? 1 : 0;
+    const int g0 = KIND == kMxGateUp ? t.nt : 2 * t.nt;
+    const int g1 = KIND == kMxGateUp ? t.nt : 2 * t.nt + 1;
+    tma_load_2d(b_dst, &tmW, fb, 0, value_row(a, e, 0, g0, kt));
+    tma_load_2d(b_dst + C::kHalf * C::kRowBytes, &tmW, fb, 0, value_row(a, e, sec1, g1, kt));
+    bulk_load(s_dst, sf_image(a, e, t.nt, kt), C::kSfBytes, fb);
   };
 
   if (warp < C::kProducerWarps) {
@@ -278,22 +291,17 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
           const uint32_t a_base = smemA + stage * C::kABytes;
           const uint32_t b_base = smemB + stage * C::kBBytes;
           const uint32_t s_base = smemS + stage * C::kSfBytes;
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tmem_cp_32x128b_x4(tmem_base + sfb_col<KIND>(stage, h),
-                               rows16_desc(s_base + h * C::kSfImage));
+          // tile rows 0-127 to columns 0-3, rows 128-191 (and filler) to 4-7
+          const uint32_t sfb = tmem_base + sfb_col<KIND>(stage);
+          tmem_cp_32x128b_x4(sfb, rows16_desc(s_base));
+          tmem_cp_32x128b_x4(sfb + 4, rows16_desc(s_base + C::kSfImage));
 #pragma unroll
           for (int k = 0; k < C::kBK / C::kUmmaK; ++k) {
             const uint64_t ad = sw128_kmajor_desc(a_base + k * 32);
+            const uint64_t bd = sw128_kmajor_desc(b_base + k * 32);
             const uint32_t idesc = idesc_with_sf_ids(C::kIdesc, k, k);
             const uint32_t accum = (kt > kb || k > 0) ? 1u : 0u;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint64_t bd =
-                  sw128_kmajor_desc(b_base + h * C::kHalf * C::kRowBytes + k * 32);
-              umma_mxf8f6f4(d_tmem + h * C::kHalf, ad, bd, idesc, sfa,
-                            tmem_base + sfb_col<KIND>(stage, h), accum);
-            }
+            umma_mxf8f6f4(d_tmem, ad, bd, idesc, sfa, sfb, accum);
           }
           umma_commit(smem_u32(&empty_bar[stage]));
           if (++stage == C::kStages) {
@@ -465,44 +473,68 @@ __device__ __forceinline__ long long natural_row(long long row, int R, int inter
   return e * R + (r < half ? 2 * r : 2 * (r - half) + 1);
 }
 
-// Packed values: rows of Kp = round_up(K, 128) e2m1 elements, zero beyond K;
-// interleaved gate/up rows are put in halves.
-__global__ void pack_values_kernel(const uint8_t* __restrict__ w, long long rows, int R, int K,
-                                   int Kp, int interleaved, uint8_t* __restrict__ out) {
-  const long long out_pitch = Kp / 2, in_pitch = K / 2;
-  const long long n = rows * out_pitch;
+// Packed values, tile-major: byte 64 r + b of tile (e, section, group g,
+// K tile kt) holds natural bytes 64 kt + b of section row 96 g + r (K
+// elements 128 kt + 2b and 2b + 1), zero past the section's rows or past K;
+// interleaved gate/up rows are put in halves.  One tile is 96 x 64 bytes.
+__global__ void pack_values_kernel(const uint8_t* __restrict__ w, int E, int R, int K,
+                                   int sections, int groups, int kp_tiles, int interleaved,
+                                   uint8_t* __restrict__ out) {
+  const int in_pitch = K / 2;
+  const int rows_per_sec = R / sections;
+  const long long n = static_cast<long long>(E) * sections * groups * kp_tiles * 96 * 64;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = i / out_pitch, col = i - row * out_pitch;
-    out[i] = col < in_pitch ? w[natural_row(row, R, interleaved) * in_pitch + col] : 0;
+    const int b = static_cast<int>(i & 63);
+    long long t = i >> 6;
+    const int r = static_cast<int>(t % 96);
+    t /= 96;
+    const int kt = static_cast<int>(t % kp_tiles);
+    t /= kp_tiles;
+    const int g = static_cast<int>(t % groups);
+    t /= groups;
+    const int sec = static_cast<int>(t % sections);
+    const int e = static_cast<int>(t / sections);
+    const int srow = 96 * g + r;
+    const int col = 64 * kt + b;
+    uint8_t v = 0;
+    if (srow < rows_per_sec && col < in_pitch) {
+      const long long row = natural_row(static_cast<long long>(e) * R + sec * rows_per_sec + srow,
+                                        R, interleaved);
+      v = w[row * in_pitch + col];
+    }
+    out[i] = v;
   }
 }
 
-// Scale images: byte l*16 + c*4 + b of image (e, section, group, kt) is the
-// scale of section row 96 g + 32 c + l, K block 4 kt + b (c < 3), else 127.
-// Groups come in pairs (a 192-row tile reads two), so rows past the section's
-// end exist as unit scales.
+// Scale images, one of 1 KB per (expert, weight tile, K tile): byte
+// 512 p + 16 l + 4 c + b is the scale of tile row 128 p + 32 c + l, K block
+// 4 kt + b, else 127.  Tile row r of weight tile t is, for two sections
+// (w13), row 96 t + r of the gate rows (r < 96) or row 96 t + r - 96 of the
+// up rows, and for one section (w2) row 192 t + r; rows past the section's
+// end and tile rows 192-255 are unit scales.
 __global__ void pack_scales_kernel(const uint8_t* __restrict__ sc, int E, int R, int K,
-                                   int sections, int groups, int kp_tiles, int interleaved,
+                                   int sections, int n_tiles, int kp_tiles, int interleaved,
                                    uint8_t* __restrict__ out) {
   const int nblk = K / 32;
   const int rows_per_sec = R / sections;
-  const long long n = static_cast<long long>(E) * sections * groups * kp_tiles * 512;
+  const int span = 192 / sections;  // rows of one section in a tile
+  const long long n = static_cast<long long>(E) * n_tiles * kp_tiles * 1024;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int byte = static_cast<int>(i & 511);
-    long long img = i >> 9;
+    const int byte = static_cast<int>(i & 1023);
+    long long img = i >> 10;
     const int kt = static_cast<int>(img % kp_tiles);
     img /= kp_tiles;
-    const int g = static_cast<int>(img % groups);
-    img /= groups;
-    const int sec = static_cast<int>(img % sections);
-    const int e = static_cast<int>(img / sections);
-    const int l = byte >> 4, c = (byte >> 2) & 3, b = byte & 3;
-    const int srow = 96 * g + 32 * c + l;
+    const int t = static_cast<int>(img % n_tiles);
+    const int e = static_cast<int>(img / n_tiles);
+    const int p = byte >> 9, l = (byte >> 4) & 31, c = (byte >> 2) & 3, b = byte & 3;
+    const int tr = 128 * p + 32 * c + l;
+    const int sec = tr / span;
+    const int srow = span * t + tr % span;
     const int blk = 4 * kt + b;
     uint8_t v = 127;
-    if (c < 3 && srow < rows_per_sec && blk < nblk) {
+    if (tr < 192 && srow < rows_per_sec && blk < nblk) {
       const long long row = natural_row(static_cast<long long>(e) * R + sec * rows_per_sec + srow,
                                         R, interleaved);
       v = sc[row * nblk + blk];
@@ -528,12 +560,13 @@ cudaError_t launch_pack_mx(const uint8_t* w, const uint8_t* w_scale, int E, int 
                            cudaStream_t s) {
   const int Kp = (K + 127) / 128 * 128;
   const int groups = mx_scale_groups(R / sections);
-  pack_values_kernel<<<1184, 256, 0, s>>>(w, static_cast<long long>(E) * R, R, K, Kp, interleaved,
+  pack_values_kernel<<<1184, 256, 0, s>>>(w, E, R, K, sections, groups, Kp / 128, interleaved,
                                           w_packed);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  pack_scales_kernel<<<1184, 256, 0, s>>>(w_scale, E, R, K, sections, groups, Kp / 128,
-                                          interleaved, s_packed);
+  pack_scales_kernel<<<1184, 256, 0, s>>>(w_scale, E, R, K, sections,
+                                          mx_weight_tiles(R, sections), Kp / 128, interleaved,
+                                          s_packed);
   return cudaGetLastError();
 }
 

@@ -88,6 +88,11 @@ int check_gemm_shapes(const moe_problem_t* p) {
   if (is_mx(p) && bm != kBlockM) return MOE_ERR_UNSUPPORTED;
   if (is_mx(p)) {
     if (p->H % 32 != 0 || p->I % 32 != 0) return MOE_ERR_UNSUPPORTED;
+    // TMA row coordinates of the tile-major packed values are 32-bit
+    const long long L = p->local_experts > 0 ? p->local_experts : p->E;
+    const long long tiles13 = L * 2 * mx_scale_groups(p->I) * (mx_padded_k(p->H) / 128);
+    const long long tiles2 = L * mx_scale_groups(p->H) * (mx_padded_k(p->I) / 128);
+    if (std::max(tiles13, tiles2) * 96 >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
     if (!(p->h_scale >= 0.0f) || p->h_scale > 3.0e38f) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
   }
@@ -427,6 +432,13 @@ int run_gemm2(const moe_problem_t* p, const void* h, const void* w2, const float
                                        pair_grid(max_tiles, 1, p->act), s));
 }
 
+// Rows of 128 K elements in the tile-major packed values of an (E, R, K)
+// weight tensor with `sections` sections: E * sections * groups * K tiles
+// tiles of 96 rows each.
+long long mx_value_rows(long long E, int R, int K, int sections) {
+  return E * sections * mx_scale_groups(R / sections) * (mx_padded_k(K) / 128) * 96ll;
+}
+
 MxArgs mx_args(const moe_problem_t* p) {
   MxArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -465,8 +477,8 @@ int run_gemm1_mx(const moe_problem_t* p, const void* xq, const float* x_row_scal
   CUtensorMap tmA, tmW;
   int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, p->H, a.cap, p->H, 128, 128);
   if (rc != MOE_OK) return rc;
-  rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, Hp, 2ll * p->I * local_experts(p),
-                      Hp / 2, 128, 96);
+  rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, 128,
+                      mx_value_rows(local_experts(p), 2 * p->I, p->H, 2), 64, 128, 96);
   if (rc != MOE_OK) return rc;
   a.sorted_ids = sorted_ids;
   a.block_info = block_info;
@@ -500,8 +512,8 @@ int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const u
   CUtensorMap tmA, tmW;
   int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq, p->I, a.cap, p->I, 128, 128);
   if (rc != MOE_OK) return rc;
-  rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, Ip, 1ll * p->H * local_experts(p),
-                      Ip / 2, 128, 192);
+  rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, 128,
+                      mx_value_rows(local_experts(p), p->H, p->I, 1), 64, 128, 96);
   if (rc != MOE_OK) return rc;
   a.sorted_ids = sorted_ids;
   a.block_info = block_info;
@@ -852,9 +864,9 @@ size_t moe_mx_packed_bytes(int E, int R, int K, int sections, size_t* value_byte
       R % sections != 0)
     return 0;
   const size_t Kp = static_cast<size_t>(mx_padded_k(K));
-  const size_t vb = static_cast<size_t>(E) * R * (Kp / 2);
-  const size_t sb =
-      static_cast<size_t>(E) * sections * mx_scale_groups(R / sections) * (Kp / 128) * 512;
+  const size_t vb = static_cast<size_t>(E) * sections * mx_scale_groups(R / sections) *
+                    (Kp / 128) * 96 * 64;
+  const size_t sb = static_cast<size_t>(E) * mx_weight_tiles(R, sections) * (Kp / 128) * 1024;
   if (value_bytes) *value_bytes = vb;
   if (scale_bytes) *scale_bytes = sb;
   return vb + sb;

@@ -97,3 +97,22 @@ def sample_tokens(T, n, seed=0):
     while len(picks) < min(n, T):
         picks.add(int(rng.integers(0, T)))
     return np.array(sorted(picks), np.int32)
+
+
+def block_tokens(inp: gen.MoEInputs, block_m: int, n_random: int = 8, seed: int = 0,
+                 expert_base: int = 0, local_experts: int = 0):
+    """Tokens that together touch every align block of the routing in `inp`:
+    the token of the first and of the last valid slot of each block (so
+    every active expert, every tile of the GEMMs' persistent schedule and
+    every K split is reached by a checked row), plus `n_random` sampled
+    tokens.  The blocks come from the oracle's align of the same ids."""
+    c = inp.cfg
+    ids = inp.topk_ids.cpu().numpy()
+    al = oracle.align(ids, c.E, block_m, expert_base=expert_base, local_experts=local_experts)
+    s = al["sorted_ids"]
+    picks = set(sample_tokens(c.T, n_random, seed).tolist())
+    for b in range(al["num_blocks"]):
+        first, valid = int(al["block_info"][b][2]), int(al["block_info"][b][3])
+        picks.add(int(s[first]) // c.K)
+        picks.add(int(s[first + valid - 1]) // c.K)
+    return np.array(sorted(picks), np.int32), al["num_blocks"]

@@ -9,8 +9,8 @@ import torch
 
 import oracle
 import oracle_pins as pins
-from gpu_util import (assert_close, errors, generate, np_store, oracle_forward_tokens,
-                      oracle_problem, problem_kw, sample_tokens)
+from gpu_util import (assert_close, block_tokens, errors, generate, np_store,
+                      oracle_forward_tokens, oracle_problem, problem_kw, sample_tokens)
 import mixture_experts_grouped_02_gb300 as moe
 from mixture_experts_grouped_02_gb300 import _abi
 from mixture_experts_grouped_02_gb300 import inputs as gen
@@ -425,7 +425,8 @@ def test_forward_decode_full_size(name):
     cfg = gen.config(name)
     inp = generate(cfg, seed=0, device="cuda")
     out, _ = _run_forward(inp, cfg, poison=False)
-    toks = sample_tokens(cfg.T, 8)
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype)
+    toks, _ = block_tokens(inp, moe.moe_resolve_block_m(p))
     ref = oracle_forward_tokens(inp, toks)
     assert_close(out[torch.from_numpy(toks).long().cuda()], ref, what=name)
     assert torch.isfinite(out.float()).all()
@@ -436,7 +437,10 @@ def test_forward_prefill_full_size_sampled(name):
     cfg = gen.config(name)
     inp = generate(cfg, seed=0, device="cuda")
     out, ws = _run_forward(inp, cfg, poison=False)
-    toks = sample_tokens(cfg.T, 6, seed=1)
+    # a checked token in every align block: the first and last valid slot
+    p = moe.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.dtype)
+    toks, nb = block_tokens(inp, moe.moe_resolve_block_m(p), seed=1)
+    assert nb > 0 and len(toks) >= nb // cfg.K
     ref = oracle_forward_tokens(inp, toks)
     assert_close(out[torch.from_numpy(toks).long().cuda()], ref, what=name)
     assert torch.isfinite(out.float()).all()
@@ -551,23 +555,33 @@ def test_pack_mx_layout(E, R, K, sections):
     vals, imgs = moe.pack_mx(torch.from_numpy(w).cuda(), torch.from_numpy(sc).cuda(), sections)
     torch.cuda.synchronize()
     Kp = (K + 127) // 128 * 128
-    exp_vals = np.zeros((E, R, Kp // 2), np.uint8)
-    exp_vals[..., :K // 2] = w
-    assert np.array_equal(vals.cpu().numpy(), exp_vals)
     rs = R // sections
     G, KT = 2 * (-(-rs // 192)), Kp // 128
-    exp = np.full((E, sections, G, KT, 32, 4, 4), 127, np.uint8)
-    for g in range(G):
-        for c in range(3):
-            for l in range(32):
-                row = 96 * g + 32 * c + l
-                if row >= rs:
-                    continue
-                for kt in range(KT):
-                    for b in range(4):
-                        blk = 4 * kt + b
-                        if blk < K // 32:
-                            exp[:, :, g, kt, l, c, b] = sc[:, np.arange(sections) * rs + row, blk]
+    # values, tile-major: (expert, section, group, K tile) tiles of 96 rows x 64 bytes
+    nat = np.zeros((E, sections, G * 96, Kp // 2), np.uint8)
+    nat[:, :, :rs, :K // 2] = w.reshape(E, sections, rs, K // 2)
+    exp_vals = nat.reshape(E, sections, G, 96, KT, 64).transpose(0, 1, 2, 4, 3, 5)
+    assert np.array_equal(vals.cpu().numpy(), exp_vals)
+    # scale images: one of 1 KB per (expert, 192-row weight tile, K tile);
+    # byte 512 p + 16 l + 4 c + b is tile row 128 p + 32 c + l, K block 4 t + b
+    span = 192 // sections
+    NT = -(-rs // span)
+    exp = np.full((E, NT, KT, 2, 32, 4, 4), 127, np.uint8)
+    for n in range(NT):
+        for p in range(2):
+            for c in range(4):
+                for l in range(32):
+                    tr = 128 * p + 32 * c + l
+                    if tr >= 192:
+                        continue
+                    sec, srow = tr // span, span * n + tr % span
+                    if srow >= rs:
+                        continue
+                    for t in range(KT):
+                        for b in range(4):
+                            blk = 4 * t + b
+                            if blk < K // 32:
+                                exp[:, n, t, p, l, c, b] = sc[:, sec * rs + srow, blk]
     assert np.array_equal(imgs.cpu().numpy(), exp.ravel())
 
 
@@ -672,7 +686,8 @@ def test_forward_lowp_full_size_sampled():
     inp = generate(cfg, seed=0, device="cuda")
     out = _run_forward_mx(inp, cfg)
     assert torch.isfinite(out.float()).all()
-    _check_mx(out, inp, sample_tokens(cfg.T, 8, seed=2))
+    toks, _ = block_tokens(inp, 128, seed=2)  # every align block of the 128-row tiles
+    _check_mx(out, inp, toks)
 
 
 # ------------------------------------------------------------------ expert shards
@@ -868,8 +883,8 @@ def test_forward_fused_combine_status_blocks_output():
 def test_forward_fused_combine_full_size_sampled(name):
     cfg = gen.config(name)
     inp = generate(cfg, seed=0, device="cuda")
-    out, _ = _run_forward_fused(inp, cfg)
-    toks = sample_tokens(cfg.T, 6, seed=3)
+    out, p = _run_forward_fused(inp, cfg)
+    toks, _ = block_tokens(inp, moe.moe_resolve_block_m(p), seed=3)
     assert_close(out[torch.from_numpy(toks).long().cuda()], oracle_forward_tokens(inp, toks),
                  what=name + " fused")
     assert torch.isfinite(out.float()).all()
@@ -919,7 +934,7 @@ def _run_oai_mx(d, cfg):
     w13p, s13p = moe.pack_mx(d.w13, d.w13_scale, 2, interleaved=True)
     w2p, s2p = moe.pack_mx(d.w2, d.w2_scale, 1)
     return moe.forward(d.x, d.topk_ids, d.topk_weights, w13p, w2p, w13_scale=s13p, w2_scale=s2p,
-                       weight="mxfp4", h_scale=d.h_scale, **kw)
+                       weight="mxfp4", h_scale=d.h_scale, intermediate=cfg.I, **kw)
 
 
 @pytest.mark.parametrize("case", [(96, 256, 320, 16, 4), (5, 512, 256, 8, 2)],
@@ -937,4 +952,74 @@ def test_forward_lowp_oai_full_size_sampled():
     d = gen.generate(cfg, seed=0, device="cuda")
     out = _run_oai_mx(d, cfg)
     assert torch.isfinite(out.float()).all()
-    _check_mx(out, d, sample_tokens(cfg.T, 24, seed=5), h_scale=d.h_scale)
+    toks, _ = block_tokens(d, 128, seed=5)
+    _check_mx(out, d, toks, h_scale=d.h_scale)
+
+
+# ------------------------------------------------------------------ edge cases of the method
+
+def _scale_gate_up(inp, gate_shift, up_shift):
+    """Scale w13's gate rows by 2^gate_shift and its up rows by 2^up_shift,
+    exactly: bf16 weights times a power of two, or mxfp4 e8m0 codes shifted
+    (the e2m1 values stay).  Rows follow the workload's layout (halves, or
+    GPT-OSS's alternating rows)."""
+    I = inp.cfg.I
+    gate = slice(0, 2 * I, 2) if inp.interleaved else slice(0, I)
+    up = slice(1, 2 * I, 2) if inp.interleaved else slice(I, 2 * I)
+    if inp.w13_scale is None:
+        w = inp.w13.clone()
+        w[:, gate] *= 2.0 ** gate_shift
+        w[:, up] *= 2.0 ** up_shift
+        inp.w13 = w
+    else:
+        s = inp.w13_scale.to(torch.int32)
+        s[:, gate] += gate_shift
+        s[:, up] += up_shift
+        assert int(s.min()) >= 1 and int(s.max()) <= 254
+        inp.w13_scale = s.to(torch.uint8)
+    return inp
+
+
+@pytest.mark.parametrize("kind", ["bf16", "bf16_oai", "mxfp4", "mxfp4_oai"])
+def test_forward_gate_far_past_exp_overflow(kind):
+    """Gate pre-activations of |g| up to several hundred, where e^-g
+    overflows fp32 for g < -88 (SiLU(g) -> -0) and SiLU(g) = g above it; for
+    GPT-OSS's clamped SwiGLU the gate is also far above `limit` and the
+    linear branch far outside [-limit, limit] (up rows scaled up).  The up
+    rows are scaled so that the output keeps its usual magnitude."""
+    oai = kind.endswith("_oai")
+    mx = kind.startswith("mxfp4")
+    cfg = gen.MoEConfig("edge", 96, 256, 320, 8, 2, "mxfp4" if mx else "bf16",
+                        "uniform" if mx else "normal", "swiglu_oai" if oai else "silu")
+    inp = _scale_gate_up(gen.generate(cfg, seed=61), 7, 3 if oai else -7)
+    d = inp.to("cuda")
+    # the gate reaches far past 88 in both directions
+    xg = d.x.float() @ (d.w13[0, 0:2 * cfg.I:2] if oai else d.w13[0, :cfg.I]).float().T \
+        if not mx else None
+    if xg is not None:
+        assert float(xg.max()) > 100 and float(xg.min()) < -100
+    if mx:
+        out = _run_oai_mx(d, cfg) if oai else _run_forward_mx(d, cfg)
+        _check_mx(out, inp, np.arange(cfg.T), h_scale=inp.h_scale if oai else 1.0)
+    else:
+        out = moe.forward(d.x, d.topk_ids, d.topk_weights, d.w13, d.w2, **problem_kw(d))
+        assert_close(out, oracle_forward_tokens(inp, np.arange(cfg.T)), what=kind)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_forward_non_finite_token_stays_in_its_row(fused):
+    """A NaN and an infinity in one token's x: that token's output row is
+    non-finite like the oracle's, and every other token's row matches the
+    oracle (no tile mixes tokens)."""
+    cfg = gen.MoEConfig("nonfinite", 64, 256, 320, 4, 2, "bf16", "normal")
+    inp = gen.generate(cfg, seed=62)
+    inp.x[7, 3] = float("nan")
+    inp.x[20, 0] = float("inf")
+    d = inp.to("cuda")
+    out = moe.forward(d.x, d.topk_ids, d.topk_weights, d.w13, d.w2, fused_combine=fused)
+    ref = oracle_forward_tokens(inp, np.arange(cfg.T))
+    got = out.double().cpu().numpy()
+    bad = np.zeros(cfg.T, bool)
+    bad[[7, 20]] = True
+    assert not np.isfinite(ref[bad]).any() and not np.isfinite(got[bad]).any()
+    assert_close(out[torch.from_numpy(~bad).cuda()], ref[~bad], what="finite tokens")
