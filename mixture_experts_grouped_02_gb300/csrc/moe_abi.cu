@@ -467,7 +467,10 @@ int run_gemm1_mx(const moe_problem_t* p, const void* xq, const float* x_row_scal
   a.n_tiles = (p->I + 95) / 96;
   a.k_tiles = Hp / 128;
   a.splits = 1;
-  a.band = std::min(kBand, a.n_tiles);
+  // every weight tile of a block in one band: the co-resident CTAs then
+  // share the block's A rows in L2 across all its weight tiles (measured
+  // 2 % faster than bands of 8 on the low-precision workload)
+  a.band = a.n_tiles;
   a.a = static_cast<const uint8_t*>(xq);
   a.x_row_scale = x_row_scale;
   a.w_scale = w13_scale;
@@ -502,7 +505,7 @@ int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const u
   a.n_tiles = (p->H + 191) / 192;
   a.k_tiles = Ip / 128;
   a.splits = splits;
-  a.band = std::min(kBand, a.n_tiles);
+  a.band = a.n_tiles;  // as for gate/up
   a.a = static_cast<const uint8_t*>(hq);
   a.w_scale = w2_scale;
   a.sections = 1;
