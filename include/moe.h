@@ -440,6 +440,24 @@ int moe_forward_noalloc(const moe_problem_t* p, const void* x, const int32_t* to
  * MOE_ERR_CUDA.  No counterpart on the pages.  Allocates nothing. */
 int moe_forward_noalloc_status(void* stream);
 
+/* ---- test of the kernels' failure path (not for use in a model) -----------
+ * Runs moe_gemm1_silu (gemm = 1) or moe_gemm2_weighted (gemm = 2) with the
+ * same arguments (a_rows: x rows / hq codes for gemm 1, h for gemm 2; w and
+ * w_scale: w13 or w2; k_splits: gemm 2 only), except that the kernel's
+ * producers issue no copies at all and every pipeline wait gives up after
+ * wait_limit_ns (1 ms to 2 s) of wall clock.  With nothing in flight the
+ * first wait of each CTA runs out: the kernel raises its abort flag, frees
+ * its tensor memory, writes MOE_ERR_TIMEOUT to *dev_status (which must not
+ * be NULL to observe it) and returns; `out` is not written.  No counterpart
+ * on the pages: it exists so that tests can drive the bounded waits
+ * (MOE_ERR_TIMEOUT) without ever hanging a GPU. */
+int moe_test_gemm_wait_timeout(const moe_problem_t* p, int gemm, const void* a_rows,
+                               const float* x_row_scale, const void* w, const uint8_t* w_scale,
+                               const float* topk_weights, const int32_t* sorted_ids,
+                               const int32_t* block_info, const int32_t* num_blocks, void* out,
+                               int k_splits, unsigned long long wait_limit_ns,
+                               int32_t* dev_status, void* stream);
+
 /* Launch geometry of the current device: its SM count and how many CTA pairs
  * of the bf16 gate/up kernel it holds at once (0 if unknown). */
 int moe_device_info(int* sm_count, int* pair_clusters);

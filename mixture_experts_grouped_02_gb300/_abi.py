@@ -37,7 +37,7 @@ EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_a
            "moe_forward", "moe_forward_noalloc", "moe_get_device_status", "moe_mx_packed_bytes",
            "moe_pack_mx_weights", "moe_quantize_gather_x_fp8", "moe_device_info",
            "moe_gather_rows", "moe_align_local", "moe_route_align", "moe_align_scratch_bytes",
-           "moe_combine_finish", "moe_forward_noalloc_status")
+           "moe_combine_finish", "moe_forward_noalloc_status", "moe_test_gemm_wait_timeout")
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
 MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP = 0, 1
@@ -128,6 +128,9 @@ def _declare(L):
     L.moe_forward.argtypes = [PP] + [vp] * 9 + [sz, vp]
     L.moe_forward_noalloc.restype = i32
     L.moe_forward_noalloc.argtypes = [PP] + [vp] * 9
+    L.moe_test_gemm_wait_timeout.restype = i32
+    L.moe_test_gemm_wait_timeout.argtypes = [PP, i32] + [vp] * 9 + [i32, ctypes.c_ulonglong,
+                                                                  vp, vp]
     L.moe_forward_noalloc_status.restype = i32
     L.moe_forward_noalloc_status.argtypes = [vp]
     L.moe_get_device_status.restype = i32
@@ -297,6 +300,19 @@ def moe_forward_noalloc(p: Problem, x, topk_ids, topk_weights, w13, w13_scale, w
     _check(lib().moe_forward_noalloc(ctypes.byref(p), _p(x), _p(topk_ids), _p(topk_weights),
                                      _p(w13), _p(w13_scale), _p(w2), _p(w2_scale), _p(out),
                                      _stream(stream)), "moe_forward_noalloc")
+
+
+def moe_test_gemm_wait_timeout(p: Problem, gemm, a_rows, x_row_scale, w, w_scale, topk_weights,
+                               sorted_ids, block_info, num_blocks, out, k_splits, wait_limit_ns,
+                               dev_status, stream=None):
+    """The GEMM `gemm` (1: gate/up, 2: down) launched with starved pipelines
+    and a short wait limit: the kernels' failure path, for tests."""
+    _check(lib().moe_test_gemm_wait_timeout(ctypes.byref(p), int(gemm), _p(a_rows),
+                                            _p(x_row_scale), _p(w), _p(w_scale),
+                                            _p(topk_weights), _p(sorted_ids), _p(block_info),
+                                            _p(num_blocks), _p(out), int(k_splits),
+                                            int(wait_limit_ns), _p(dev_status),
+                                            _stream(stream)), "moe_test_gemm_wait_timeout")
 
 
 def moe_forward_noalloc_status(stream=None) -> int:

@@ -47,7 +47,9 @@
 //
 // Every mbarrier wait is bounded (MxArgs::timeout_ns of wall clock); a thread
 // that gives up raises the CTA's abort flag, which every other wait polls,
-// and the kernel records MOE_ERR_TIMEOUT, drains and frees its TMEM.
+// and the kernel records MOE_ERR_TIMEOUT, drains and frees its TMEM.  A test
+// launch (MxArgs::starve) issues no copies, so that this path runs with
+// nothing in flight.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -234,10 +236,12 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
 
   if (warp < C::kProducerWarps) {
       // ------------------------------------------------------- TMA producer
+      // (a.starve, the failure-path test: no copies at all, so that the
+      // pipeline's first wait runs out with nothing in flight)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < total && ok && !a.starve; tile += gridDim.x) {
         const Tile t = decode_tile(tile, num_blocks, a);
         const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
         const int e = bi.x, r0 = bi.z;

@@ -49,7 +49,9 @@
 // Every mbarrier wait is bounded (GemmArgs::timeout_ns of wall clock): a
 // thread that gives up raises the CTA's abort flag, which every other wait
 // polls, lets issued copies and MMAs drain, and the kernel records
-// MOE_ERR_TIMEOUT in the status word and frees its TMEM.
+// MOE_ERR_TIMEOUT in the status word and frees its TMEM.  A test launch
+// (GemmArgs::starve) issues no copies, so that this path runs with nothing
+// in flight.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -226,7 +228,9 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
 
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // (a.starve, the failure-path test: no copies at all, so that the
+    // pipeline's first wait runs out with nothing in flight)
+    if (lane == 0 && !a.starve) {
       const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);
       uint32_t stage = 0, phase = 0;
       bool ok = true;

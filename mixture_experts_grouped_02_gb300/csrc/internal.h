@@ -115,6 +115,7 @@ struct GemmArgs {
   int dual_small;             // tiles of at most 32 tokens load two K steps per stage
   int32_t* status;
   unsigned long long timeout_ns;
+  int starve;                 // failure-path test: the producers issue no copies
   Epilogue ep;
   int w_rows_per_expert;      // gate/up: rows of one expert in the gate weight map
   int up_row_offset;          // gate/up: up row j = gate row j + this (in the up map)
@@ -143,6 +144,7 @@ struct MxArgs {
   float h_scale;               // hq = e4m3(a / h_scale)
   int32_t* status;
   unsigned long long timeout_ns;
+  int starve;                  // failure-path test: the producer issues no copies
   Epilogue ep;
 };
 

@@ -315,6 +315,22 @@ Epilogue epilogue_of(const moe_problem_t* p) {
   return ep;
 }
 
+// The failure-path test (moe_test_gemm_wait_timeout): while set on this
+// thread, the GEMM launches it makes starve their pipelines and give up
+// after `timeout_ns`.
+struct WaitTest {
+  unsigned long long timeout_ns;
+};
+thread_local const WaitTest* t_wait_test = nullptr;
+
+template <class Args>
+void apply_wait_test(Args& a) {
+  if (t_wait_test != nullptr) {
+    a.timeout_ns = t_wait_test->timeout_ns;
+    a.starve = 1;
+  }
+}
+
 GemmArgs base_args(const moe_problem_t* p) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -332,6 +348,7 @@ GemmArgs base_args(const moe_problem_t* p) {
   // in flight; in prefill launches (hundreds of rows per expert) the same
   // stages measured slower.
   a.dual_small = p->T <= 32 || static_cast<long long>(p->T) * p->K <= 32ll * local_experts(p);
+  apply_wait_test(a);
   return a;
 }
 
@@ -451,6 +468,7 @@ MxArgs mx_args(const moe_problem_t* p) {
   a.h_scale = h_scale_of(p);
   a.timeout_ns = kWaitTimeoutNs;
   a.ep = epilogue_of(p);
+  apply_wait_test(a);
   return a;
 }
 
@@ -782,6 +800,26 @@ int moe_gemm2_weighted(const moe_problem_t* p, const void* h, const void* w2,
   }
   return run_gemm2(p, h, w2, topk_weights, sorted_ids, block_info, num_blocks, y, k_splits,
                    dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int moe_test_gemm_wait_timeout(const moe_problem_t* p, int gemm, const void* a_rows,
+                               const float* x_row_scale, const void* w, const uint8_t* w_scale,
+                               const float* topk_weights, const int32_t* sorted_ids,
+                               const int32_t* block_info, const int32_t* num_blocks, void* out,
+                               int k_splits, unsigned long long wait_limit_ns,
+                               int32_t* dev_status, void* stream) {
+  if (gemm != 1 && gemm != 2) return MOE_ERR_INVALID_ARG;
+  if (wait_limit_ns < 1000000ull || wait_limit_ns > kWaitTimeoutNs) return MOE_ERR_INVALID_ARG;
+  const WaitTest test{wait_limit_ns};
+  t_wait_test = &test;
+  const int rc = gemm == 1 ? moe_gemm1_silu(p, a_rows, x_row_scale, w, w_scale, sorted_ids,
+                                            block_info, num_blocks, out, dev_status, stream)
+                           : moe_gemm2_weighted(p, a_rows, w, w_scale, topk_weights, sorted_ids,
+                                                block_info, num_blocks,
+                                                static_cast<float*>(out), k_splits, dev_status,
+                                                stream);
+  t_wait_test = nullptr;
+  return rc;
 }
 
 int moe_combine(const float* y, int k_splits, size_t cap, const int32_t* inv_perm, int T, int K,
