@@ -47,8 +47,10 @@ KERNEL_SOURCES = {"wpair": ("gemm_wpair.cu", "sched.cuh"), "mx": ("gemm_mx.cu", 
 # 8 TB/s, bf16 tensor 2.25 PFLOP/s, fp8 4.5 PFLOP/s
 NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}
 # the workloads timed besides the default one, each graded on its own bound
-# (ordered so that workloads sharing a weight shape run one after another)
-WORKLOADS = ([f"mixtral_decode_T{t}" for t in gen.DECODE_T] + ["dsv3_prefill"] +
+# (ordered so that workloads sharing a weight shape run one after another;
+# ":fused" runs the workload with the combine fused into the down GEMM)
+WORKLOADS = ([f"mixtral_decode_T{t}" for t in gen.DECODE_T] +
+             ["dsv3_prefill", "dsv3_prefill:fused"] +
              [f"dsv3_decode_T{t}" for t in gen.DECODE_T] + ["lowp", "lowp_oai"])
 
 
@@ -442,7 +444,9 @@ def run_workloads(moe, _abi, args, dev, main_cfg, main_inp):
     t0 = time.time()
     records = []
     weights = {}
-    for name in WORKLOADS:
+    for entry in WORKLOADS:
+        name, _, mode = entry.partition(":")
+        fused = mode == "fused"
         cfg = gen.config(name)
         key = (cfg.H, cfg.I, cfg.E, cfg.dtype)
         if key == (main_cfg.H, main_cfg.I, main_cfg.E, main_cfg.dtype):
@@ -456,7 +460,7 @@ def run_workloads(moe, _abi, args, dev, main_cfg, main_inp):
         inp = gen.MoEInputs(cfg, gen.draw_x(cfg, 0, dev), w13, w2, ids, w, s13, s2)
         if cfg.activation == "swiglu_oai":
             gen.draw_swiglu_oai(inp, seed=0, device=dev)
-        stages, p, wsp, _, _, bm, stream = build_stages(moe, _abi, cfg, inp, dev, 0)
+        stages, p, wsp, _, _, bm, stream = build_stages(moe, _abi, cfg, inp, dev, 0, fused=fused)
         ms_step, stage_ms = time_stage_loop(stages, stream, dev, 3, args.workload_steps)
         status = moe.moe_get_device_status(wsp.status, stream)
         if status != 0:
@@ -467,7 +471,8 @@ def run_workloads(moe, _abi, args, dev, main_cfg, main_inp):
         roof = graded_roofline(cfg, kern, ms_step, bytes_alg, hbm_gbs, bf16_burst)
         roof["traffic"] = profiled_traffic(name, roof["kernel"], cfg.dtype == "mxfp4")
         records.append({
-            "workload": name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.K,
+            "workload": entry, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.K,
+            "combine": "fused into GEMM2 (fp32 atomics)" if fused else "separate, deterministic",
             "dtype": cfg.dtype, "block_m": bm, "k_splits": moe.moe_gemm2_default_splits(p),
             "steps": args.workload_steps, "ms_per_step": ms_step,
             "tokens_per_s": cfg.T / (ms_step * 1e-3),

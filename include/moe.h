@@ -45,9 +45,13 @@ typedef enum {
     MOE_ERR_WORKSPACE = 3,     /* workspace too small or misaligned          */
     MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed          */
     MOE_ERR_DEVICE_BAD_ID = 5, /* (device) an expert id outside [0, E)       */
-    MOE_ERR_TIMEOUT = 6        /* (device) a pipeline wait ran out; the      */
+    MOE_ERR_TIMEOUT = 6,       /* (device) a pipeline wait ran out; the      */
                                /* kernel stopped, freed its tensor memory    */
                                /* and returned                               */
+    MOE_ERR_BOUNDS = 7         /* (device, checked build only) an index read */
+                               /* from an input or the workspace lay outside */
+                               /* the buffer it addresses; the access was    */
+                               /* skipped                                    */
 } moe_status_t;
 
 typedef enum {

@@ -23,6 +23,7 @@ MOE_ERR_WORKSPACE = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_DEVICE_BAD_ID = 5
 MOE_ERR_TIMEOUT = 6
+MOE_ERR_BOUNDS = 7
 
 MOE_F32, MOE_BF16, MOE_E4M3, MOE_E2M1_MX = 0, 1, 2, 3
 
@@ -83,6 +84,18 @@ def lib(build_if_missing: bool = True):
             _declare(L)
             _lib = L
     return _lib
+
+
+def checked_lib():
+    """libmoe_gb300_checked.so (built if absent or stale): the same entry
+    points with every kernel index range-checked (MOE_ERR_BOUNDS), loaded
+    beside the product library; call its functions directly."""
+    with _lock:
+        if not _build.up_to_date(checked=True):
+            _build.build(checked=True)
+        L = ctypes.CDLL(_build.LIB_CHECKED)
+        _declare(L)
+        return L
 
 
 def _declare(L):

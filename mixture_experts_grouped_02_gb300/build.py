@@ -3,6 +3,12 @@
 Each translation unit compiles in parallel to an object under ``_build/``;
 the objects link into ``libmoe_gb300.so`` next to this file.  Nothing is
 rebuilt when the library is newer than every source.
+
+``build(checked=True)`` builds the same sources with -DMOE_BOUNDS_CHECK into
+``libmoe_gb300_checked.so`` (objects under ``_build_checked/``): every index
+a kernel reads from its inputs is range-checked before the access it
+addresses, and a failure is reported as MOE_ERR_BOUNDS instead of touching
+memory outside its buffer.  Tests use it in place of a memory checker.
 """
 from __future__ import annotations
 
@@ -17,6 +23,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
+BUILD_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_CHECKED = os.path.join(HERE, "libmoe_gb300_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -39,24 +47,27 @@ def _deps():
         os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(checked: bool = False) -> bool:
+    lib = LIB_CHECKED if checked else LIB
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    lib, build_dir = (LIB_CHECKED, BUILD_CHECKED) if checked else (LIB, BUILD)
+    if not force and up_to_date(checked):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     nv = nvcc()
+    flags = list(extra_flags) + (["-DMOE_BOUNDS_CHECK"] if checked else [])
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
-        cmd = [nv, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
+        cmd = [nv, *ARCH, *NVCC_FLAGS, *flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -70,12 +81,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if failed:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run([nv, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True)
-    print(LIB)
+    checked = "--checked" in sys.argv
+    print(build(force="--force" in sys.argv, verbose=True, checked=checked))

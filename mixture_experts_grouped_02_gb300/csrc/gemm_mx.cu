@@ -52,6 +52,7 @@
 // nothing in flight.
 #include <cuda_bf16.h>
 
+#include "bounds.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -213,12 +214,12 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
 
-  const int num_blocks = *a.num_blocks;
+  const int num_blocks = checked_num_blocks(*a.num_blocks, a.max_blocks, a.status);
   const int total = num_blocks * a.n_tiles * a.splits;
   const uint64_t to = a.timeout_ns;
 
   // A tile, weight tile and scale images of one stage; thread-0 work
-  auto load_stage = [&](const Tile& t, int e, int r0, int kt, uint32_t stage) {
+  auto load_stage = [&](const Tile& t, int e, int r0, int kt, uint32_t stage, bool bi_ok) {
     const uint32_t fb = smem_u32(&full_bar[stage]);
     const uint32_t b_dst = smemB + stage * C::kBBytes;
     const uint32_t s_dst = smemS + stage * C::kSfBytes;
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
     const int g1 = KIND == kMxGateUp ? t.nt : 2 * t.nt + 1;
     tma_load_2d(b_dst, &tmW, fb, 0, value_row(a, e, 0, g0, kt));
     tma_load_2d(b_dst + C::kHalf * C::kRowBytes, &tmW, fb, 0, value_row(a, e, sec1, g1, kt));
-    bulk_load(s_dst, sf_image(a, e, t.nt, kt), C::kSfBytes, fb);
+    bulk_load(s_dst, bi_ok ? sf_image(a, e, t.nt, kt) : a.w_scale, C::kSfBytes, fb);
   };
 
   if (warp < C::kProducerWarps) {
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
         const Tile t = decode_tile(tile, num_blocks, a);
         const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
         const int e = bi.x, r0 = bi.z;
+        const bool bi_ok = block_in_bounds(bi, a.n_held, a.cap, C::kBM, nullptr);
         int kb, ke;
         split_range(a, t.split, kb, ke);
         for (int kt = kb; kt < ke; ++kt) {
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
             ok = false;
             break;
           }
-          if (lane == 0) load_stage(t, e, r0, kt, stage);
+          if (lane == 0) load_stage(t, e, r0, kt, stage, bi_ok);
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -334,8 +336,11 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode_tile(tile, num_blocks, a);
       const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
-      const int r0 = bi.z, valid = bi.w;
-      if (has_bias) {
+      // checked build: a block outside the held experts or the capacity
+      // loads and stores nothing (valid = 0)
+      const bool bi_ok = block_in_bounds(bi, a.n_held, a.cap, C::kBM, a.status);
+      const int r0 = bi.z, valid = bi_ok ? bi.w : 0;
+      if (has_bias && bi_ok) {
         // this tile's biases, read once; the slot of this accumulator was
         // last read two tiles ago, before the barrier of the previous tile
         for (int i = et; i < C::kBN; i += 128) {
@@ -356,7 +361,8 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
       float rs = 0.0f, wt = 0.0f;
       int tok = 0;  // down, fused combine: the accumulator row
       if (row_ok) {
-        const int i = a.sorted_ids[r0 + r];
+        int i = a.sorted_ids[r0 + r];
+        if (!in_bounds(i >= 0 && i < a.T * a.K, a.status)) i = 0;
         if constexpr (KIND == kMxGateUp) {
           rs = a.x_row_scale[i / a.K];
         } else {

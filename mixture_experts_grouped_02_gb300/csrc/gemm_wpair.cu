@@ -54,6 +54,7 @@
 // in flight.
 #include <cuda_bf16.h>
 
+#include "bounds.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = s_tmem_base;
 
-  const int num_blocks = skip ? 0 : *a.num_blocks;
+  const int num_blocks = skip ? 0 : checked_num_blocks(*a.num_blocks, a.max_blocks, a.status);
   const int total = num_blocks * a.n_tiles * a.splits;
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
@@ -413,8 +414,11 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
     for (int tile = cluster; tile < total; tile += nclusters) {
       const Tile t = decode_tile(tile, num_blocks, a);
       const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
-      const int valid = bi.w;
-      const int n = tile_n(valid);
+      // checked build: a block outside the held experts or the capacity
+      // stores and loads nothing (valid = 0)
+      const bool bi_ok = block_in_bounds(bi, a.n_held, a.cap, C::kNMax, a.status);
+      const int valid = bi_ok ? bi.w : 0;
+      const int n = tile_n(bi.w);
       // down: the routing weight and token row of slot 32j + lane, and this
       // lane's w2 bias, loaded before the accumulator is ready so that
       // their latency hides behind the MMAs (short-K tiles are otherwise
@@ -429,6 +433,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
         for (int j = 0; j < kChunks; ++j) {
           const int my = 32 * j + lane;
           sid[j] = my < valid ? a.sorted_ids[bi.z + my] : -1;
+          if (sid[j] >= 0 && !in_bounds(sid[j] < a.T * a.K, a.status)) sid[j] = -1;
         }
 #pragma unroll
         for (int j = 0; j < kChunks; ++j) {
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
         }
         // the w2 bias joins once, in the first K split
         const int c = t.nt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
-        if (a.ep.b2 != nullptr && t.split == 0 && c < a.H)
+        if (a.ep.b2 != nullptr && t.split == 0 && c < a.H && bi_ok)
           bias2 = a.ep.b2[static_cast<long long>(bi.x) * a.H + c];
       }
       int good = 1;
@@ -457,7 +462,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
         T* hcol = reinterpret_cast<T*>(a.out) + j;
         // this lane's bias: of gate j (lanes 0-63) or of up j (64-127)
         float bias = 0.0f;
-        if (a.ep.b13 != nullptr && j < a.I)
+        if (a.ep.b13 != nullptr && j < a.I && bi_ok)
           bias = a.ep.b13[gate_warp ? gate_bias_index(a.ep, a.I, bi.x, j)
                                     : up_bias_index(a.ep, a.I, bi.x, j)];
         for (int c0 = 0; c0 < n; c0 += 32) {

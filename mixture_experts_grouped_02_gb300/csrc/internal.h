@@ -116,6 +116,8 @@ struct GemmArgs {
   int32_t* status;
   unsigned long long timeout_ns;
   int starve;                 // failure-path test: the producers issue no copies
+  int n_held;                 // experts whose weights the call holds
+  int max_blocks;             // entries of block_info (cap / block_m)
   Epilogue ep;
   int w_rows_per_expert;      // gate/up: rows of one expert in the gate weight map
   int up_row_offset;          // gate/up: up row j = gate row j + this (in the up map)
@@ -145,6 +147,8 @@ struct MxArgs {
   int32_t* status;
   unsigned long long timeout_ns;
   int starve;                  // failure-path test: the producer issues no copies
+  int n_held;                  // experts whose weights the call holds
+  int max_blocks;              // entries of block_info (cap / 128)
   Epilogue ep;
 };
 
@@ -193,13 +197,16 @@ cudaError_t launch_quantize_x(const void* x, int x_dtype, int T, int H, uint8_t*
                               float* row_scale, cudaStream_t s);
 // acc_zero (nullable): rows of H fp32 of a fused combine's accumulator,
 // set to zero for every token by the same CTAs.
+// cap: rows of the sorted buffer (the checked build tests slots against it;
+// kUnknownCap when the caller did not say).
+constexpr long long kUnknownCap = 1ll << 62;
 cudaError_t launch_gather_rows(const void* x, int T, int row_bytes, int K, const int32_t* inv_perm,
                                void* xs, float* acc_zero, int H, const int32_t* status,
-                               cudaStream_t s);
+                               cudaStream_t s, long long cap = kUnknownCap);
 cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, int K,
                                      const int32_t* inv_perm, uint8_t* xq_sorted,
                                      float* row_scale, float* acc_zero, const int32_t* status,
-                                     cudaStream_t s);
+                                     cudaStream_t s, long long cap = kUnknownCap);
 cudaError_t launch_combine_finish(const float* acc, int T, int H, int out_dtype, void* out,
                                   const int32_t* status, cudaStream_t s);
 

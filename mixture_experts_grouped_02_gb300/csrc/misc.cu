@@ -4,6 +4,7 @@
 
 #include <algorithm>
 
+#include "bounds.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -50,7 +51,8 @@ __device__ __forceinline__ void add4(float4& acc, const float4 v) {
 template <typename OutT, int TPC>
 __device__ __forceinline__ void combine_group(const float* __restrict__ y,
                                               const int32_t* __restrict__ inv_perm, int T, int K,
-                                              int H, int t0, int c, OutT* __restrict__ out) {
+                                              int H, int t0, int c, OutT* __restrict__ out,
+                                              long long cap, const int32_t* status) {
   constexpr int KM = kCombineBatch / TPC;
   float4 v[TPC][KM];
   unsigned live = 0;  // bit u*KM + k: assignment k of token t0 + u has a slot here
@@ -60,7 +62,7 @@ __device__ __forceinline__ void combine_group(const float* __restrict__ y,
     for (int k = 0; k < KM; ++k)
       if (k < K && t0 + u < T) {
         const int sl = inv_perm[static_cast<long long>(t0 + u) * K + k];
-        if (sl >= 0) {
+        if (sl >= 0 && in_bounds(sl < cap, status)) {
           v[u][k] = __ldg(reinterpret_cast<const float4*>(y + static_cast<long long>(sl) * H) + c);
           live |= 1u << (u * KM + k);
         }
@@ -90,14 +92,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   for (int t0 = blockIdx.x * TPC; t0 < T; t0 += gridDim.x * TPC) {
     for (int c = blockIdx.y * 256 + threadIdx.x; c < c_end; c += blockDim.x) {
       if constexpr (TPC > 1) {
-        combine_group<OutT, TPC>(y, inv_perm, T, K, H, t0, c, out);
+        combine_group<OutT, TPC>(y, inv_perm, T, K, H, t0, c, out, cap, status);
       } else if (splits == 1 && K <= kCombineBatch) {
-        combine_group<OutT, 1>(y, inv_perm, T, K, H, t0, c, out);
+        combine_group<OutT, 1>(y, inv_perm, T, K, H, t0, c, out, cap, status);
       } else {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = 0; k < K; ++k) {
           const long long row = inv_perm[static_cast<long long>(t0) * K + k];
-          if (row < 0) continue;
+          if (row < 0 || !in_bounds(row < cap, status)) continue;
           for (int q = 0; q < splits; ++q)
             add4(acc, __ldg(reinterpret_cast<const float4*>(
                                 y + (static_cast<long long>(q) * cap + row) * H) +
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(256) quantize_x_kernel(const void* __restrict_
 __global__ void __launch_bounds__(256) quantize_gather_x_kernel(
     const void* __restrict__ x, int bf16, int T, int H, int K, const int32_t* __restrict__ inv_perm,
     uint8_t* __restrict__ xq_sorted, float* __restrict__ row_scale, float4* __restrict__ acc_zero,
-    const int32_t* status) {
+    const int32_t* status, long long cap) {
   pdl_wait();
   pdl_launch_dependents();
   if (status != nullptr && *status != 0) return;
@@ -182,7 +184,8 @@ __global__ void __launch_bounds__(256) quantize_gather_x_kernel(
       asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pk) : "f"(v1), "f"(v0));
       for (int k = 0; k < K; ++k) {
         const long long slot = inv_perm[static_cast<long long>(t) * K + k];
-        if (slot >= 0) *reinterpret_cast<uint16_t*>(xq_sorted + slot * H + c) = pk;
+        if (slot >= 0 && in_bounds(slot < cap, status))
+          *reinterpret_cast<uint16_t*>(xq_sorted + slot * H + c) = pk;
       }
     }
     __syncthreads();
@@ -199,7 +202,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ inv_perm,
                                                           uint4* __restrict__ xs,
                                                           float4* __restrict__ acc_zero,
-                                                          int acc_vec, const int32_t* status) {
+                                                          int acc_vec, const int32_t* status,
+                                                          long long cap) {
   pdl_wait();
   pdl_launch_dependents();
   if (status != nullptr && *status != 0) return;
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
       const uint4 v = __ldg(src + c);
       for (int k = 0; k < K; ++k) {
         const long long slot = inv_perm[static_cast<long long>(t) * K + k];
-        if (slot >= 0) xs[slot * row_vec + c] = v;
+        if (slot >= 0 && in_bounds(slot < cap, status)) xs[slot * row_vec + c] = v;
       }
     }
   }
@@ -237,25 +241,25 @@ __global__ void __launch_bounds__(256) combine_finish_kernel(const float4* __res
 
 cudaError_t launch_gather_rows(const void* x, int T, int row_bytes, int K, const int32_t* inv_perm,
                                void* xs, float* acc_zero, int H, const int32_t* status,
-                               cudaStream_t s) {
+                               cudaStream_t s, long long cap) {
   const int grid = T < 65535 ? T : 65535;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, s, attr);
   return cudaLaunchKernelEx(&cfg, gather_rows_kernel, static_cast<const uint4*>(x), T,
                             row_bytes / 16, K, inv_perm, static_cast<uint4*>(xs),
-                            reinterpret_cast<float4*>(acc_zero), H / 4, status);
+                            reinterpret_cast<float4*>(acc_zero), H / 4, status, cap);
 }
 
 cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, int K,
                                      const int32_t* inv_perm, uint8_t* xq_sorted,
                                      float* row_scale, float* acc_zero, const int32_t* status,
-                                     cudaStream_t s) {
+                                     cudaStream_t s, long long cap) {
   const int grid = T < 65535 ? T : 65535;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, s, attr);
   return cudaLaunchKernelEx(&cfg, quantize_gather_x_kernel, x, x_dtype == MOE_BF16 ? 1 : 0, T, H,
                             K, inv_perm, xq_sorted, row_scale, reinterpret_cast<float4*>(acc_zero),
-                            status);
+                            status, cap);
 }
 
 cudaError_t launch_combine_finish(const float* acc, int T, int H, int out_dtype, void* out,

@@ -340,6 +340,8 @@ GemmArgs base_args(const moe_problem_t* p) {
   a.E = p->E;
   a.K = p->K;
   a.cap = capacity(p->T, p->K, local_experts(p), block_m_of(p));
+  a.n_held = local_experts(p);
+  a.max_blocks = static_cast<int>(a.cap / block_m_of(p));
   a.timeout_ns = kWaitTimeoutNs;
   a.ep = epilogue_of(p);
   // decode-like launches, where most align blocks hold at most 32 tokens:
@@ -465,6 +467,8 @@ MxArgs mx_args(const moe_problem_t* p) {
   a.E = p->E;
   a.K = p->K;
   a.cap = capacity(p->T, p->K, local_experts(p), kBlockM);
+  a.n_held = local_experts(p);
+  a.max_blocks = static_cast<int>(a.cap / kBlockM);
   a.h_scale = h_scale_of(p);
   a.timeout_ns = kWaitTimeoutNs;
   a.ep = epilogue_of(p);
@@ -565,6 +569,7 @@ const char* moe_status_string(int status) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_BAD_ID: return "expert id outside [0, E)";
     case MOE_ERR_TIMEOUT: return "pipeline wait timed out";
+    case MOE_ERR_BOUNDS: return "index outside its buffer (checked build)";
     default: return "unknown status";
   }
 }
@@ -874,8 +879,7 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
     uint8_t* xq = part(MOE_WS_XQ);
     float* xs = reinterpret_cast<float*>(part(MOE_WS_X_SCALE));
     if (launch_quantize_gather_x(x, p->act, p->T, p->H, p->K, inv_perm, xq, xs, acc_zero, status,
-                                 s) !=
-        cudaSuccess)
+                                 s, capacity(p->T, p->K, local_experts(p), bm)) != cudaSuccess)
       return MOE_ERR_CUDA;
     rc = run_gemm1_mx(p, xq, xs, w13, w13_scale, sorted_ids, block_info, num_blocks, h, status, s);
     if (rc != MOE_OK) return rc;
@@ -885,7 +889,8 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
   } else {
     void* xs = part(MOE_WS_XQ);  // token rows in sorted order
     if (launch_gather_rows(x, p->T, static_cast<int>(p->H * act_bytes(p->act)), p->K, inv_perm,
-                           xs, acc_zero, p->H, status, s) != cudaSuccess)
+                           xs, acc_zero, p->H, status, s,
+                           capacity(p->T, p->K, local_experts(p), bm)) != cudaSuccess)
       return MOE_ERR_CUDA;
     rc = run_gemm1(p, xs, w13, sorted_ids, block_info, num_blocks, h, status, s);
     if (rc != MOE_OK) return rc;
