@@ -264,14 +264,13 @@ int moe_route_align(const void* logits, int logit_dtype, int T, int E, int K, in
  *   the reduction: values (E, R, K/2) bytes, e2m1 pairs, lower K index in the
  *   low nibble; scales (E, R, K/32) e8m0 bytes.
  *   The R rows of an expert form `sections` equal sections (2 for w13: gate
- *   rows and up rows; 1 for w2), each cut into G = 2*ceil((R/sections)/192)
- *   groups of 96 rows; K is cut into Kp/128 tiles of 128 elements (Kp = K
- *   rounded up to 128).  Tile (e, s, g, t) is group g of section s of expert
- *   e over K tile t.
- *   packed values: tile-major (E, sections, G, Kp/128, 96, 64) bytes: byte
- *   64*r + b of tile (e, s, g, t) holds natural bytes 64*t + b of section row
- *   96*g + r (K elements 128*t + 2b, 2b + 1), zero nibbles past K or past the
- *   section's rows.  One tile is 6 KB of consecutive bytes, which one TMA
+ *   rows and up rows; 1 for w2); K is cut into Kp/128 tiles of 128 elements
+ *   (Kp = K rounded up to 128).
+ *   packed values: tile-major (E, NT, Kp/128, 192, 64) bytes (NT as for the
+ *   scale images below): byte 64*r + b of tile (e, n, t) holds natural bytes
+ *   64*t + b (K elements 128*t + 2b, 2b + 1) of row r of weight tile n (the
+ *   same tile rows as the scale images), zero nibbles past K or past the
+ *   section's rows.  One tile is 12 KB of consecutive bytes, which one TMA
  *   copy expands into the 16-byte slots the MMA reads 4-bit operands from.
  *   packed scales: 1 KB images (E, NT, Kp/128, 1024), one per 192-row
  *   weight tile n and K tile t: NT = ceil((R/2)/96) tiles of 96 rows of

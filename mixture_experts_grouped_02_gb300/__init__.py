@@ -124,10 +124,10 @@ def pack_mx(w: torch.Tensor, w_scale: torch.Tensor, sections: int, stream=None,
     E, R, half_k = w.shape
     K = 2 * half_k
     vb, sb = moe_mx_packed_bytes(E, R, K, sections)
-    # tile-major: (expert, section, 96-row group, 128-element K tile, 96, 64)
-    groups = 2 * (-(-(R // sections) // 192))
-    vals = torch.empty((E, sections, groups, (K + 127) // 128, 96, 64), dtype=torch.uint8,
-                       device=w.device)
+    # tile-major: (expert, 192-row weight tile, 128-element K tile, 192, 64)
+    span = 192 // sections
+    tiles = -(-(R // sections) // span)
+    vals = torch.empty((E, tiles, (K + 127) // 128, 192, 64), dtype=torch.uint8, device=w.device)
     assert vals.numel() == vb
     imgs = torch.empty(sb, dtype=torch.uint8, device=w.device)
     moe_pack_mx_weights(w.contiguous(), w_scale.contiguous(), E, R, K, sections, int(interleaved),

@@ -23,10 +23,10 @@
 //    unit into the 16-byte slots the block-scaled MMA reads 4-bit operands
 //    from (16 values in the first 8 bytes), swizzled the same way, and the
 //    tile's 1 KB scale image (two 128-row parts of 512 bytes);
-//  * the weights are packed tile-major (moe_pack_mx_weights): the 96 rows x
-//    128 K elements of one MMA half of one stage are 6 KB of consecutive
-//    bytes, so each weight load reads whole DRAM pages instead of 64 bytes
-//    from each of 96 rows;
+//  * the weights are packed tile-major (moe_pack_mx_weights): the 192 weight
+//    rows x 128 K elements of one stage are 12 KB of consecutive bytes,
+//    loaded by one TMA box (a stage issues three copies: A, weights, scales;
+//    the weights as two 96-row boxes measured 3-7 % slower);
 //  * one producer thread fills a stage with TMA: A as a plain tile of sorted
 //    rows (gate/up: the fp8 step has already written each token's codes to
 //    the slots it occupies, so the gather happened there; down: hq; the end
@@ -132,12 +132,12 @@ __device__ __forceinline__ float activate(const Epilogue& ep, float g, float u) 
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-// Outer coordinate of the first row of the (expert, section, 96-row group,
-// K tile) block in the tile-major value map (rows of 128 K elements; the
+// Outer coordinate of the first of the 192 rows of weight tile nt of expert
+// e over K tile kt in the tile-major value map (rows of 128 K elements; the
 // host checks that it fits in 32 bits).
-__device__ __forceinline__ int value_row(const MxArgs& a, int e, int sec, int grp, int kt) {
+__device__ __forceinline__ int value_row(const MxArgs& a, int e, int nt, int kt) {
   return static_cast<int>(
-      (((static_cast<long long>(e) * a.sections + sec) * a.groups + grp) * a.kp_tiles + kt) * 96);
+      ((static_cast<long long>(e) * a.n_tiles + nt) * a.kp_tiles + kt) * 192);
 }
 // The 1 KB scale image of weight tile nt of expert e over K tile kt.
 __device__ __forceinline__ const uint8_t* sf_image(const MxArgs& a, int e, int nt, int kt) {
@@ -225,13 +225,9 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
     const uint32_t s_dst = smemS + stage * C::kSfBytes;
     mbar_arrive_expect_tx(fb, C::kTxBytes);
     tma_load_2d(smemA + stage * C::kABytes, &tmA, fb, kt * C::kBK, r0);
-    // the two 96-row halves: gate rows and up rows of group nt (gate/up),
-    // or groups 2nt and 2nt+1 of w2 (down)
-    const int sec1 = KIND == kMxGateUp ? 1 : 0;
-    const int g0 = KIND == kMxGateUp ? t.nt : 2 * t.nt;
-    const int g1 = KIND == kMxGateUp ? t.nt : 2 * t.nt + 1;
-    tma_load_2d(b_dst, &tmW, fb, 0, value_row(a, e, 0, g0, kt));
-    tma_load_2d(b_dst + C::kHalf * C::kRowBytes, &tmW, fb, 0, value_row(a, e, sec1, g1, kt));
+    // the tile's 192 weight rows (gate/up: 96 gate rows, then the 96 up rows
+    // of the same indices)
+    tma_load_2d(b_dst, &tmW, fb, 0, value_row(a, e, t.nt, kt));
     bulk_load(s_dst, bi_ok ? sf_image(a, e, t.nt, kt) : a.w_scale, C::kSfBytes, fb);
   };
 
@@ -483,29 +479,31 @@ __device__ __forceinline__ long long natural_row(long long row, int R, int inter
   return e * R + (r < half ? 2 * r : 2 * (r - half) + 1);
 }
 
-// Packed values, tile-major: byte 64 r + b of tile (e, section, group g,
-// K tile kt) holds natural bytes 64 kt + b of section row 96 g + r (K
-// elements 128 kt + 2b and 2b + 1), zero past the section's rows or past K;
-// interleaved gate/up rows are put in halves.  One tile is 96 x 64 bytes.
+// Packed values, tile-major: byte 64 r + b of tile (e, weight tile nt, K
+// tile kt) holds natural bytes 64 kt + b (K elements 128 kt + 2b and 2b + 1)
+// of tile row r: for two sections (w13) gate row 96 nt + r (r < 96) or up
+// row 96 nt + r - 96, for one section (w2) row 192 nt + r; zero past the
+// section's rows or past K; interleaved gate/up rows are put in halves.  One
+// tile is 192 x 64 bytes.
 __global__ void pack_values_kernel(const uint8_t* __restrict__ w, int E, int R, int K,
-                                   int sections, int groups, int kp_tiles, int interleaved,
+                                   int sections, int n_tiles, int kp_tiles, int interleaved,
                                    uint8_t* __restrict__ out) {
   const int in_pitch = K / 2;
   const int rows_per_sec = R / sections;
-  const long long n = static_cast<long long>(E) * sections * groups * kp_tiles * 96 * 64;
+  const int span = 192 / sections;  // rows of one section in a tile
+  const long long n = static_cast<long long>(E) * n_tiles * kp_tiles * 192 * 64;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int b = static_cast<int>(i & 63);
     long long t = i >> 6;
-    const int r = static_cast<int>(t % 96);
-    t /= 96;
+    const int r = static_cast<int>(t % 192);
+    t /= 192;
     const int kt = static_cast<int>(t % kp_tiles);
     t /= kp_tiles;
-    const int g = static_cast<int>(t % groups);
-    t /= groups;
-    const int sec = static_cast<int>(t % sections);
-    const int e = static_cast<int>(t / sections);
-    const int srow = 96 * g + r;
+    const int nt = static_cast<int>(t % n_tiles);
+    const int e = static_cast<int>(t / n_tiles);
+    const int sec = r / span;
+    const int srow = span * nt + r % span;
     const int col = 64 * kt + b;
     uint8_t v = 0;
     if (srow < rows_per_sec && col < in_pitch) {
@@ -569,9 +567,8 @@ cudaError_t launch_pack_mx(const uint8_t* w, const uint8_t* w_scale, int E, int 
                            int sections, int interleaved, uint8_t* w_packed, uint8_t* s_packed,
                            cudaStream_t s) {
   const int Kp = (K + 127) / 128 * 128;
-  const int groups = mx_scale_groups(R / sections);
-  pack_values_kernel<<<1184, 256, 0, s>>>(w, E, R, K, sections, groups, Kp / 128, interleaved,
-                                          w_packed);
+  pack_values_kernel<<<1184, 256, 0, s>>>(w, E, R, K, sections, mx_weight_tiles(R, sections),
+                                          Kp / 128, interleaved, w_packed);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   pack_scales_kernel<<<1184, 256, 0, s>>>(w_scale, E, R, K, sections,

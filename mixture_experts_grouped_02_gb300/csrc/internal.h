@@ -134,7 +134,6 @@ struct MxArgs {
   const float* x_row_scale;    // gate/up: per-token fp32 scale of xq
   const uint8_t* w_scale;      // scale images (E, n_tiles, kp_tiles, 1 KB)
   int sections;                // 2 for w13 (gate rows, up rows), 1 for w2
-  int groups;                  // 96-row groups per section of the packed values
   int kp_tiles;                // 128-element K tiles per padded weight row
   const int32_t* sorted_ids;
   const int32_t* block_info;
@@ -152,9 +151,9 @@ struct MxArgs {
   Epilogue ep;
 };
 
-// tmW: packed e2m1 values of w13 / w2, tile-major (E, sections, groups,
-// K tiles) x 96 rows of 128 elements (64 bytes), box 128 x 96, expanded to
-// 16-byte slots in shared memory.  tmA: the e4m3 A rows in sorted order, xq (cap x H bytes) for
+// tmW: packed e2m1 values of w13 / w2, tile-major (E, weight tiles, K tiles)
+// x 192 rows of 128 elements (64 bytes), box 128 x 192, expanded to 16-byte
+// slots in shared memory.  tmA: the e4m3 A rows in sorted order, xq (cap x H bytes) for
 // gate/up, hq (cap x I bytes) for down, box 128 x 128.
 cudaError_t launch_mx_gate_up(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW,
                               int grid, cudaStream_t s);
@@ -164,9 +163,6 @@ cudaError_t launch_pack_mx(const uint8_t* w, const uint8_t* w_scale, int E, int 
                            int sections, int interleaved, uint8_t* w_packed, uint8_t* s_packed,
                            cudaStream_t s);
 
-// 96-row groups of the packed values per section of `rows` weight rows (an
-// even number, so that a 192-row weight tile of one section is two groups).
-inline int mx_scale_groups(int rows) { return 2 * ((rows + 191) / 192); }
 // 192-row weight tiles of an expert's R rows: 96 rows of each of two
 // sections (w13: gate and up), or 192 rows of one (w2).  One scale image
 // per tile and K tile.

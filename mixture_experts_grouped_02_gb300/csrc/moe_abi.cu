@@ -90,9 +90,9 @@ int check_gemm_shapes(const moe_problem_t* p) {
     if (p->H % 32 != 0 || p->I % 32 != 0) return MOE_ERR_UNSUPPORTED;
     // TMA row coordinates of the tile-major packed values are 32-bit
     const long long L = p->local_experts > 0 ? p->local_experts : p->E;
-    const long long tiles13 = L * 2 * mx_scale_groups(p->I) * (mx_padded_k(p->H) / 128);
-    const long long tiles2 = L * mx_scale_groups(p->H) * (mx_padded_k(p->I) / 128);
-    if (std::max(tiles13, tiles2) * 96 >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+    const long long tiles13 = L * mx_weight_tiles(2 * p->I, 2) * (mx_padded_k(p->H) / 128);
+    const long long tiles2 = L * mx_weight_tiles(p->H, 1) * (mx_padded_k(p->I) / 128);
+    if (std::max(tiles13, tiles2) * 192 >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
     if (!(p->h_scale >= 0.0f) || p->h_scale > 3.0e38f) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
   }
@@ -452,10 +452,10 @@ int run_gemm2(const moe_problem_t* p, const void* h, const void* w2, const float
 }
 
 // Rows of 128 K elements in the tile-major packed values of an (E, R, K)
-// weight tensor with `sections` sections: E * sections * groups * K tiles
-// tiles of 96 rows each.
+// weight tensor with `sections` sections: E * weight tiles * K tiles tiles
+// of 192 rows each.
 long long mx_value_rows(long long E, int R, int K, int sections) {
-  return E * sections * mx_scale_groups(R / sections) * (mx_padded_k(K) / 128) * 96ll;
+  return E * mx_weight_tiles(R, sections) * (mx_padded_k(K) / 128) * 192ll;
 }
 
 MxArgs mx_args(const moe_problem_t* p) {
@@ -497,13 +497,12 @@ int run_gemm1_mx(const moe_problem_t* p, const void* xq, const float* x_row_scal
   a.x_row_scale = x_row_scale;
   a.w_scale = w13_scale;
   a.sections = 2;
-  a.groups = mx_scale_groups(p->I);
   a.kp_tiles = Hp / 128;
   CUtensorMap tmA, tmW;
   int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, p->H, a.cap, p->H, 128, 128);
   if (rc != MOE_OK) return rc;
   rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, 128,
-                      mx_value_rows(local_experts(p), 2 * p->I, p->H, 2), 64, 128, 96);
+                      mx_value_rows(local_experts(p), 2 * p->I, p->H, 2), 64, 128, 192);
   if (rc != MOE_OK) return rc;
   a.sorted_ids = sorted_ids;
   a.block_info = block_info;
@@ -531,14 +530,13 @@ int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const u
   a.a = static_cast<const uint8_t*>(hq);
   a.w_scale = w2_scale;
   a.sections = 1;
-  a.groups = mx_scale_groups(p->H);
   a.kp_tiles = Ip / 128;
   a.fused = p->fused_combine;
   CUtensorMap tmA, tmW;
   int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq, p->I, a.cap, p->I, 128, 128);
   if (rc != MOE_OK) return rc;
   rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, 128,
-                      mx_value_rows(local_experts(p), p->H, p->I, 1), 64, 128, 96);
+                      mx_value_rows(local_experts(p), p->H, p->I, 1), 64, 128, 192);
   if (rc != MOE_OK) return rc;
   a.sorted_ids = sorted_ids;
   a.block_info = block_info;
@@ -910,8 +908,7 @@ size_t moe_mx_packed_bytes(int E, int R, int K, int sections, size_t* value_byte
       R % sections != 0)
     return 0;
   const size_t Kp = static_cast<size_t>(mx_padded_k(K));
-  const size_t vb = static_cast<size_t>(E) * sections * mx_scale_groups(R / sections) *
-                    (Kp / 128) * 96 * 64;
+  const size_t vb = static_cast<size_t>(mx_value_rows(E, R, K, sections)) * 64;
   const size_t sb = static_cast<size_t>(E) * mx_weight_tiles(R, sections) * (Kp / 128) * 1024;
   if (value_bytes) *value_bytes = vb;
   if (scale_bytes) *scale_bytes = sb;

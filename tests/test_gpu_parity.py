@@ -556,11 +556,15 @@ def test_pack_mx_layout(E, R, K, sections):
     torch.cuda.synchronize()
     Kp = (K + 127) // 128 * 128
     rs = R // sections
-    G, KT = 2 * (-(-rs // 192)), Kp // 128
-    # values, tile-major: (expert, section, group, K tile) tiles of 96 rows x 64 bytes
-    nat = np.zeros((E, sections, G * 96, Kp // 2), np.uint8)
+    KT = Kp // 128
+    span = 192 // sections
+    NT = -(-rs // span)
+    # values, tile-major: (expert, weight tile, K tile) tiles of 192 rows x 64
+    # bytes; tile row r is section r // span, row span * n + r % span
+    nat = np.zeros((E, sections, NT * span, Kp // 2), np.uint8)
     nat[:, :, :rs, :K // 2] = w.reshape(E, sections, rs, K // 2)
-    exp_vals = nat.reshape(E, sections, G, 96, KT, 64).transpose(0, 1, 2, 4, 3, 5)
+    tiles = nat.reshape(E, sections, NT, span, KT, 64).transpose(0, 2, 4, 1, 3, 5)
+    exp_vals = tiles.reshape(E, NT, KT, 192, 64)
     assert np.array_equal(vals.cpu().numpy(), exp_vals)
     # scale images: one of 1 KB per (expert, 192-row weight tile, K tile);
     # byte 512 p + 16 l + 4 c + b is tile row 128 p + 32 c + l, K block 4 t + b
