@@ -15,11 +15,15 @@
 // row count rounded up to 16 (at most 256).  A block of an expert that
 // received 5 tokens runs N = 16 instead of a full 128- or 256-row tile, so
 // padding costs next to no tensor-core time and a sparsely used expert's
-// tiles are pure weight streaming.  Per CTA and 64-wide K step (one stage):
-// 128 weight rows (16 KB) and N/2 token rows, loaded as a 16-row box when
-// N <= 32 (decode) and as a 128-row box otherwise; six 32 KB stages (seven
-// for the down projection).  Decode-like launches use the DUAL
-// instantiation (WCfg), whose stages of small tiles carry two K steps.
+// tiles are pure weight streaming.  Per CTA and 64-wide K step: 128 weight
+// rows (16 KB) and N/2 token rows, loaded as a 16-row box when N <= 32
+// (decode) and as a 128-row box otherwise.  A stage carries two K steps
+// (three 64 KB stages): the pipeline pays a fixed cost per stage, besides its
+// bytes and MMAs, and two K steps per stage took the Mixtral-shaped prefill
+// GEMMs from 1.21 / 0.64 ms to 1.13 / 0.60 ms against six stages of one.
+// Decode-like launches use the DUAL instantiation (WCfg): six stages of one
+// K step for large tiles, and for tiles of at most 32 tokens two K steps of
+// weights in the W and X slots with their 16-row token boxes in a T slot.
 //  * gate/up: a CTA's 128 weight rows are 64 gate rows and the 64 up rows
 //    with the same indices j, so TMEM lanes 0-63 hold gate and 64-127 up of
 //    the same j for every token column.  The epilogue warp of lanes
@@ -87,12 +91,14 @@ struct WCfg {
   static constexpr int kRowBytes = 128;
   static constexpr int kBK = kRowBytes / sizeof(T);
   static constexpr int kUmmaK = 32 / sizeof(T);
-  // down without DUAL: no exchange buffer or T slots, room for 7
-  static constexpr int kStages = (KIND == kDown && !DUAL) ? 7 : 6;
-  static constexpr int kABytes = kWRows * kRowBytes;            // W slot: 16 KB of weights
+  static constexpr int kSub = DUAL ? 1 : 2;   // K steps per stage (large tiles)
+  static constexpr int kStages = DUAL ? 6 : 3;
+  static constexpr int kStepWBytes = kWRows * kRowBytes;        // one K step of weights: 16 KB
+  static constexpr int kABytes = kSub * kStepWBytes;            // W slot
   static constexpr int kBigRows = kNMax / 2;                    // token box rows
   static constexpr int kSmallRows = 16;
-  static constexpr int kBBytes = kBigRows * kRowBytes;          // X slot: 16 KB
+  static constexpr int kStepXBytes = kBigRows * kRowBytes;      // one K step of tokens: 16 KB
+  static constexpr int kBBytes = kSub * kStepXBytes;            // X slot
   static constexpr int kSmallBytes = kSmallRows * kRowBytes;    // one 16-row token box
   static constexpr int kTBytes = DUAL ? 2 * kSmallBytes : 0;    // T slot (DUAL)
   static constexpr int kStageBytes = kABytes + kBBytes + kTBytes;
@@ -243,9 +249,10 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
         const int half = n >> 1;
         const bool small = half <= C::kSmallRows;
         const int tok_row = bi.z + static_cast<int>(rank) * half;
-        const uint32_t tx =
-            2u * static_cast<uint32_t>(C::kABytes + (small ? C::kSmallRows : C::kBigRows) *
-                                                        C::kRowBytes);
+        // bytes of one K step of both CTAs
+        const uint32_t tx = 2u * static_cast<uint32_t>(
+                                     C::kStepWBytes +
+                                     (small ? C::kSmallRows : C::kBigRows) * C::kRowBytes);
         // this CTA's weight rows: 64 gate rows j and the 64 up rows j (at
         // the same row of the up map, shifted by up_row_offset), or 128 rows
         // of w2
@@ -286,22 +293,26 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
           }
           continue;
         }
-        for (int kt = kb; kt < ke; ++kt) {
+        for (int kt = kb; kt < ke; kt += C::kSub) {
           if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, to)) {
             ok = false;
             break;
           }
           const uint32_t fb = full0 + stage * 8u;
-          if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), tx);
-          const uint32_t sa = smemA + stage * C::kABytes;
-          if constexpr (KIND == kGateUp) {
-            tma_load_2d_pair(sa, &tmW, fb, kt * C::kBK, wrow);
-            tma_load_2d_pair(sa + C::kABytes / 2, &tmWu, fb, kt * C::kBK, wrow + a.up_row_offset);
-          } else {
-            tma_load_2d_pair(sa, &tmW, fb, kt * C::kBK, wrow);
+          const int nk = min(C::kSub, ke - kt);
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), tx * nk);
+          for (int u = 0; u < nk; ++u) {
+            const uint32_t sa = smemA + stage * C::kABytes + u * C::kStepWBytes;
+            if constexpr (KIND == kGateUp) {
+              tma_load_2d_pair(sa, &tmW, fb, (kt + u) * C::kBK, wrow);
+              tma_load_2d_pair(sa + C::kStepWBytes / 2, &tmWu, fb, (kt + u) * C::kBK,
+                               wrow + a.up_row_offset);
+            } else {
+              tma_load_2d_pair(sa, &tmW, fb, (kt + u) * C::kBK, wrow);
+            }
+            tma_load_2d_pair(smemB + stage * C::kBBytes + u * C::kStepXBytes,
+                             small ? &tmTokS : &tmTok, fb, (kt + u) * C::kBK, tok_row);
           }
-          tma_load_2d_pair(smemB + stage * C::kBBytes, small ? &tmTokS : &tmTok, fb, kt * C::kBK,
-                           tok_row);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
@@ -363,23 +374,26 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
           if (acc == 0) acc_phase ^= 1;
           continue;
         }
-        for (int kt = kb; kt < ke; ++kt) {
+        for (int kt = kb; kt < ke; kt += C::kSub) {
           if (!mbar_wait_bounded_cluster(smem_u32(&full_bar[stage]), phase, &s_abort, to)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a_base = smemA + stage * C::kABytes;
-          const uint32_t b_base = smemB + stage * C::kBBytes;
+          const int nk = min(C::kSub, ke - kt);
+          for (int u = 0; u < nk; ++u) {
+            const uint32_t a_base = smemA + stage * C::kABytes + u * C::kStepWBytes;
+            const uint32_t b_base = smemB + stage * C::kBBytes + u * C::kStepXBytes;
 #pragma unroll
-          for (int k = 0; k < C::kBK / C::kUmmaK; ++k) {
-            const uint64_t ad = sw128_kmajor_desc(a_base + k * 32);
-            const uint64_t bd = sw128_kmajor_desc(b_base + k * 32);
-            const uint32_t accum = (kt > kb || k > 0) ? 1u : 0u;
-            if constexpr (Elem<T>::kFmt == 1)
-              umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
-            else
-              umma_tf32_pair(d_tmem, ad, bd, idesc, accum);
+            for (int k = 0; k < C::kBK / C::kUmmaK; ++k) {
+              const uint64_t ad = sw128_kmajor_desc(a_base + k * 32);
+              const uint64_t bd = sw128_kmajor_desc(b_base + k * 32);
+              const uint32_t accum = (kt > kb || u > 0 || k > 0) ? 1u : 0u;
+              if constexpr (Elem<T>::kFmt == 1)
+                umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+              else
+                umma_tf32_pair(d_tmem, ad, bd, idesc, accum);
+            }
           }
           umma_commit_pair(smem_u32(&empty_bar[stage]), 0x3);
           if (++stage == C::kStages) {
