@@ -30,7 +30,8 @@
 //  * one producer thread fills a stage with TMA: A as a plain tile of sorted
 //    rows (gate/up: the fp8 step has already written each token's codes to
 //    the slots it occupies, so the gather happened there; down: hq; the end
-//    of K past the tensor reads as zeros), the weight tile and the two scale
+//    of K past the tensor reads as zeros; a block of at most 64 valid rows
+//    loads a 64-row box, half the bytes), the weight tile and the two scale
 //    images (bulk copies), all completing one mbarrier;
 //  * the MMA thread copies each stage's scale image into tensor memory (two
 //    tcgen05.cp of 32 x 128 bits replicated into the four lane quarters, at
@@ -72,6 +73,8 @@ struct MxCfg {
   static constexpr int kUmmaK = 32;                   // K per MMA (one scale block)
   static constexpr int kStages = 5;
   static constexpr int kABytes = kBM * kRowBytes;     // 16 KB
+  static constexpr int kAHalfRows = kBM / 2;          // the short A box (blocks of <= 64 rows)
+  static constexpr int kAHalfBytes = kAHalfRows * kRowBytes;
   static constexpr int kBBytes = kBN * kRowBytes;     // 24 KB in shared memory
   static constexpr int kBDataBytes = kBN * kBK / 2;   // 12 KB of packed values
   static constexpr int kSfImage = 512;                // 128 tile rows x 4 K blocks of scales
@@ -147,6 +150,7 @@ __device__ __forceinline__ const uint8_t* sf_image(const MxArgs& a, int e, int n
 template <int KIND>
 __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ MxArgs a, const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmA64,
                    const __grid_constant__ CUtensorMap tmW) {
   using C = MxCfg<KIND>;
   extern __shared__ uint8_t smem_raw[];
@@ -199,6 +203,7 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
   if (warp == C::kMmaWarp) tmem_alloc(smem_u32(&s_tmem_base), C::kTmemCols);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmA64);
     tma_prefetch_desc(&tmW);
   }
   tc_fence_before_sync();
@@ -218,13 +223,18 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
   const int total = num_blocks * a.n_tiles * a.splits;
   const uint64_t to = a.timeout_ns;
 
-  // A tile, weight tile and scale images of one stage; thread-0 work
-  auto load_stage = [&](const Tile& t, int e, int r0, int kt, uint32_t stage, bool bi_ok) {
+  // A tile, weight tile and scale images of one stage; thread-0 work.  A
+  // block of at most 64 valid rows loads only its first 64 A rows: rows 64-127
+  // of the stage keep whatever an earlier stage left there, which reaches
+  // only accumulator rows 64-127 (each accumulator row reads its own A row),
+  // and the epilogue stores none of those.
+  auto load_stage = [&](const Tile& t, int e, int r0, bool short_a, int kt, uint32_t stage,
+                        bool bi_ok) {
     const uint32_t fb = smem_u32(&full_bar[stage]);
     const uint32_t b_dst = smemB + stage * C::kBBytes;
     const uint32_t s_dst = smemS + stage * C::kSfBytes;
-    mbar_arrive_expect_tx(fb, C::kTxBytes);
-    tma_load_2d(smemA + stage * C::kABytes, &tmA, fb, kt * C::kBK, r0);
+    mbar_arrive_expect_tx(fb, C::kTxBytes - (short_a ? C::kABytes - C::kAHalfBytes : 0));
+    tma_load_2d(smemA + stage * C::kABytes, short_a ? &tmA64 : &tmA, fb, kt * C::kBK, r0);
     // the tile's 192 weight rows (gate/up: 96 gate rows, then the 96 up rows
     // of the same indices)
     tma_load_2d(b_dst, &tmW, fb, 0, value_row(a, e, t.nt, kt));
@@ -243,6 +253,7 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
         const int4 bi = reinterpret_cast<const int4*>(a.block_info)[t.mb];
         const int e = bi.x, r0 = bi.z;
         const bool bi_ok = block_in_bounds(bi, a.n_held, a.cap, C::kBM, nullptr);
+        const bool short_a = bi.w <= C::kAHalfRows;
         int kb, ke;
         split_range(a, t.split, kb, ke);
         for (int kt = kb; kt < ke; ++kt) {
@@ -254,7 +265,7 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
             ok = false;
             break;
           }
-          if (lane == 0) load_stage(t, e, r0, kt, stage, bi_ok);
+          if (lane == 0) load_stage(t, e, r0, short_a, kt, stage, bi_ok);
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -457,8 +468,8 @@ __global__ void __launch_bounds__(MxCfg<KIND>::kThreads, 1)
 }
 
 template <int KIND>
-cudaError_t launch(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW, int grid,
-                   cudaStream_t s) {
+cudaError_t launch(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmA64,
+                   const CUtensorMap& tmW, int grid, cudaStream_t s) {
   using C = MxCfg<KIND>;
   auto kern = mx_gemm_kernel<KIND>;
   cudaError_t err =
@@ -466,7 +477,7 @@ cudaError_t launch(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& t
   if (err != cudaSuccess) return err;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, attr);
-  return cudaLaunchKernelEx(&cfg, kern, a, tmA, tmW);
+  return cudaLaunchKernelEx(&cfg, kern, a, tmA, tmA64, tmW);
 }
 
 // ------------------------------------------------------------------ packing
@@ -557,14 +568,14 @@ __global__ void pack_scales_kernel(const uint8_t* __restrict__ sc, int E, int R,
 
 }  // namespace
 
-cudaError_t launch_mx_gate_up(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                              int grid, cudaStream_t s) {
-  return launch<kMxGateUp>(a, tmA, tmW, grid, s);
+cudaError_t launch_mx_gate_up(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmA64,
+                              const CUtensorMap& tmW, int grid, cudaStream_t s) {
+  return launch<kMxGateUp>(a, tmA, tmA64, tmW, grid, s);
 }
 
-cudaError_t launch_mx_down(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                           int grid, cudaStream_t s) {
-  return launch<kMxDown>(a, tmA, tmW, grid, s);
+cudaError_t launch_mx_down(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmA64,
+                           const CUtensorMap& tmW, int grid, cudaStream_t s) {
+  return launch<kMxDown>(a, tmA, tmA64, tmW, grid, s);
 }
 
 cudaError_t launch_pack_mx(const uint8_t* w, const uint8_t* w_scale, int E, int R, int K,

@@ -154,11 +154,12 @@ struct MxArgs {
 // tmW: packed e2m1 values of w13 / w2, tile-major (E, weight tiles, K tiles)
 // x 192 rows of 128 elements (64 bytes), box 128 x 192, expanded to 16-byte
 // slots in shared memory.  tmA: the e4m3 A rows in sorted order, xq (cap x H bytes) for
-// gate/up, hq (cap x I bytes) for down, box 128 x 128.
-cudaError_t launch_mx_gate_up(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                              int grid, cudaStream_t s);
-cudaError_t launch_mx_down(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                           int grid, cudaStream_t s);
+// gate/up, hq (cap x I bytes) for down, box 128 x 128; tmA64: the same rows with
+// a box of 128 x 64, loaded for blocks of at most 64 valid rows.
+cudaError_t launch_mx_gate_up(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmA64,
+                              const CUtensorMap& tmW, int grid, cudaStream_t s);
+cudaError_t launch_mx_down(const MxArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmA64,
+                           const CUtensorMap& tmW, int grid, cudaStream_t s);
 cudaError_t launch_pack_mx(const uint8_t* w, const uint8_t* w_scale, int E, int R, int K,
                            int sections, int interleaved, uint8_t* w_packed, uint8_t* s_packed,
                            cudaStream_t s);

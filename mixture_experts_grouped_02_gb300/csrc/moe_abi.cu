@@ -498,8 +498,10 @@ int run_gemm1_mx(const moe_problem_t* p, const void* xq, const float* x_row_scal
   a.w_scale = w13_scale;
   a.sections = 2;
   a.kp_tiles = Hp / 128;
-  CUtensorMap tmA, tmW;
+  CUtensorMap tmA, tmA64, tmW;
   int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, p->H, a.cap, p->H, 128, 128);
+  if (rc == MOE_OK)
+    rc = make_map_typed(&tmA64, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, p->H, a.cap, p->H, 128, 64);
   if (rc != MOE_OK) return rc;
   rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, 128,
                       mx_value_rows(local_experts(p), 2 * p->I, p->H, 2), 64, 128, 192);
@@ -511,7 +513,7 @@ int run_gemm1_mx(const moe_problem_t* p, const void* xq, const float* x_row_scal
   a.status = status;
   const long long max_tiles = (a.cap / kBlockM) * a.n_tiles;
   const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
-  return cuda_status(launch_mx_gate_up(a, tmA, tmW, grid, s));
+  return cuda_status(launch_mx_gate_up(a, tmA, tmA64, tmW, grid, s));
 }
 
 int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const uint8_t* w2_scale,
@@ -532,8 +534,10 @@ int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const u
   a.sections = 1;
   a.kp_tiles = Ip / 128;
   a.fused = p->fused_combine;
-  CUtensorMap tmA, tmW;
+  CUtensorMap tmA, tmA64, tmW;
   int rc = make_map_typed(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq, p->I, a.cap, p->I, 128, 128);
+  if (rc == MOE_OK)
+    rc = make_map_typed(&tmA64, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq, p->I, a.cap, p->I, 128, 64);
   if (rc != MOE_OK) return rc;
   rc = make_map_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, 128,
                       mx_value_rows(local_experts(p), p->H, p->I, 1), 64, 128, 192);
@@ -546,7 +550,7 @@ int run_gemm2_mx(const moe_problem_t* p, const void* hq, const void* w2, const u
   a.status = status;
   const long long max_tiles = (a.cap / kBlockM) * a.n_tiles * splits;
   const int grid = static_cast<int>(std::max(1ll, std::min<long long>(sm_count(), max_tiles)));
-  return cuda_status(launch_mx_down(a, tmA, tmW, grid, s));
+  return cuda_status(launch_mx_down(a, tmA, tmA64, tmW, grid, s));
 }
 
 }  // namespace
