@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "sched.cuh"
 
 namespace moe {
 size_t align_smem_bytes(int E);
@@ -24,7 +25,6 @@ constexpr int kAbiVersion = 3;
 constexpr size_t kWsAlign = 1024;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxDevices = 64;
-constexpr int kBand = 8;
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -388,7 +388,7 @@ int run_gemm1(const moe_problem_t* p, const void* x_sorted, const void* w13,
   a.n_tiles = (p->I + 127) / 128;
   a.k_tiles = p->H / bk;
   a.splits = 1;
-  a.band = std::min(kBand, a.n_tiles);
+  a.band = gate_up_band(a.n_tiles);
   a.sorted_ids = sorted_ids;
   a.block_info = block_info;
   a.num_blocks = num_blocks;
@@ -433,7 +433,7 @@ int run_gemm2(const moe_problem_t* p, const void* h, const void* w2, const float
   a.n_tiles = (p->H + 255) / 256;
   a.k_tiles = p->I / bk;
   a.splits = splits;
-  a.band = std::min(kBand, a.n_tiles);
+  a.band = down_band(a.n_tiles);
   a.sorted_ids = sorted_ids;
   a.block_info = block_info;
   a.num_blocks = num_blocks;
