@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
     wpair_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmTok,
                       const __grid_constant__ CUtensorMap tmTokS,
                       const __grid_constant__ CUtensorMap tmW,
-                      const __grid_constant__ CUtensorMap tmWu) {
+                      const __grid_constant__ CUtensorMap tmWu,
+                      const __grid_constant__ CUtensorMap tmX) {
   using C = WCfg<KIND, T, DUAL>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::kStages];
@@ -177,6 +178,8 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
   __shared__ int s_skip;
   __shared__ int s_skip_pair;
   __shared__ volatile int s_abort;
+  // gather mode: x rows of this CTA's tokens of the current tile (producer)
+  __shared__ int s_rows[WCfg<KIND, T, DUAL>::kNMax / 2];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -221,6 +224,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
     tma_prefetch_desc(&tmTokS);
     tma_prefetch_desc(&tmW);
     if (KIND == kGateUp) tma_prefetch_desc(&tmWu);
+    if (a.gather) tma_prefetch_desc(&tmX);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -249,10 +253,33 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
         const int half = n >> 1;
         const bool small = half <= C::kSmallRows;
         const int tok_row = bi.z + static_cast<int>(rank) * half;
+        // token rows per K step: a 16- or 128-row box of the sorted rows, or
+        // (gather mode) this CTA's `half` rows gathered from x, four at a
+        // time, by the x row of each slot (padding slots read row 0; their
+        // accumulator columns are not stored)
+        const int tok_rows = a.gather ? half : (small ? C::kSmallRows : C::kBigRows);
+        if (a.gather) {
+          for (int i = 0; i < half; ++i) {
+            const long long slot = static_cast<long long>(tok_row) + i;
+            int x_row = 0;
+            if (slot < a.cap) {
+              const int sid = a.sorted_ids[slot];
+              if (sid >= 0 && sid < a.T * a.K) x_row = sid / a.K;
+            }
+            s_rows[i] = x_row;
+          }
+        }
+        auto load_tokens = [&](uint32_t dst, uint32_t fb, int kcoord) {
+          if (a.gather) {
+            for (int g = 0; g < half; g += 4)
+              tma_gather4_pair(dst + g * C::kRowBytes, &tmX, fb, kcoord, s_rows[g], s_rows[g + 1],
+                               s_rows[g + 2], s_rows[g + 3]);
+          } else {
+            tma_load_2d_pair(dst, small ? &tmTokS : &tmTok, fb, kcoord, tok_row);
+          }
+        };
         // bytes of one K step of both CTAs
-        const uint32_t tx = 2u * static_cast<uint32_t>(
-                                     C::kStepWBytes +
-                                     (small ? C::kSmallRows : C::kBigRows) * C::kRowBytes);
+        const uint32_t tx = 2u * static_cast<uint32_t>(C::kStepWBytes + tok_rows * C::kRowBytes);
         // this CTA's weight rows: 64 gate rows j and the 64 up rows j (at
         // the same row of the up map, shifted by up_row_offset), or 128 rows
         // of w2
@@ -272,9 +299,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
             const uint32_t fb = full0 + stage * 8u;
             const int nk = min(2, ke - kt);
             const uint32_t st = smemT + stage * C::kTBytes;
-            if (leader)
-              mbar_arrive_expect_tx(smem_u32(&full_bar[stage]),
-                                    2u * static_cast<uint32_t>(nk * (C::kABytes + C::kSmallBytes)));
+            if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), tx * nk);
             for (int u = 0; u < nk; ++u) {
               const uint32_t sw = u == 0 ? smemA + stage * C::kABytes : smemB + stage * C::kBBytes;
               if constexpr (KIND == kGateUp) {
@@ -284,7 +309,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
               } else {
                 tma_load_2d_pair(sw, &tmW, fb, (kt + u) * C::kBK, wrow);
               }
-              tma_load_2d_pair(st + u * C::kSmallBytes, &tmTokS, fb, (kt + u) * C::kBK, tok_row);
+              load_tokens(st + u * C::kSmallBytes, fb, (kt + u) * C::kBK);
             }
             if (++stage == C::kStages) {
               stage = 0;
@@ -310,8 +335,7 @@ __global__ void __launch_bounds__(WCfg<KIND, T, DUAL>::kThreads, 1)
             } else {
               tma_load_2d_pair(sa, &tmW, fb, (kt + u) * C::kBK, wrow);
             }
-            tma_load_2d_pair(smemB + stage * C::kBBytes + u * C::kStepXBytes,
-                             small ? &tmTokS : &tmTok, fb, (kt + u) * C::kBK, tok_row);
+            load_tokens(smemB + stage * C::kBBytes + u * C::kStepXBytes, fb, (kt + u) * C::kBK);
           }
           if (++stage == C::kStages) {
             stage = 0;
@@ -605,7 +629,8 @@ int max_pairs() {
 
 template <int KIND, typename T, bool DUAL>
 cudaError_t launch_as(const GemmArgs& a, const CUtensorMap& tmTok, const CUtensorMap& tmTokS,
-                      const CUtensorMap& tmW, const CUtensorMap& tmWu, int grid, cudaStream_t s) {
+                      const CUtensorMap& tmW, const CUtensorMap& tmWu, const CUtensorMap& tmX,
+                      int grid, cudaStream_t s) {
   using C = WCfg<KIND, T, DUAL>;
   auto kern = wpair_gemm_kernel<KIND, T, DUAL>;
   cudaError_t err =
@@ -613,14 +638,15 @@ cudaError_t launch_as(const GemmArgs& a, const CUtensorMap& tmTok, const CUtenso
   if (err != cudaSuccess) return err;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = wpair_config<KIND, T, DUAL>(grid, s, attr);
-  return cudaLaunchKernelEx(&cfg, kern, a, tmTok, tmTokS, tmW, tmWu);
+  return cudaLaunchKernelEx(&cfg, kern, a, tmTok, tmTokS, tmW, tmWu, tmX);
 }
 
 template <int KIND, typename T>
 cudaError_t launch(const GemmArgs& a, const CUtensorMap& tmTok, const CUtensorMap& tmTokS,
-                   const CUtensorMap& tmW, const CUtensorMap& tmWu, int grid, cudaStream_t s) {
-  if (a.dual_small) return launch_as<KIND, T, true>(a, tmTok, tmTokS, tmW, tmWu, grid, s);
-  return launch_as<KIND, T, false>(a, tmTok, tmTokS, tmW, tmWu, grid, s);
+                   const CUtensorMap& tmW, const CUtensorMap& tmWu, const CUtensorMap& tmX,
+                   int grid, cudaStream_t s) {
+  if (a.dual_small) return launch_as<KIND, T, true>(a, tmTok, tmTokS, tmW, tmWu, tmX, grid, s);
+  return launch_as<KIND, T, false>(a, tmTok, tmTokS, tmW, tmWu, tmX, grid, s);
 }
 
 }  // namespace
@@ -633,17 +659,19 @@ int wpair_max_active(int kind, int dtype) {
 
 cudaError_t launch_wpair_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
                                  const CUtensorMap& tmTokS, const CUtensorMap& tmW,
-                                 const CUtensorMap& tmWu, int grid, cudaStream_t s) {
+                                 const CUtensorMap& tmWu, const CUtensorMap& tmX, int grid,
+                                 cudaStream_t s) {
   if (dtype == MOE_BF16)
-    return launch<kGateUp, __nv_bfloat16>(a, tmTok, tmTokS, tmW, tmWu, grid, s);
-  return launch<kGateUp, float>(a, tmTok, tmTokS, tmW, tmWu, grid, s);
+    return launch<kGateUp, __nv_bfloat16>(a, tmTok, tmTokS, tmW, tmWu, tmX, grid, s);
+  return launch<kGateUp, float>(a, tmTok, tmTokS, tmW, tmWu, tmX, grid, s);
 }
 
 cudaError_t launch_wpair_down(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
                               const CUtensorMap& tmTokS, const CUtensorMap& tmW, int grid,
                               cudaStream_t s) {
-  if (dtype == MOE_BF16) return launch<kDown, __nv_bfloat16>(a, tmTok, tmTokS, tmW, tmW, grid, s);
-  return launch<kDown, float>(a, tmTok, tmTokS, tmW, tmW, grid, s);
+  if (dtype == MOE_BF16)
+    return launch<kDown, __nv_bfloat16>(a, tmTok, tmTokS, tmW, tmW, tmTok, grid, s);
+  return launch<kDown, float>(a, tmTok, tmTokS, tmW, tmW, tmTok, grid, s);
 }
 
 }  // namespace moe

@@ -121,6 +121,7 @@ struct GemmArgs {
   Epilogue ep;
   int w_rows_per_expert;      // gate/up: rows of one expert in the gate weight map
   int up_row_offset;          // gate/up: up row j = gate row j + this (in the up map)
+  int gather;                 // gate/up: token rows gathered from x (T rows) by sorted_ids
 };
 
 // Arguments of one block-scaled (fp8 activations x mxfp4 weights) grouped
@@ -215,10 +216,12 @@ constexpr int kPairBlockM = 256;
 // boxes of 128 and 16 rows; tmW: w13 (box 64 rows) or w2 (box 128 rows).
 int wpair_max_active(int kind, int dtype);
 // tmWu: the map of the up rows (gate/up; the same map as tmW when w13 is in
-// halves); unused by down.
+// halves); unused by down.  tmX (gate/up with GemmArgs::gather): x as T rows
+// of H elements, box 64 x 1 (bf16; 32 x 1 fp32), read by tile::gather4.
 cudaError_t launch_wpair_gate_up(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
                                  const CUtensorMap& tmTokS, const CUtensorMap& tmW,
-                                 const CUtensorMap& tmWu, int grid, cudaStream_t s);
+                                 const CUtensorMap& tmWu, const CUtensorMap& tmX, int grid,
+                                 cudaStream_t s);
 cudaError_t launch_wpair_down(int dtype, const GemmArgs& a, const CUtensorMap& tmTok,
                               const CUtensorMap& tmTokS, const CUtensorMap& tmW, int grid,
                               cudaStream_t s);

@@ -331,6 +331,23 @@ void apply_wait_test(Args& a) {
   }
 }
 
+// Decode-like problems: at most 32 tokens in all, or at most 32 rows per
+// expert on average, so that most align blocks hold at most 32 tokens.
+bool decode_like(const moe_problem_t* p) {
+  return p->T <= 32 || static_cast<long long>(p->T) * p->K <= 32ll * local_experts(p);
+}
+
+// moe_forward gathers the token rows inside the gate/up GEMM (tile::gather4
+// by sorted_ids) instead of in a pass of its own for bf16/fp32 problems of at
+// most 8 assignments.  A gather4 copy of 4 rows costs the producer about 116
+// SM cycles (measured), so the in-GEMM gather grows with tiles x rows while
+// the separate pass costs one launch of about 6 us: Mixtral-shaped T = 1 145
+// -> 142 us per step, DeepSeek-V3-shaped T = 1 even, Mixtral T = 8 407 ->
+// 413 us, T = 128 499 -> 677 us, prefill 3.8-5.3x slower gate/up GEMMs.
+bool gather_in_gemm(const moe_problem_t* p) {
+  return !is_mx(p) && static_cast<long long>(p->T) * p->K <= 8;
+}
+
 GemmArgs base_args(const moe_problem_t* p) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -349,7 +366,7 @@ GemmArgs base_args(const moe_problem_t* p) {
   // Their tiles stream weights, and two K steps per stage double the bytes
   // in flight; in prefill launches (hundreds of rows per expert) the same
   // stages measured slower.
-  a.dual_small = p->T <= 32 || static_cast<long long>(p->T) * p->K <= 32ll * local_experts(p);
+  a.dual_small = decode_like(p);
   apply_wait_test(a);
   return a;
 }
@@ -378,11 +395,13 @@ int pair_grid(long long tiles, int kind, int dtype) {
   return static_cast<int>(2 * clusters);
 }
 
-// Gate/up: token rows of x in sorted order (moe_gather_rows) x w13, on CTA
-// pairs with 256 weight rows (128 gate + 128 up indices j) per tile.
-int run_gemm1(const moe_problem_t* p, const void* x_sorted, const void* w13,
+// Gate/up: token rows x w13, on CTA pairs with 256 weight rows (128 gate +
+// 128 up indices j) per tile.  rows: x in sorted order (cap rows, as
+// moe_gather_rows writes it), or with `gather` x itself (T rows), which the
+// producer gathers by sorted_ids.
+int run_gemm1(const moe_problem_t* p, const void* rows, const void* w13,
               const int32_t* sorted_ids, const int32_t* block_info, const int32_t* num_blocks,
-              void* h, int32_t* status, cudaStream_t s) {
+              void* h, int32_t* status, cudaStream_t s, bool gather = false) {
   GemmArgs a = base_args(p);
   const int bk = p->act == MOE_BF16 ? 64 : 32;
   a.n_tiles = (p->I + 127) / 128;
@@ -394,8 +413,9 @@ int run_gemm1(const moe_problem_t* p, const void* x_sorted, const void* w13,
   a.num_blocks = num_blocks;
   a.out = h;
   a.status = status;
-  a.x = x_sorted;
-  CUtensorMap tmTok, tmTokS, tmW, tmWu;
+  a.x = rows;
+  a.gather = gather ? 1 : 0;
+  CUtensorMap tmTok, tmTokS, tmW, tmWu, tmX;
   int rc;
   if (p->gate_up_interleaved) {
     // gate rows 2j and up rows 2j+1: two maps of I rows per expert, each row
@@ -416,11 +436,17 @@ int run_gemm1(const moe_problem_t* p, const void* x_sorted, const void* w13,
     a.w_rows_per_expert = 2 * p->I;
     a.up_row_offset = p->I;
   }
-  if (rc == MOE_OK) rc = make_map(&tmTok, p->act, x_sorted, p->H, a.cap, bk, 128);
-  if (rc == MOE_OK) rc = make_map(&tmTokS, p->act, x_sorted, p->H, a.cap, bk, 16);
+  if (gather) {
+    if (rc == MOE_OK) rc = make_map(&tmX, p->act, rows, p->H, p->T, bk, 1);
+    tmTok = tmTokS = tmX;  // not read
+  } else {
+    if (rc == MOE_OK) rc = make_map(&tmTok, p->act, rows, p->H, a.cap, bk, 128);
+    if (rc == MOE_OK) rc = make_map(&tmTokS, p->act, rows, p->H, a.cap, bk, 16);
+    tmX = tmTok;  // not read
+  }
   if (rc != MOE_OK) return rc;
   const long long max_tiles = (a.cap / block_m_of(p)) * a.n_tiles;
-  return cuda_status(launch_wpair_gate_up(p->act, a, tmTok, tmTokS, tmW, tmWu,
+  return cuda_status(launch_wpair_gate_up(p->act, a, tmTok, tmTokS, tmW, tmWu, tmX,
                                           pair_grid(max_tiles, 0, p->act), s));
 }
 
@@ -786,6 +812,25 @@ int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_sca
                    static_cast<cudaStream_t>(stream));
 }
 
+int moe_gemm1_silu_gather(const moe_problem_t* p, const void* x, const void* w13,
+                          const int32_t* sorted_ids, const int32_t* block_info,
+                          const int32_t* num_blocks, void* h, int32_t* dev_status, void* stream) {
+  int rc = check_problem(p);
+  if (rc != MOE_OK) return rc;
+  rc = check_gemm_shapes(p);
+  if (rc != MOE_OK) return rc;
+  if (is_mx(p)) return MOE_ERR_UNSUPPORTED;
+  if (p->T == 0) return MOE_OK;
+  if (!x || !w13 || !sorted_ids || !block_info || !num_blocks || !h) return MOE_ERR_INVALID_ARG;
+  return run_gemm1(p, x, w13, sorted_ids, block_info, num_blocks, h, dev_status,
+                   static_cast<cudaStream_t>(stream), true);
+}
+
+int moe_forward_gathers_in_gemm(const moe_problem_t* p) {
+  if (check_problem(p) != MOE_OK) return -1;
+  return gather_in_gemm(p) ? 1 : 0;
+}
+
 int moe_gemm2_weighted(const moe_problem_t* p, const void* h, const void* w2,
                        const uint8_t* w2_scale, const float* topk_weights,
                        const int32_t* sorted_ids, const int32_t* block_info,
@@ -889,12 +934,21 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                       splits, status, s);
     if (rc != MOE_OK) return rc;
   } else {
-    void* xs = part(MOE_WS_XQ);  // token rows in sorted order
-    if (launch_gather_rows(x, p->T, static_cast<int>(p->H * act_bytes(p->act)), p->K, inv_perm,
-                           xs, acc_zero, p->H, status, s,
-                           capacity(p->T, p->K, local_experts(p), bm)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    rc = run_gemm1(p, xs, w13, sorted_ids, block_info, num_blocks, h, status, s);
+    if (gather_in_gemm(p)) {
+      // the gate/up producer gathers x rows itself; a fused combine's
+      // accumulator is zeroed here instead of in the gather pass
+      if (acc_zero != nullptr &&
+          cudaMemsetAsync(acc_zero, 0, sizeof(float) * p->T * p->H, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      rc = run_gemm1(p, x, w13, sorted_ids, block_info, num_blocks, h, status, s, true);
+    } else {
+      void* xs = part(MOE_WS_XQ);  // token rows in sorted order
+      if (launch_gather_rows(x, p->T, static_cast<int>(p->H * act_bytes(p->act)), p->K,
+                             inv_perm, xs, acc_zero, p->H, status, s,
+                             capacity(p->T, p->K, local_experts(p), bm)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      rc = run_gemm1(p, xs, w13, sorted_ids, block_info, num_blocks, h, status, s);
+    }
     if (rc != MOE_OK) return rc;
     rc = run_gemm2(p, h, w2, topk_weights, sorted_ids, block_info, num_blocks, y, splits, status,
                    s);

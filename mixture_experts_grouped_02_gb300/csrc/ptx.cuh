@@ -176,6 +176,21 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Four rows r0..r3 of a 2-D tensor map whose box is one row high, at inner
+// coordinate c0, into four consecutive 128-byte rows of shared memory
+// (swizzled like a 4-row box), counted on an mbarrier of either CTA of a
+// CTA pair.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap* tm,
+                                                 uint32_t bar, int c0, int r0, int r1, int r2,
+                                                 int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 
 // Warp-collective: allocate `ncols` TMEM columns, base address -> *dst (smem).
