@@ -62,6 +62,7 @@ CASES = [
     ("tf32", 33, 128, 256, 8, 2, "f32", False),
     ("mx", 150, 320, 288, 3, 2, "mxfp4", False),
     ("bf16_fused", 300, 256, 320, 3, 2, "bf16", True),
+    ("bf16_gather_in_gemm", 3, 256, 320, 8, 2, "bf16", False),  # T*K <= 8: gathered in GEMM1
 ]
 
 
