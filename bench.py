@@ -366,20 +366,13 @@ def build_stages(moe, _abi, cfg, inp, dev, block_m=0, shard=None, fused=False):
     if mx:
         stages.append(("quantize_gather_x", lambda: moe.moe_quantize_gather_x_fp8(
             inp.x, _abi.MOE_BF16, cfg.T, cfg.H, cfg.K, inv, xq, xs, st, stream, acc)))
-    elif moe.moe_forward_gathers_in_gemm(p):  # the gate/up producer gathers the rows itself
-        if fused:
-            stages.append(("zero_acc", lambda: acc.zero_()))
     else:  # token rows to their sorted slots
         x_sorted = part(_abi.MOE_WS_XQ, inp.x.dtype)
         stages.append(("gather", lambda: moe.moe_gather_rows(
             inp.x, p.act, cfg.T, cfg.H, cfg.K, inv, x_sorted, st, stream, acc)))
-    if not mx and moe.moe_forward_gathers_in_gemm(p):
-        stages.append(("gemm_gate_up", lambda: moe.moe_gemm1_silu_gather(
-            p, inp.x, w13, sorted_ids, binfo, nblk, h, st, stream)))
-    else:
-        a_rows = xq if mx else x_sorted
-        stages.append(("gemm_gate_up", lambda: moe.moe_gemm1_silu(
-            p, a_rows, xs, w13, s13, sorted_ids, binfo, nblk, h, st, stream)))
+    a_rows = xq if mx else x_sorted
+    stages.append(("gemm_gate_up", lambda: moe.moe_gemm1_silu(
+        p, a_rows, xs, w13, s13, sorted_ids, binfo, nblk, h, st, stream)))
     stages.append(("gemm_down", lambda: moe.moe_gemm2_weighted(
         p, h, w2, s2, inp.topk_weights, sorted_ids, binfo, nblk, y, splits, st, stream)))
     if fused:

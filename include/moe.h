@@ -107,8 +107,7 @@ typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SWIGLU_CLAMP = 1 } moe_activation_t;
  *            scatter-add of "factor_moe_fused_gemm.cu"
  *            (weighted_scatter_add_kernel): GEMM2's epilogue adds each
  *            weighted row into an fp32 (T, H) accumulator with atomic adds
- *            (zeroed by the gather step before, or by a memset where
- *            moe_forward gathers inside the GEMM) and moe_combine_finish
+ *            (zeroed by the gather step before) and moe_combine_finish
  *            rounds it to out.  The order of the adds is not fixed, so the
  *            fp32 sums, and rarely the rounded outputs, may differ between
  *            runs in the last bits.  The workspace then holds T*H fp32
@@ -361,20 +360,14 @@ int moe_gemm1_silu(const moe_problem_t* p, const void* x, const float* x_row_sca
  * moe_gather_rows' output, bit for bit.  bf16 / fp32 activations only: MX
  * weights return MOE_ERR_UNSUPPORTED (their fp8 step,
  * moe_quantize_gather_x_fp8, already gathers).  Other arguments, shapes and
- * errors as moe_gemm1_silu. */
+ * errors as moe_gemm1_silu.  moe_forward keeps the separate gather pass:
+ * a 4-row gather copy costs the producer far more than a tile box
+ * (measured: even, within noise, at one token; slower from eight on). */
 int moe_gemm1_silu_gather(const moe_problem_t* p, const void* x, const void* w13,
                           const int32_t* sorted_ids, const int32_t* block_info,
                           const int32_t* num_blocks, void* h, int32_t* dev_status,
                           void* stream);
 
-/* 1 when moe_forward runs p's gate/up GEMM with the gather inside
- * (moe_gemm1_silu_gather, no moe_gather_rows pass; a fused combine's
- * accumulator is then zeroed by a memset), 0 when it gathers in a pass of
- * its own first; -1 for an invalid problem.  bf16/fp32 problems of at most
- * 8 assignments (T*K <= 8) gather inside: each 4-row gather copy costs the
- * GEMM's producer more than a tile box, which only a single-token step's
- * saved launch outweighs. */
-int moe_forward_gathers_in_gemm(const moe_problem_t* p);
 
 /* ---- GEMM2 x routing weight -----------------------------------------------
  * Source: "moe triton kernel use tma", the review comment on
@@ -420,10 +413,8 @@ int moe_combine_finish(const float* acc, int T, int H, int out_dtype, void* out,
 /* ---- the whole forward -----------------------------------------------------
  * Runs align -> [fp8 step with the gather (MX) | gather] -> GEMM1 -> GEMM2
  * -> combine (with p->fused_combine: GEMM2 adding into the accumulator the
- * gather step zeroed -> moe_combine_finish) on `stream`; where
- * moe_forward_gathers_in_gemm(p) is 1, GEMM1 gathers the token rows itself
- * (moe_gemm1_silu_gather) and a memset zeroes a fused combine's accumulator;
- * every intermediate lives in `workspace` (device memory of at
+ * gather step zeroed -> moe_combine_finish) on `stream`; every
+ * intermediate lives in `workspace` (device memory of at
  * least moe_workspace_size(p) bytes, 256-byte aligned, owned by the caller,
  * reusable across calls but not shared by calls in flight at once).
  *   x (T, H) act; topk_ids (T, K) int32; topk_weights (T, K) fp32;

@@ -16,7 +16,7 @@ from ._abi import (MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP, MOE_BF16, MOE_E2M1_MX, MO
                    moe_align, moe_align_capacity, moe_align_local, moe_combine, moe_forward,
                    moe_route_align, moe_align_scratch_bytes, moe_combine_finish,
                    moe_forward_noalloc, moe_forward_noalloc_status, moe_gather_rows, moe_gemm1_silu,
-                   moe_gemm1_silu_gather, moe_forward_gathers_in_gemm, moe_gemm2_default_splits,
+                   moe_gemm1_silu_gather, moe_gemm2_default_splits,
                    moe_gemm2_weighted, moe_get_device_status, moe_mx_packed_bytes,
                    moe_pack_mx_weights, moe_quantize_gather_x_fp8, moe_quantize_x_fp8,
                    moe_resolve_block_m, moe_workspace_offsets, moe_workspace_size)
@@ -28,7 +28,7 @@ __all__ = ["MOE_ACT_SILU", "MOE_ACT_SWIGLU_CLAMP", "MoEError", "Problem", "make_
            "moe_align_scratch_bytes", "moe_combine_finish",
            "moe_route_align", "route_align",
            "moe_combine", "moe_forward",
-           "moe_gemm1_silu", "moe_gemm1_silu_gather", "moe_forward_gathers_in_gemm",
+           "moe_gemm1_silu", "moe_gemm1_silu_gather",
            "moe_gemm2_default_splits", "moe_gemm2_weighted",
            "moe_get_device_status", "moe_quantize_x_fp8", "moe_resolve_block_m",
            "moe_workspace_offsets", "moe_workspace_size"]

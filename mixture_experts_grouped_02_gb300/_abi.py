@@ -39,7 +39,7 @@ EXPORTS = ("moe_status_string", "moe_abi_version", "moe_resolve_block_m", "moe_a
            "moe_pack_mx_weights", "moe_quantize_gather_x_fp8", "moe_device_info",
            "moe_gather_rows", "moe_align_local", "moe_route_align", "moe_align_scratch_bytes",
            "moe_combine_finish", "moe_forward_noalloc_status", "moe_test_gemm_wait_timeout",
-           "moe_gemm1_silu_gather", "moe_forward_gathers_in_gemm")
+           "moe_gemm1_silu_gather")
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
 MOE_ACT_SILU, MOE_ACT_SWIGLU_CLAMP = 0, 1
@@ -136,8 +136,6 @@ def _declare(L):
     L.moe_gemm1_silu.argtypes = [PP] + [vp] * 10
     L.moe_gemm1_silu_gather.restype = i32
     L.moe_gemm1_silu_gather.argtypes = [PP] + [vp] * 8
-    L.moe_forward_gathers_in_gemm.restype = i32
-    L.moe_forward_gathers_in_gemm.argtypes = [PP]
     L.moe_gemm2_weighted.restype = i32
     L.moe_gemm2_weighted.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp]
     L.moe_combine.restype = i32
@@ -292,13 +290,6 @@ def moe_gemm1_silu_gather(p: Problem, x, w13, sorted_ids, block_info, num_blocks
     _check(lib().moe_gemm1_silu_gather(ctypes.byref(p), _p(x), _p(w13), _p(sorted_ids),
                                        _p(block_info), _p(num_blocks), _p(h), _p(dev_status),
                                        _stream(stream)), "moe_gemm1_silu_gather")
-
-
-def moe_forward_gathers_in_gemm(p: Problem) -> bool:
-    r = lib().moe_forward_gathers_in_gemm(ctypes.byref(p))
-    if r < 0:
-        raise MoEError(MOE_ERR_INVALID_ARG, "moe_forward_gathers_in_gemm: invalid problem")
-    return r == 1
 
 
 def moe_gemm2_weighted(p: Problem, h, w2, w2_scale, topk_weights, sorted_ids, block_info,

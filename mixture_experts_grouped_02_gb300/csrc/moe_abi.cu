@@ -337,17 +337,6 @@ bool decode_like(const moe_problem_t* p) {
   return p->T <= 32 || static_cast<long long>(p->T) * p->K <= 32ll * local_experts(p);
 }
 
-// moe_forward gathers the token rows inside the gate/up GEMM (tile::gather4
-// by sorted_ids) instead of in a pass of its own for bf16/fp32 problems of at
-// most 8 assignments.  A gather4 copy of 4 rows costs the producer about 116
-// SM cycles (measured), so the in-GEMM gather grows with tiles x rows while
-// the separate pass costs one launch of about 6 us: Mixtral-shaped T = 1 145
-// -> 142 us per step, DeepSeek-V3-shaped T = 1 even, Mixtral T = 8 407 ->
-// 413 us, T = 128 499 -> 677 us, prefill 3.8-5.3x slower gate/up GEMMs.
-bool gather_in_gemm(const moe_problem_t* p) {
-  return !is_mx(p) && static_cast<long long>(p->T) * p->K <= 8;
-}
-
 GemmArgs base_args(const moe_problem_t* p) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -826,11 +815,6 @@ int moe_gemm1_silu_gather(const moe_problem_t* p, const void* x, const void* w13
                    static_cast<cudaStream_t>(stream), true);
 }
 
-int moe_forward_gathers_in_gemm(const moe_problem_t* p) {
-  if (check_problem(p) != MOE_OK) return -1;
-  return gather_in_gemm(p) ? 1 : 0;
-}
-
 int moe_gemm2_weighted(const moe_problem_t* p, const void* h, const void* w2,
                        const uint8_t* w2_scale, const float* topk_weights,
                        const int32_t* sorted_ids, const int32_t* block_info,
@@ -934,21 +918,12 @@ int moe_forward(const moe_problem_t* p, const void* x, const int32_t* topk_ids,
                       splits, status, s);
     if (rc != MOE_OK) return rc;
   } else {
-    if (gather_in_gemm(p)) {
-      // the gate/up producer gathers x rows itself; a fused combine's
-      // accumulator is zeroed here instead of in the gather pass
-      if (acc_zero != nullptr &&
-          cudaMemsetAsync(acc_zero, 0, sizeof(float) * p->T * p->H, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      rc = run_gemm1(p, x, w13, sorted_ids, block_info, num_blocks, h, status, s, true);
-    } else {
-      void* xs = part(MOE_WS_XQ);  // token rows in sorted order
-      if (launch_gather_rows(x, p->T, static_cast<int>(p->H * act_bytes(p->act)), p->K,
-                             inv_perm, xs, acc_zero, p->H, status, s,
-                             capacity(p->T, p->K, local_experts(p), bm)) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      rc = run_gemm1(p, xs, w13, sorted_ids, block_info, num_blocks, h, status, s);
-    }
+    void* xs = part(MOE_WS_XQ);  // token rows in sorted order
+    if (launch_gather_rows(x, p->T, static_cast<int>(p->H * act_bytes(p->act)), p->K, inv_perm,
+                           xs, acc_zero, p->H, status, s,
+                           capacity(p->T, p->K, local_experts(p), bm)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    rc = run_gemm1(p, xs, w13, sorted_ids, block_info, num_blocks, h, status, s);
     if (rc != MOE_OK) return rc;
     rc = run_gemm2(p, h, w2, topk_weights, sorted_ids, block_info, num_blocks, y, splits, status,
                    s);

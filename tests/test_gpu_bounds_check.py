@@ -62,7 +62,6 @@ CASES = [
     ("tf32", 33, 128, 256, 8, 2, "f32", False),
     ("mx", 150, 320, 288, 3, 2, "mxfp4", False),
     ("bf16_fused", 300, 256, 320, 3, 2, "bf16", True),
-    ("bf16_gather_in_gemm", 3, 256, 320, 8, 2, "bf16", False),  # T*K <= 8: gathered in GEMM1
 ]
 
 
@@ -82,6 +81,31 @@ def test_checked_build_matches_product_build(checked, case):
         assert_close(got, ref.double().cpu().numpy(), max_abs=2e-2, rel_l2=4e-3, what=name)
     else:
         assert torch.equal(got, ref), name
+
+
+@pytest.mark.parametrize("T,E,dt", [(3, 8, "bf16"), (300, 3, "bf16"), (40, 8, "f32")])
+def test_checked_build_gather_in_gemm_matches_product_build(checked, T, E, dt):
+    """The gate/up GEMM that gathers its token rows by index (its producer
+    reads sorted_ids, checked against the capacity and T*K in this build):
+    the same h from both builds."""
+    H, I, K = 256, 320, 2
+    cfg = gen.MoEConfig("gather", T, H, I, E, K, dt, "normal")
+    d = gen.generate(cfg, seed=83).to("cuda")
+    p = moe.make_problem(T, H, I, E, K, dt)
+    bm = moe.moe_resolve_block_m(p)
+    al = moe.align(d.topk_ids, E, bm)
+    cap = moe.moe_align_capacity(T, K, E, bm)
+    outs = []
+    for L in (checked, _abi.lib()):
+        h = torch.full((cap, I), float("nan"), dtype=d.x.dtype, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        rc = L.moe_gemm1_silu_gather(ctypes.byref(p), _ptr(d.x), _ptr(d.w13),
+                                     _ptr(al["sorted_ids"]), _ptr(al["block_info"]),
+                                     _ptr(al["num_blocks"]), _ptr(h), _ptr(st), _stream())
+        assert rc == 0
+        assert _status(L, st) == 0
+        outs.append(h.view(torch.int16 if dt == "bf16" else torch.int32))
+    assert torch.equal(outs[0], outs[1])
 
 
 def _stage_problem(mx=False):

@@ -276,41 +276,6 @@ def test_gemm1_silu_gather_matches_gather_pass(case, bm, interleaved):
     assert torch.equal(_raw(h), _raw(h_ref))
 
 
-def test_forward_gathers_in_gemm_policy():
-    """moe_forward gathers inside the gate/up GEMM exactly for bf16/fp32
-    problems of at most 8 assignments."""
-    assert moe.moe_forward_gathers_in_gemm(moe.make_problem(1, 4096, 14336, 8, 2, "bf16"))
-    assert moe.moe_forward_gathers_in_gemm(moe.make_problem(4, 128, 256, 8, 2, "f32"))
-    assert moe.moe_forward_gathers_in_gemm(moe.make_problem(1, 7168, 2048, 256, 8, "bf16"))
-    assert not moe.moe_forward_gathers_in_gemm(moe.make_problem(8, 4096, 14336, 8, 2, "bf16"))
-    assert not moe.moe_forward_gathers_in_gemm(moe.make_problem(4096, 4096, 14336, 8, 2, "bf16"))
-    assert not moe.moe_forward_gathers_in_gemm(
-        moe.make_problem(1, 2880, 2880, 128, 4, "bf16", "mxfp4"))
-
-
-@pytest.mark.parametrize("fused", [False, True])
-@pytest.mark.parametrize("case", [(1, 256, 320, 8, 2, "bf16"), (3, 128, 256, 5, 2, "f32"),
-                                  (1, 256, 1536, 8, 8, "bf16")],
-                         ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s" % c)
-def test_forward_with_gather_in_gemm(case, fused):
-    """moe_forward on problems it gathers inside the gate/up GEMM for (the
-    fused combine's accumulator zeroed by a memset on a poisoned workspace):
-    every token row against the oracle."""
-    T, H, I, E, K, dt = case
-    cfg = gen.MoEConfig("gather_in_gemm", T, H, I, E, K, dt, "normal")
-    inp = gen.generate(cfg, seed=25)
-    d = inp.to("cuda")
-    p = moe.make_problem(T, H, I, E, K, dt, fused_combine=fused)
-    assert moe.moe_forward_gathers_in_gemm(p)
-    ws = moe.Workspace(p)
-    ws.buffer.fill_(0xFF)
-    out = torch.full((T, H), float("nan"), dtype=d.x.dtype, device="cuda")
-    moe.moe_forward(p, d.x, d.topk_ids, d.topk_weights, d.w13, None, d.w2, None, out, ws.buffer,
-                    ws.nbytes)
-    assert moe.moe_get_device_status(ws.status) == 0
-    assert_close(out, oracle_forward_tokens(inp, np.arange(T)), what=cfg.name)
-
-
 @pytest.mark.parametrize("bm", [32, 128, 256])
 @pytest.mark.parametrize("splits", [1, 2, 3])
 @pytest.mark.parametrize("case", STAGE_CASES, ids=lambda c: "T%d_H%d_I%d_E%d_K%d_%s" % c)
