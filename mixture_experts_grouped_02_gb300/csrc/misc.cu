@@ -192,6 +192,92 @@ __global__ void __launch_bounds__(256) quantize_gather_x_kernel(
   }
 }
 
+// 16 consecutive activations of a row as fp32 (two or four 16-byte loads).
+template <bool BF16>
+__device__ __forceinline__ void load16(const void* x, long long idx, float (&v)[16]) {
+  if constexpr (BF16) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + idx);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 q = p[h];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * h + 2 * i] = __uint_as_float(w[i] << 16);
+        v[8 * h + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + idx);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float4 q = p[h];
+      v[4 * h] = q.x;
+      v[4 * h + 1] = q.y;
+      v[4 * h + 2] = q.z;
+      v[4 * h + 3] = q.w;
+    }
+  }
+}
+
+// quantize_gather_x_kernel for rows of a multiple of 16 elements with x and
+// xq_sorted 16-byte aligned: a thread takes runs of 16 elements (16-byte
+// loads) and writes their 16 codes with one 16-byte store per slot of the
+// token.  Every code is computed exactly as in the general kernel.
+template <bool BF16>
+__global__ void __launch_bounds__(256) quantize_gather_x16_kernel(
+    const void* __restrict__ x, int T, int H, int K, const int32_t* __restrict__ inv_perm,
+    uint8_t* __restrict__ xq_sorted, float* __restrict__ row_scale, float4* __restrict__ acc_zero,
+    const int32_t* status, long long cap) {
+  pdl_wait();
+  pdl_launch_dependents();
+  if (status != nullptr && *status != 0) return;
+  __shared__ float s_red[8];
+  const int runs = H >> 4;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const long long base = static_cast<long long>(t) * H;
+    if (acc_zero != nullptr)  // the fused combine's accumulator row of this token
+      for (int c = threadIdx.x; c < (H >> 2); c += blockDim.x)
+        acc_zero[(base >> 2) + c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float amax = 0.0f;
+    for (int r = threadIdx.x; r < runs; r += blockDim.x) {
+      float v[16];
+      load16<BF16>(x, base + 16 * r, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = s_red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, s_red[w]);
+    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    if (threadIdx.x == 0) row_scale[t] = s;
+    for (int r = threadIdx.x; r < runs; r += blockDim.x) {
+      float v[16];
+      load16<BF16>(x, base + 16 * r, v);
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint16_t h;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+            : "=h"(h)
+            : "f"(__fdiv_rn(v[2 * i + 1], s)), "f"(__fdiv_rn(v[2 * i], s)));
+        pk[i] = h;
+      }
+      const uint4 q = make_uint4(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16),
+                                 pk[4] | (pk[5] << 16), pk[6] | (pk[7] << 16));
+      for (int k = 0; k < K; ++k) {
+        const long long slot = inv_perm[static_cast<long long>(t) * K + k];
+        if (slot >= 0 && in_bounds(slot < cap, status))
+          *reinterpret_cast<uint4*>(xq_sorted + slot * H + 16 * r) = q;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // Token rows to sorted slots: xs[inv_perm[t*K + k], :] = x[t, :] for every
 // choice k of token t (rows of padding slots untouched).  The gather of the
 // gate/up GEMM done as its own pass, for the CTA-pair GEMMs whose A operand
@@ -257,9 +343,17 @@ cudaError_t launch_quantize_gather_x(const void* x, int x_dtype, int T, int H, i
   const int grid = T < 65535 ? T : 65535;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, s, attr);
+  float4* acc4 = reinterpret_cast<float4*>(acc_zero);
+  const bool vec = H % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(xq_sorted) & 15u) == 0;
+  if (vec && x_dtype == MOE_BF16)
+    return cudaLaunchKernelEx(&cfg, quantize_gather_x16_kernel<true>, x, T, H, K, inv_perm,
+                              xq_sorted, row_scale, acc4, status, cap);
+  if (vec)
+    return cudaLaunchKernelEx(&cfg, quantize_gather_x16_kernel<false>, x, T, H, K, inv_perm,
+                              xq_sorted, row_scale, acc4, status, cap);
   return cudaLaunchKernelEx(&cfg, quantize_gather_x_kernel, x, x_dtype == MOE_BF16 ? 1 : 0, T, H,
-                            K, inv_perm, xq_sorted, row_scale, reinterpret_cast<float4*>(acc_zero),
-                            status, cap);
+                            K, inv_perm, xq_sorted, row_scale, acc4, status, cap);
 }
 
 cudaError_t launch_combine_finish(const float* acc, int T, int H, int out_dtype, void* out,

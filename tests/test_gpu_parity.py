@@ -561,19 +561,21 @@ def test_gather_rows_bit_exact(dtype):
     assert (got[torch.from_numpy(~valid)] == 0).all()
 
 
-@pytest.mark.parametrize("T,H,K,E", [(2048, 2880, 4, 128), (37, 64, 2, 5)])
-def test_quantize_gather_x_fp8_bit_exact(T, H, K, E):
+@pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("T,H,K,E", [(2048, 2880, 4, 128), (37, 64, 2, 5), (19, 72, 3, 4)])
+def test_quantize_gather_x_fp8_bit_exact(T, H, K, E, xdt):
     """Codes at every sorted slot of a token equal the oracle's codes of that
-    token, bit for bit; the row scales too."""
+    token, bit for bit; the row scales too.  Rows of a multiple of 16
+    elements take the 16-element-run kernel, H = 72 the general one."""
     g = torch.Generator().manual_seed(T)
-    x = (torch.randn((T, H), generator=g) * 3).to(torch.bfloat16)
+    x = (torch.randn((T, H), generator=g) * 3).to(xdt)
     ids = pins.align_ids(T, K, E, "normal", seed=4)
     al = oracle.align(ids, E, 128)
     cap = len(al["sorted_ids"])
     xq_ref, s_ref = oracle.quantize_x_fp8(np_store(x))
     xs = torch.zeros((cap, H), dtype=torch.uint8, device="cuda")
     s = torch.empty(T, dtype=torch.float32, device="cuda")
-    moe.moe_quantize_gather_x_fp8(x.cuda(), moe.MOE_BF16, T, H, K,
+    moe.moe_quantize_gather_x_fp8(x.cuda(), moe.dtype_code(xdt), T, H, K,
                                   torch.from_numpy(al["inv_perm"]).cuda(), xs, s)
     torch.cuda.synchronize()
     valid = al["sorted_ids"] < T * K
