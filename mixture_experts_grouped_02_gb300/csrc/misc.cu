@@ -96,14 +96,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       } else if (splits == 1 && K <= kCombineBatch) {
         combine_group<OutT, 1>(y, inv_perm, T, K, H, t0, c, out, cap, status);
       } else {
+        // the splits of each assignment four loads at a time, added in
+        // split order (the decode shapes run up to 19 splits)
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = 0; k < K; ++k) {
           const long long row = inv_perm[static_cast<long long>(t0) * K + k];
           if (row < 0 || !in_bounds(row < cap, status)) continue;
-          for (int q = 0; q < splits; ++q)
-            add4(acc, __ldg(reinterpret_cast<const float4*>(
-                                y + (static_cast<long long>(q) * cap + row) * H) +
-                            c));
+          const float4* col = reinterpret_cast<const float4*>(y + row * H) + c;
+          const long long plane = cap * (H >> 2);  // float4s between splits
+          for (int q = 0; q < splits; q += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (q + j < splits) v[j] = __ldg(col + (q + j) * plane);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (q + j < splits) add4(acc, v[j]);
+          }
         }
         store_out4(out + static_cast<long long>(t0) * H, c, acc);
       }
