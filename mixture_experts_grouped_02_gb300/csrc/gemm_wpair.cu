@@ -24,6 +24,9 @@
 // Decode-like launches use the DUAL instantiation (WCfg): six stages of one
 // K step for large tiles, and for tiles of at most 32 tokens two K steps of
 // weights in the W and X slots with their 16-row token boxes in a T slot.
+// Gather mode (GemmArgs::gather, gate/up only): the token rows come straight
+// from x, four rows per tile::gather4 copy by the x row of each slot, in
+// place of the box of sorted rows; the shared-memory layout is the same.
 //  * gate/up: a CTA's 128 weight rows are 64 gate rows and the 64 up rows
 //    with the same indices j, so TMEM lanes 0-63 hold gate and 64-127 up of
 //    the same j for every token column.  The epilogue warp of lanes
