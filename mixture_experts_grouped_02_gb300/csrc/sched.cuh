@@ -14,8 +14,8 @@ namespace moe {
 // per band, and the blocks of one expert reuse a weight tile only while they
 // run in the same round of the persistent grid, which a wide band spreads
 // out.  Gate/up: with many weight tiles (Mixtral-shaped: 112) a band of 16
-// reads the token rows 7 times instead of 14 (DRAM traffic 1.43x -> 1.26x of
-// the algorithmic bytes, 1 % faster); with few (DeepSeek-V3-shaped: 16) a
+// reads the token rows 7 times instead of 14 (DRAM traffic 1.43x -> 1.26-1.32x
+// of the algorithmic bytes over three captures, 1 % faster); with few (DeepSeek-V3-shaped: 16) a
 // band of 8 measured faster.  Down: a band of 16 measured 1-3 % faster on
 // every shape.
 inline int gate_up_band(int n_tiles) {
