@@ -323,6 +323,51 @@ __device__ __forceinline__ void finish_pass(const AlignArgs& p, const int* s_cnt
   if (tid == 0) p.num_blocks[0] = nb;
 }
 
+// Batches of at most 32 assignments (decode steps): one warp reads the ids,
+// counts them per local expert and ranks each among the lower lanes with
+// the same expert (the stable order), then the whole CTA writes the offsets,
+// padding and descriptors with the passes above.  A few barriers instead of
+// the per-warp histograms' chain of passes: this CTA's time is its barriers
+// and memory round trips, not its arithmetic (measured 9.3 us for two ids).
+__device__ __forceinline__ void align_small(const AlignArgs& p, int key_bits, int* s_cnt,
+                                            int* s_pad, int* s_tmp, int* s_carry, int* s_bad) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int L = p.e_local, na = p.n_assign;
+  for (int x = tid; x < L; x += kAlignThreads) s_cnt[x] = 0;
+  __syncthreads();
+  int e = -1, rank = 0;
+  if (tid < 32) {
+    const int id = lane < na ? p.ids[lane] : -1;
+    const bool bad = lane < na && (id < 0 || id >= p.E);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) *s_bad = 1;
+    if (lane < na && !bad) e = id - p.e_base;  // local expert
+    if (e < 0 || e >= L) e = -1;               // another shard's expert: not listed here
+    const unsigned peers = peers_of(e + 1, key_bits);
+    rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && lane == __ffs(peers) - 1) s_cnt[e] = __popc(peers);
+  }
+  __syncthreads();
+  if (*s_bad) {
+    if (tid == 0) {
+      report_error(p.status, MOE_ERR_DEVICE_BAD_ID);
+      p.num_blocks[0] = 0;
+    }
+    return;
+  }
+  for (int x = tid; x < L; x += kAlignThreads) p.counts[x] = s_cnt[x];
+  offsets_pass(p, s_cnt, s_pad, s_tmp, s_carry);
+  if (tid < na) {
+    if (e >= 0) {
+      const int slot = s_pad[e] + rank;
+      p.sorted_ids[slot] = tid;
+      p.inv_perm[tid] = slot;
+    } else {
+      p.inv_perm[tid] = -1;
+    }
+  }
+  finish_pass(p, s_cnt, s_pad);
+}
+
 // ---------------------------------------------------------------- kernels
 
 // The whole align in one CTA of 32 warps (batches up to a few ten thousand
@@ -344,12 +389,17 @@ __global__ void __launch_bounds__(kAlignThreads, 1) align_kernel(const AlignArgs
   pdl_wait();  // ids written by the routing kernel, when it ran first
   pdl_launch_dependents();
   if (tid == 0) s_bad = 0;
-  for (int i = tid; i < kAlignWarps * L; i += kAlignThreads) hist[i] = 0;
+  if (na > 32)
+    for (int i = tid; i < kAlignWarps * L; i += kAlignThreads) hist[i] = 0;
   // 0. routing of small batches, in this CTA: a warp per token; the ids it
   //    writes are read back below after the barrier
   if (p.route.logits != nullptr)
     for (int t = warp; t < p.route.T; t += kAlignWarps) route_token(p.route, t, lane);
   __syncthreads();
+  if (na <= 32) {
+    align_small(p, key_bits, s_cnt, s_pad, s_tmp, s_carry, &s_bad);
+    return;
+  }
 
   // chunk of warp w: [w*chunk, min(na, (w+1)*chunk)), chunk a multiple of 32
   const int chunk = ((na + kAlignWarps - 1) / kAlignWarps + 31) & ~31;

@@ -63,7 +63,18 @@ def test_align_skewed_dsv3_routing():
 
 
 def test_align_bad_id_sets_status():
+    # 6 assignments: the one-warp path of small batches
     ids = torch.tensor([[0, 1], [2, 9], [3, 4]], dtype=torch.int32, device="cuda")
+    st = _status()
+    got = moe.align(ids, 8, 16, dev_status=st)
+    assert moe.moe_get_device_status(st) == _abi.MOE_ERR_DEVICE_BAD_ID
+    assert int(got["num_blocks"].item()) == 0
+
+
+def test_align_bad_id_sets_status_large_batch():
+    # 3000 assignments: the per-warp histograms of the single-CTA path
+    ids = torch.from_numpy(pins.align_ids(1500, 2, 8, "normal")).cuda()
+    ids[777, 1] = -2
     st = _status()
     got = moe.align(ids, 8, 16, dev_status=st)
     assert moe.moe_get_device_status(st) == _abi.MOE_ERR_DEVICE_BAD_ID
@@ -73,7 +84,8 @@ def test_align_bad_id_sets_status():
 @pytest.mark.parametrize("case,shard", [((300, 4, 16, 64, "skewed"), (0, 5)),
                                         ((37, 3, 8, 32, "normal"), (3, 4)),
                                         ((2000, 8, 256, 128, "normal"), (224, 32)),
-                                        ((64, 2, 8, 256, "normal"), (7, 1))])
+                                        ((64, 2, 8, 256, "normal"), (7, 1)),
+                                        ((12, 2, 16, 32, "normal"), (4, 6))])
 def test_align_local_bit_exact(case, shard):
     T, K, E, bm, kind = case
     base, L = shard
